@@ -1,0 +1,227 @@
+/*
+ * spg.h -- C ABI of the scaled-precision GEMM library for GB300 (sm_103a).
+ *
+ * The library computes the scaled low-precision linear-layer GEMM
+ *     Y[T, N] = epilogue( dequant(A) . dequant(W)^T )
+ * with fp32 accumulation in tensor memory and bf16 output, in two formats:
+ *   - FP8 E4M3 with one fp32 scale per activation row and per weight row
+ *     (ninfer PR #167, "The fp8 A8 GEMM stages its operands through TMA",
+ *     opening paragraph and "What actually changes");
+ *   - NVFP4: E2M1 codes, one E4M3 scale per 16 K-elements and one fp32
+ *     global scale per tensor (ninfer PR #160, "The NVFP4 TMA route reads
+ *     activation scales as one tile", body);
+ * plus a per-tensor-scaled FP8 GEMM in NT / NN / TN / TT layouts with batch
+ * strides (AstrAI commit log of csrc/kernels/fp8/gemm.cuh, first bullet).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is caller-owned DEVICE memory unless stated
+ *     otherwise.  Nothing is allocated by the library on any call.  Scales
+ *     (row, global, per-tensor) are device pointers, so no call reads a
+ *     value back to the host.
+ *   - Every call only enqueues work on `stream` (0 = the legacy default
+ *     stream) and returns; results are ready when the stream reaches them.
+ *   - Matrices are row-major with their natural leading dimension (no
+ *     padding) unless stated otherwise.  bf16 values are passed as raw
+ *     16-bit patterns (`void*`).
+ *   - All base pointers must be 16-byte aligned (SPG_ERR_MISALIGNED).
+ *   - Argument errors are detected on the host before any launch and leave
+ *     outputs untouched.  A launch failure returns SPG_ERR_CUDA.  Every wait
+ *     inside a kernel is bounded in time; a wait that runs out records a
+ *     code in the library's device error word, the kernel returns without
+ *     faulting, and spg_last_device_error() reports SPG_ERR_TIMEOUT.
+ *   - Empty problems (T == 0, N == 0, rows == 0, batch == 0) return SPG_OK
+ *     without launching anything.
+ */
+#ifndef SPG_H_
+#define SPG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPG_API __attribute__((visibility("default")))
+#else
+#define SPG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t. */
+typedef struct CUstream_st* spg_stream_t;
+
+typedef enum {
+  SPG_EPI_LINEAR = 0, /* Y = s * acc                                   */
+  SPG_EPI_ADD = 1,    /* Y = s * acc + residual   (linear_add)         */
+  SPG_EPI_SWIGLU = 2  /* Y[:, j] = silu(y[:, 2j]) * y[:, 2j+1]         */
+} spg_epilogue;
+
+typedef enum {
+  SPG_OK = 0,
+  SPG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum   */
+  SPG_ERR_UNSUPPORTED_SHAPE = 2, /* a divisibility rule below is broken     */
+  SPG_ERR_MISALIGNED = 3,        /* a base pointer is not 16-byte aligned   */
+  SPG_ERR_CUDA = 4,              /* a CUDA launch / driver call failed      */
+  SPG_ERR_TIMEOUT = 5            /* a bounded in-kernel wait ran out        */
+} spg_status;
+
+typedef enum {
+  SPG_KIND_FP8_ROWSCALED = 0,
+  SPG_KIND_NVFP4 = 1,
+  SPG_KIND_FP8_TENSOR = 2
+} spg_kind;
+
+/* One launch configuration picked by the route selector. */
+typedef struct {
+  int32_t kind;         /* spg_kind                                           */
+  int32_t block_m;      /* output rows per CTA tile (tcgen05 M)               */
+  int32_t block_n;      /* accumulator columns per CTA tile (tcgen05 N total) */
+  int32_t block_k;      /* K elements per pipeline stage                      */
+  int32_t stages;       /* shared-memory ring depth                           */
+  int32_t acc_buffers;  /* TMEM accumulator buffers (epilogue overlap)        */
+  int32_t group_m;      /* m-blocks per rasterization group                   */
+  int32_t grid;         /* persistent CTAs launched                           */
+  int64_t tiles;        /* output tiles of the whole problem (all batches)    */
+  int32_t smem_bytes;   /* dynamic shared memory per CTA                      */
+  int32_t variant;      /* kernel variant index inside the library            */
+} spg_route;
+
+/* Human-readable name of a status code (static string). */
+SPG_API const char* spg_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+SPG_API int spg_version(void);
+
+/* Bound, in nanoseconds, of every in-kernel wait of later launches
+ * (default 2e9).  Host-side setting; not thread-safe against concurrent
+ * launches. */
+SPG_API void spg_set_wait_timeout_ns(uint64_t ns);
+
+/* Synchronizes `stream`, then reads and clears the library's device error
+ * word.  Returns SPG_OK, SPG_ERR_TIMEOUT (a bounded wait ran out in some
+ * earlier launch) or SPG_ERR_CUDA (the stream reported an error). */
+SPG_API spg_status spg_last_device_error(spg_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Quantizers
+ * ------------------------------------------------------------------- */
+
+/* FP8 E4M3 row quantizer (activations at run time, weights once).
+ * For each row r of x [rows, K] (bf16):
+ *   amax = max_k |x[r,k]|;  s = amax / 448 (IEEE fp32; s = 1 when amax = 0);
+ *   codes[r,k] = E4M3(x[r,k] / s), round-to-nearest-even, saturating to
+ *   +-448, sign kept for values that round to zero;  scales[r] = s.
+ * ninfer PR #167, opening paragraph (row-scaled A8 activations) and
+ * "What actually changes".
+ * x: bf16 [rows, K]; codes: u8 [rows, K]; scales: fp32 [rows].
+ * Requires K % 8 == 0 and K > 0. */
+SPG_API spg_status spg_quantize_fp8_rows(const void* x, int64_t rows, int64_t K, uint8_t* codes,
+                                 float* scales, spg_stream_t stream);
+
+/* FP8 E4M3 per-tensor quantizer: one scale s = amax(x)/448 for all numel
+ * values (s = 1 when amax = 0), then the same code rule as above.
+ * AstrAI commit log of csrc/kernels/fp8/gemm.cuh, quantize bullets (amax
+ * scratch zeroed with a memset, codes plus a scale published on device).
+ * x: bf16 [numel]; codes: u8 [numel]; scale: fp32 [1] (device);
+ * amax_scratch: caller-owned device scratch of ONE fp32, overwritten.
+ * Requires numel % 8 == 0. */
+SPG_API spg_status spg_quantize_fp8_tensor(const void* x, int64_t numel, uint8_t* codes, float* scale,
+                                   float* amax_scratch, spg_stream_t stream);
+
+/* NVFP4 global scale g = amax(x) / (448 * 6) (g = 1 when amax = 0), written
+ * to the device scalar g.  The largest 16-element block scale of the tensor
+ * then encodes to the E4M3 maximum 448.  ninfer PR #160 body (an E4M3 scale
+ * per 16 elements) with one fp32 global scale per tensor.
+ * amax_scratch: caller-owned device scratch of ONE fp32, overwritten.
+ * Requires numel % 8 == 0. */
+SPG_API spg_status spg_nvfp4_global_scale(const void* x, int64_t numel, float* g, float* amax_scratch,
+                                  spg_stream_t stream);
+
+/* NVFP4 block quantizer.  For each 16-element block b of row r of x
+ * [rows, K] (bf16), with the device scalar g:
+ *   sf   = E4M3((amax_b / 6) / g)        (two IEEE fp32 divisions, RNE, satfinite)
+ *   d    = dec(sf) * g                   (IEEE fp32 multiply)
+ *   code = E2M1(x / d)  (RNE, satfinite, sign kept), or 0 when d == 0
+ * codes: u8 [rows, K/2], element 2i in the low nibble of byte i.
+ * sf: the blocked scale layout below, spg_nvfp4_sf_bytes(rows, K) bytes; the
+ * padding rows are written as zero.  ninfer PR #160 body: the quantizer writes
+ * the scale plane in the tile layout the GEMM loads as one TMA tile.
+ * Requires K % 64 == 0. */
+SPG_API spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K, const float* g,
+                              uint8_t* codes, uint8_t* sf, spg_stream_t stream);
+
+/* Bytes of the blocked NVFP4 scale layout for a [rows, K] operand:
+ * ceil(rows/128)*128 * ceil(K/64)*4.  Layout: the [rows, K/16] scale matrix
+ * is cut into tiles of 128 rows x 4 scales (512 bytes), stored tile row by
+ * tile row, K-tiles innermost; inside a tile the scale of (row r, column c)
+ * sits at byte (r % 32) * 16 + (r / 32) * 4 + c.  (Host function.) */
+SPG_API size_t spg_nvfp4_sf_bytes(int64_t rows, int64_t K);
+
+/* Byte offset of the scale of (row, 16-element block kb) in that layout
+ * (host function; -1 for out-of-range arguments). */
+SPG_API int64_t spg_nvfp4_sf_offset(int64_t row, int64_t kb, int64_t K);
+
+/* ---------------------------------------------------------------------
+ * GEMMs
+ * ------------------------------------------------------------------- */
+
+/* FP8 E4M3 row-scaled GEMM with a fused epilogue.
+ *   acc[t,n] = sum_k e4m3(A[t,k]) * e4m3(W[n,k])          (fp32, TMEM)
+ *   y[t,n]   = acc[t,n] * sa[t] * sw[n]
+ *   LINEAR: Y[t,n] = bf16(y);  ADD: Y[t,n] = bf16(y + residual[t,n]);
+ *   SWIGLU: Y[t,j] = bf16(silu(y[t,2j]) * y[t,2j+1]),  Y is [T, N/2].
+ * ninfer PR #167: opening paragraph (linear, linear_add, linear_swiglu call
+ * sites; same accumulator, scale application and epilogue on every route),
+ * review item "paired SwiGLU handling".
+ * A: u8 [T,K]; sa: fp32 [T]; W: u8 [N,K]; sw: fp32 [N];
+ * residual: bf16 [T,N] (ADD only, else may be NULL); Y: bf16 [T,N] or [T,N/2].
+ * Requires K % 16 == 0, K > 0, N % 8 == 0 (N % 16 == 0 for SWIGLU). */
+SPG_API spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, const uint8_t* W,
+                              const float* sw, const void* residual, void* Y, int64_t T,
+                              int64_t N, int64_t K, int epilogue, spg_stream_t stream);
+
+/* NVFP4 block-scaled GEMM with the same epilogues.
+ *   acc[t,n] = sum_k e2m1(A[t,k]) e4m3(sfA[t,k/16]) e2m1(W[n,k]) e4m3(sfW[n,k/16])
+ *   y[t,n]   = acc[t,n] * gA * gW, then the epilogue as above.
+ * ninfer PR #160 body (E2M1 codes, E4M3 scale per 16 elements, linear_add and
+ * the fused SwiGLU route).
+ * A: u8 [T, K/2] packed codes; sfA: blocked layout for (T, K); gA: fp32 [1];
+ * W: u8 [N, K/2]; sfW: blocked layout for (N, K); gW: fp32 [1];
+ * residual / Y as for the FP8 GEMM.
+ * Requires K % 256 == 0, N % 8 == 0 (N % 16 == 0 for SWIGLU). */
+SPG_API spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA, const uint8_t* W,
+                      const uint8_t* sfW, const float* gW, const void* residual, void* Y,
+                      int64_t T, int64_t N, int64_t K, int epilogue, spg_stream_t stream);
+
+/* Per-tensor-scaled FP8 E4M3 GEMM, bf16 out, batched.
+ *   C[b] = bf16( sA * sB * opA(A[b]) . opB(B[b]) ),  C[b] is [M, N]
+ * layout_a = 'N': A[b] is [M, K];   'T': A[b] is [K, M]  (opA = transpose)
+ * layout_b = 'T': B[b] is [N, K];   'N': B[b] is [K, N]
+ * so "NT" is the forward A.B^T, "NN" the dX product and "TN" the dW product
+ * of a linear layer (AstrAI commit log: layout tags, 3D operands).
+ * Matrix b of A starts at A + b*strideA elements (likewise B, C); a stride
+ * of 0 broadcasts one matrix over the batch (A and B only).
+ * sA, sB: fp32 [1] device scalars.
+ * Requires K % 16 == 0 for a K-major operand, M % 16 == 0 for a 'T' A,
+ * N % 16 == 0 for an 'N' B, N % 8 == 0, strides that are multiples of 16
+ * elements (C: of 8) and, for a non-zero stride, at least one matrix. */
+SPG_API spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batch, const uint8_t* A,
+                           int64_t strideA, const float* sA, const uint8_t* B, int64_t strideB,
+                           const float* sB, void* C, int64_t strideC, int64_t M, int64_t N,
+                           int64_t K, spg_stream_t stream);
+
+/* Per-shape tile / route selector (host only, no device query after the
+ * first call).  kind: spg_kind; T: rows of the output (M for the tensor
+ * GEMM).  Fills *out with the configuration the GEMM entry points would
+ * launch for this shape.  ninfer PR #167 "Routing" (a waves-times-work cost
+ * comparison) and the AstrAI dispatch-threshold bullets, re-derived for
+ * 152 SMs. */
+SPG_API spg_status spg_select_route(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
+                            int64_t batch, spg_route* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPG_H_ */

@@ -98,23 +98,26 @@ SPG_EXPORT double spg_oracle_e2m1_value(uint32_t code) {
 /* ------------------------------------------------------------------ */
 
 /* Round |x| to the nearest of the non-negative finite magnitudes held by
- * codes 0..max_code (ascending by code), ties to the even code.  Values
- * above the largest magnitude saturate to it. */
+ * codes 0..max_code (ascending by code, as both formats are), ties to the
+ * even code.  Values at or above the largest magnitude saturate to it.
+ * A binary search finds the neighbours c, c+1 with mags[c] <= |x| <
+ * mags[c+1]; the nearer one wins. */
 static uint32_t nearest_magnitude_code(double ax, const double* mags,
                                        uint32_t max_code) {
-  /* Saturate first: far above the grid every distance rounds to the same
-   * fp64 value and the nearest search alone would no longer decide. */
   if (ax >= mags[max_code]) return max_code;
-  uint32_t best = 0;
-  double best_d = fabs(ax - mags[0]);
-  for (uint32_t c = 1; c <= max_code; ++c) {
-    double d = fabs(ax - mags[c]);
-    if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) != 0)) {
-      best = c;
-      best_d = d;
-    }
+  if (ax <= mags[0]) return 0;
+  uint32_t lo = 0, hi = max_code; /* mags[lo] <= ax < mags[hi] */
+  while (hi - lo > 1) {
+    uint32_t mid = (lo + hi) / 2;
+    if (mags[mid] <= ax)
+      lo = mid;
+    else
+      hi = mid;
   }
-  return best;
+  double d_lo = ax - mags[lo], d_hi = mags[hi] - ax;
+  if (d_lo < d_hi) return lo;
+  if (d_hi < d_lo) return hi;
+  return (lo & 1u) == 0 ? lo : hi;
 }
 
 static double g_e4m3_mag[127];

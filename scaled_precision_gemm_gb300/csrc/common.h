@@ -1,0 +1,29 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "spg.h"
+
+namespace spg {
+
+// Device address of the library's error word on the current device (the
+// word every bounded in-kernel wait writes on time-out).  nullptr on failure.
+unsigned int* device_error_word();
+
+// Bound of every in-kernel wait, in nanoseconds.
+uint64_t wait_timeout_ns();
+
+// Streaming multiprocessors of the current device (queried once per device).
+int num_sms();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Map the last launch error to a status.
+inline spg_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? SPG_OK : SPG_ERR_CUDA;
+}
+
+}  // namespace spg

@@ -1,0 +1,50 @@
+// FP8 E4M3 row-scaled GEMM entry point (ninfer PR #167: the row-scaled A8
+// GEMM with linear / linear_add / linear_swiglu epilogues).
+#include "gemm_launch.cuh"
+
+using namespace spg;
+
+namespace {
+
+template <int EPI>
+spg_status dispatch_bn(int bn, const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  if (bn == 256) return launch_gemm_variant<kKindFp8, EPI, 256, 4, false, false, kScaleRow>(m, p, grid, s);
+  return launch_gemm_variant<kKindFp8, EPI, 128, 6, false, false, kScaleRow>(m, p, grid, s);
+}
+
+}  // namespace
+
+extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, const uint8_t* W,
+                                         const float* sw, const void* residual, void* Y,
+                                         int64_t T, int64_t N, int64_t K, int epilogue,
+                                         spg_stream_t stream) {
+  if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2) return SPG_ERR_INVALID_ARG;
+  if (T == 0 || N == 0) return SPG_OK;
+  if (!A || !sa || !W || !sw || !Y || (epilogue == SPG_EPI_ADD && !residual))
+    return SPG_ERR_INVALID_ARG;
+  if (K == 0 || K % 16 != 0 || N % 8 != 0 || (epilogue == SPG_EPI_SWIGLU && N % 16 != 0) ||
+      T > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(sa) || !aligned16(W) || !aligned16(sw) || !aligned16(Y) ||
+      (epilogue == SPG_EPI_ADD && !aligned16(residual)))
+    return SPG_ERR_MISALIGNED;
+
+  const spg_route r = select_route_internal(SPG_KIND_FP8_ROWSCALED, T, N, K, epilogue, 1);
+  const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
+  GemmMaps maps;
+  if (!make_tmap_3d(&maps.a, A, false, K, T, 1, K, K * T, 128, 128, 128) ||
+      !make_tmap_3d(&maps.b, W, false, K, N, 1, K, K * N, 128, r.block_n, 128) ||
+      !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
+    return SPG_ERR_CUDA;
+  GemmParams p;
+  fill_common_params(p, r, T, N, K, K, n_out, 1);
+  if (!p.err) return SPG_ERR_CUDA;
+  p.row_scale = sa;
+  p.col_scale = sw;
+  p.residual = static_cast<const __nv_bfloat16*>(residual);
+  switch (epilogue) {
+    case SPG_EPI_LINEAR: return dispatch_bn<SPG_EPI_LINEAR>(r.block_n, maps, p, r.grid, stream);
+    case SPG_EPI_ADD: return dispatch_bn<SPG_EPI_ADD>(r.block_n, maps, p, r.grid, stream);
+    default: return dispatch_bn<SPG_EPI_SWIGLU>(r.block_n, maps, p, r.grid, stream);
+  }
+}

@@ -1,0 +1,471 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   warp 0      TMA producer: fills a STAGES-deep shared-memory ring with
+//               128-byte-wide K slices of A and B (and, for NVFP4, the
+//               matching 128x4 scale tiles as single bulk copies).
+//   warp 1      TMEM owner and MMA issuer: one elected lane issues
+//               tcgen05.mma (kind::f8f6f4 for E4M3, kind::mxf4nvf4 block-scaled
+//               for NVFP4) into a double-buffered fp32 TMEM accumulator and
+//               releases ring slots with tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane = one
+//               output row per thread), apply the scales and the fused
+//               epilogue (linear / linear_add / linear_swiglu), stage the bf16
+//               tile in 64-byte-swizzled shared memory and write it with TMA
+//               stores, overlapping the next tile's main loop.
+//
+// The arithmetic is the same on every route and tile shape: per output
+// element one fp32 accumulation of the K products in the tensor core, then
+// y = acc * scale (row scales sa[t]*sw[n], or the scalar product of two
+// device scalars), then the epilogue and one bf16 rounding (ninfer PR #167,
+// opening paragraph: same accumulator, same scale application, same
+// epilogue and output policies on both routes).
+//
+// Every mbarrier wait is bounded in time; on time-out the kernel records a
+// code in the device error word and every role drains and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace spg {
+
+enum GemmKind : int { kKindFp8 = 0, kKindNvfp4 = 1 };
+enum ScaleMode : int { kScaleRow = 0, kScaleScalar = 1 };
+
+// Error codes written to the device error word (first one wins).
+enum : unsigned int {
+  kErrWaitEmpty = 0x101,
+  kErrWaitFull = 0x102,
+  kErrWaitAccEmpty = 0x103,
+  kErrWaitAccFull = 0x104,
+  kErrDrain = 0x105,
+};
+
+struct GemmParams {
+  int M;             // output rows (T)
+  int N;             // accumulator columns
+  int K;             // reduction length in elements
+  int n_out;         // output columns (N, or N/2 for SwiGLU)
+  int num_m_blocks;  // ceil(M / 128)
+  int num_n_blocks;  // ceil(N / BN)
+  int num_k_blocks;  // ceil(K_bytes / 128)
+  int tiles_per_batch;
+  int total_tiles;
+  int group_m;      // m-blocks per rasterization group
+  int a_batch_mul;  // 0 broadcasts A matrix 0 over the batch, else 1
+  int b_batch_mul;
+  const float* row_scale;  // kScaleRow: sa [M]
+  const float* col_scale;  // kScaleRow: sw [N]
+  const float* scalar_a;   // kScaleScalar: device scalars
+  const float* scalar_b;
+  const __nv_bfloat16* residual;  // SPG_EPI_ADD: [M, N] row-major
+  const uint8_t* sfa;             // NVFP4 scales, blocked layout
+  const uint8_t* sfb;
+  int sf_tiles_per_row_block;  // K / 64
+  uint64_t timeout_ns;
+  unsigned int* err;
+};
+
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+struct GemmCfg {
+  static constexpr int kBM = 128;
+  static constexpr int kBKBytes = 128;  // K bytes per stage (one 128-byte swizzle row)
+  static constexpr int kKSteps = 4;     // MMAs per stage, 32 bytes of K each
+  static constexpr int kABytes = kBM * kBKBytes;
+  static constexpr int kBBytes = BN * kBKBytes;
+  static constexpr int kNHalves = BN / 128;  // 128-row blocks of B (NVFP4 scale tiles)
+  static constexpr int kSfaBytes = KIND == kKindNvfp4 ? 4 * 512 : 0;
+  static constexpr int kSfbBytes = KIND == kKindNvfp4 ? kNHalves * 4 * 512 : 0;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kMmaN = KIND == kKindNvfp4 ? 128 : BN;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kSfColsPerKStep = KIND == kKindNvfp4 ? 4 + 4 * kNHalves : 0;
+  static constexpr int kSfColsPerStage = kKSteps * kSfColsPerKStep;
+  static constexpr int kTmemUsed = kAccBufs * BN + STAGES * kSfColsPerStage;
+  static constexpr int kTmemCols =
+      kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiBufBytes = 32 * 64;  // 32 rows x 32 bf16
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kThreads = 192;
+  static constexpr int kOutColsPerChunk = 32;
+  static constexpr int kAccColsPerChunk = EPI == SPG_EPI_SWIGLU ? 64 : 32;
+  static constexpr int kChunks = BN / kAccColsPerChunk;
+
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256, a multiple of 64");
+  static_assert(KIND != kKindNvfp4 || BN % 128 == 0, "NVFP4 tiles are whole 128-row scale blocks");
+  static_assert(kTmemUsed <= 512, "TMEM budget exceeded");
+  static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned (128B swizzle)");
+  static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+  static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(!(KIND == kKindNvfp4 && (A_MN || B_MN)), "NVFP4 operands are K-major");
+
+  // Instruction descriptor.
+  __host__ __device__ static constexpr uint32_t idesc() {
+    if constexpr (KIND == kKindFp8) {
+      // [4,6) D = f32; [7,10) A = E4M3 (0); [10,13) B = E4M3 (0);
+      // [15] A major; [16] B major; [17,23) N >> 3; [24,29) M >> 4.
+      return (1u << 4) | (uint32_t(A_MN) << 15) | (uint32_t(B_MN) << 16) |
+             (uint32_t(kMmaN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+    } else {
+      // Block-scaled: [4,6) B scale id 0; [7,10) A = E2M1 (1); [10,13) B = E2M1 (1);
+      // [17,23) N >> 3; [23] scale type UE4M3 (0); [24,29) M >> 4;
+      // [29,31) A scale id 0; [31] K = 64 (0).
+      return (1u << 7) | (1u << 10) | (uint32_t(kMmaN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+    }
+  }
+};
+
+struct TileCoord {
+  int b, mb, nb;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int tile, const GemmParams& p) {
+  TileCoord c;
+  c.b = tile / p.tiles_per_batch;
+  const int t = tile - c.b * p.tiles_per_batch;
+  const int span = p.group_m * p.num_n_blocks;
+  const int g = t / span;
+  const int first_m = g * p.group_m;
+  const int rem = p.num_m_blocks - first_m;
+  const int gsize = rem < p.group_m ? rem : p.group_m;
+  const int local = t - g * span;
+  c.mb = first_m + local % gsize;
+  c.nb = local / gsize;
+  return c;
+}
+
+// Drain-mode wait: bounded, but not cut short by the abort flag.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t timeout_ns, unsigned int* err) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 15u) == 15u && (globaltimer_ns() - t0 > timeout_ns || i > (1u << 30))) {
+      atomicCAS(err, 0u, kErrDrain);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+  using Cfg = GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* epi = smem + STAGES * Cfg::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + Cfg::kEpiBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], Cfg::kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmY);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl ctl{p.timeout_ns, p.err, abort_flag};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+        const TileCoord tc = tile_coord(tile, p);
+        const int m0 = tc.mb * Cfg::kBM;
+        const int n0 = tc.nb * BN;
+        const int za = tc.b * p.a_batch_mul;
+        const int zb = tc.b * p.b_batch_mul;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, ctl, kErrWaitEmpty)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = ring + s * Cfg::kStageBytes;
+          uint8_t* sb = sa + Cfg::kABytes;
+          mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+          const int kx = kb * Cfg::kBKBytes;
+          if constexpr (A_MN) {
+            tma_load_3d(sa, &tmA, &full[s], m0, kx, za);
+          } else {
+            tma_load_3d(sa, &tmA, &full[s], kx, m0, za);
+          }
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_3d(sb + h * 128 * Cfg::kBKBytes, &tmB, &full[s], n0 + h * 128, kx, zb);
+          } else {
+            tma_load_3d(sb, &tmB, &full[s], kx, n0, zb);
+          }
+          if constexpr (KIND == kKindNvfp4) {
+            uint8_t* ssfa = sb + Cfg::kBBytes;
+            uint8_t* ssfb = ssfa + Cfg::kSfaBytes;
+            const int64_t tpr = p.sf_tiles_per_row_block;
+            bulk_load(ssfa, p.sfa + (int64_t(tc.mb) * tpr + int64_t(kb) * 4) * 512, 2048, &full[s]);
+#pragma unroll
+            for (int h = 0; h < Cfg::kNHalves; ++h)
+              bulk_load(ssfb + h * 2048,
+                        p.sfb + ((int64_t(tc.nb) * Cfg::kNHalves + h) * tpr + int64_t(kb) * 4) * 512,
+                        2048, &full[s]);
+          }
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Wait (bounded) until every copy issued into the ring has landed, so
+      // no TMA write is in flight when the CTA leaves.
+      const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
+      for (uint32_t i = 0; i < outstanding; ++i) {
+        const uint32_t idx = issued - 1 - i;
+        mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.timeout_ns, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = Cfg::idesc();
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t acc_ph = (it >> 1) & 1;
+        if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(ring + s * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+          if constexpr (KIND == kKindNvfp4) {
+            const uint32_t ssfa = sb + Cfg::kBBytes;
+            const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+            const uint32_t sf_col0 =
+                tmem_base + uint32_t(Cfg::kAccBufs * BN + s * Cfg::kSfColsPerStage);
+#pragma unroll
+            for (int j = 0; j < Cfg::kKSteps; ++j) {
+              const uint32_t col = sf_col0 + uint32_t(j * Cfg::kSfColsPerKStep);
+              tc_cp_32x128b_warpx4(col, smem_desc(ssfa + j * 512, 0, 128, kSwizzleNone));
+#pragma unroll
+              for (int h = 0; h < Cfg::kNHalves; ++h)
+                tc_cp_32x128b_warpx4(col + 4 + 4 * h,
+                                     smem_desc(ssfb + h * 2048 + j * 512, 0, 128, kSwizzleNone));
+            }
+#pragma unroll
+            for (int j = 0; j < Cfg::kKSteps; ++j) {
+              const uint32_t col = sf_col0 + uint32_t(j * Cfg::kSfColsPerKStep);
+              const uint64_t adesc = smem_desc(sa + j * 32, 16, 1024, kSwizzle128B);
+#pragma unroll
+              for (int h = 0; h < Cfg::kNHalves; ++h) {
+                const uint64_t bdesc =
+                    smem_desc(sb + h * 128 * Cfg::kBKBytes + j * 32, 16, 1024, kSwizzle128B);
+                mma_nvf4(d_tmem + h * 128, adesc, bdesc, kIdesc, col, col + 4 + 4 * h,
+                         (kb | j) != 0);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cfg::kKSteps; ++j) {
+              uint64_t adesc, bdesc;
+              if constexpr (A_MN)
+                adesc = smem_desc(sa + j * 32 * 128, 128 * Cfg::kBKBytes, 1024, kSwizzle128B);
+              else
+                adesc = smem_desc(sa + j * 32, 16, 1024, kSwizzle128B);
+              if constexpr (B_MN)
+                bdesc = smem_desc(sb + j * 32 * 128, 128 * Cfg::kBKBytes, 1024, kSwizzle128B);
+              else
+                bdesc = smem_desc(sb + j * 32, 16, 1024, kSwizzle128B);
+              mma_f8f6f4(d_tmem, adesc, bdesc, kIdesc, (kb | j) != 0);
+            }
+          }
+          tc_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+      }
+      // All MMAs (and scale copies) must be complete before TMEM is freed.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.err);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int e = warp - 2;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_local = q * 32 + lane;
+    uint8_t* stage0 = epi + (e * 2) * Cfg::kEpiBufBytes;
+    int it = 0;
+    int chunk_ctr = 0;
+    float scalar = 1.f;
+    if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t acc_ph = (it >> 1) & 1;
+      if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
+      tc_fence_after();
+      const TileCoord tc = tile_coord(tile, p);
+      const int m0 = tc.mb * Cfg::kBM;
+      const int n0 = tc.nb * BN;
+      const int m = m0 + r_local;
+      const bool row_ok = m < p.M;
+      float row_s = scalar;
+      if constexpr (SCALE == kScaleRow) row_s = row_ok ? __ldg(p.row_scale + m) : 0.f;
+      const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+      const bool have_k = p.num_k_blocks > 0;
+
+#pragma unroll 1
+      for (int c = 0; c < Cfg::kChunks; ++c, ++chunk_ctr) {
+        const int acc_c0 = c * Cfg::kAccColsPerChunk;  // first accumulator column
+        uint32_t raw[Cfg::kAccColsPerChunk];
+        if (have_k) {
+          tmem_ld_32x32b_x32(t_row + acc_c0, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
+          if constexpr (Cfg::kAccColsPerChunk == 64)
+            tmem_ld_32x32b_x32(t_row + acc_c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < Cfg::kAccColsPerChunk; ++i) raw[i] = 0u;
+        }
+        if (c == Cfg::kChunks - 1) {
+          // The whole accumulator buffer has been read: hand it back.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        float v[Cfg::kAccColsPerChunk];
+#pragma unroll
+        for (int i = 0; i < Cfg::kAccColsPerChunk; ++i) v[i] = __uint_as_float(raw[i]);
+        const int n_c0 = n0 + acc_c0;  // first accumulator column of the chunk (global)
+        if constexpr (SCALE == kScaleRow) {
+#pragma unroll
+          for (int i = 0; i < Cfg::kAccColsPerChunk; i += 4) {
+            float4 sw = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (n_c0 + i < p.N) sw = __ldg(reinterpret_cast<const float4*>(p.col_scale + n_c0 + i));
+            v[i + 0] *= row_s * sw.x;
+            v[i + 1] *= row_s * sw.y;
+            v[i + 2] *= row_s * sw.z;
+            v[i + 3] *= row_s * sw.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < Cfg::kAccColsPerChunk; ++i) v[i] *= scalar;
+        }
+        float o[32];
+        if constexpr (EPI == SPG_EPI_SWIGLU) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float gate = v[2 * j], up = v[2 * j + 1];
+            o[j] = gate / (1.f + __expf(-gate)) * up;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = v[j];
+          if constexpr (EPI == SPG_EPI_ADD) {
+            if (row_ok) {
+              const uint4* rp = reinterpret_cast<const uint4*>(p.residual + int64_t(m) * p.N + n_c0);
+#pragma unroll
+              for (int g8 = 0; g8 < 4; ++g8) {
+                if (n_c0 + g8 * 8 < p.N) {
+                  const uint4 rv = __ldg(rp + g8);
+                  const uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                  for (int h = 0; h < 4; ++h) {
+                    o[g8 * 8 + 2 * h] += __uint_as_float(w[h] << 16);
+                    o[g8 * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xFFFF0000u);
+                  }
+                }
+              }
+            }
+          }
+        }
+        // Stage the 32 x 32 bf16 block (64-byte swizzle) and TMA-store it.
+        uint8_t* sbuf = stage0 + (chunk_ctr & 1) * Cfg::kEpiBufBytes;
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint4 pk;
+          pk.x = pack_bf16x2(o[jj * 8 + 0], o[jj * 8 + 1]);
+          pk.y = pack_bf16x2(o[jj * 8 + 2], o[jj * 8 + 3]);
+          pk.z = pack_bf16x2(o[jj * 8 + 4], o[jj * 8 + 5]);
+          pk.w = pack_bf16x2(o[jj * 8 + 6], o[jj * 8 + 7]);
+          const int phys = jj ^ ((lane >> 1) & 3);
+          *reinterpret_cast<uint4*>(sbuf + lane * 64 + phys * 16) = pk;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int out_x = (EPI == SPG_EPI_SWIGLU ? n0 / 2 : n0) + c * Cfg::kOutColsPerChunk;
+        const int out_y = m0 + q * 32;
+        if (lane == 0 && out_y < p.M && out_x < p.n_out) {
+          tma_store_3d(&tmY, sbuf, out_x, out_y, tc.b);
+        }
+        if (lane == 0) bulk_commit();
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+}  // namespace spg

@@ -1,0 +1,65 @@
+// Launch helper shared by the GEMM entry points: one function per compiled
+// kernel variant, setting the dynamic shared-memory limit once per device.
+#pragma once
+
+#include <atomic>
+
+#include "gemm_kernel.cuh"
+#include "host.h"
+
+namespace spg {
+
+struct GemmMaps {
+  CUtensorMap a, b, y;
+};
+
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+spg_status launch_gemm_variant(const GemmMaps& maps, const GemmParams& p, int grid,
+                               cudaStream_t stream) {
+  using Cfg = GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  auto kern = gemm_kernel<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmemBytes) != cudaSuccess)
+      return SPG_ERR_CUDA;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(maps.a, maps.b, maps.y, p);
+  return launch_status();
+}
+
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+constexpr int variant_smem() {
+  return GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE>::kSmemBytes;
+}
+
+// Fill the parts of GemmParams every entry point shares.
+inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int64_t N,
+                               int64_t K_bytes, int64_t K, int64_t n_out, int64_t batch) {
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.n_out = static_cast<int>(n_out);
+  p.num_m_blocks = static_cast<int>((M + 127) / 128);
+  p.num_n_blocks = static_cast<int>((N + r.block_n - 1) / r.block_n);
+  p.num_k_blocks = static_cast<int>((K_bytes + 127) / 128);
+  p.tiles_per_batch = p.num_m_blocks * p.num_n_blocks;
+  p.total_tiles = static_cast<int>(p.tiles_per_batch * batch);
+  p.group_m = r.group_m;
+  p.a_batch_mul = 0;
+  p.b_batch_mul = 0;
+  p.row_scale = p.col_scale = p.scalar_a = p.scalar_b = nullptr;
+  p.residual = nullptr;
+  p.sfa = p.sfb = nullptr;
+  p.sf_tiles_per_row_block = 0;
+  p.timeout_ns = wait_timeout_ns();
+  p.err = device_error_word();
+}
+
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+}  // namespace spg

@@ -1,0 +1,54 @@
+// NVFP4 block-scaled GEMM entry point (ninfer PR #160: E2M1 codes with an
+// E4M3 scale per 16 elements, scale tiles loaded whole, linear_add and the
+// fused SwiGLU route).
+#include "gemm_launch.cuh"
+
+using namespace spg;
+
+namespace {
+
+template <int EPI>
+spg_status launch(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm_variant<kKindNvfp4, EPI, 128, 5, false, false, kScaleScalar>(m, p, grid, s);
+}
+
+}  // namespace
+
+extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                 const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                 const void* residual, void* Y, int64_t T, int64_t N, int64_t K,
+                                 int epilogue, spg_stream_t stream) {
+  if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2) return SPG_ERR_INVALID_ARG;
+  if (T == 0 || N == 0) return SPG_OK;
+  if (!A || !sfA || !gA || !W || !sfW || !gW || !Y || (epilogue == SPG_EPI_ADD && !residual))
+    return SPG_ERR_INVALID_ARG;
+  if (K == 0 || K % 256 != 0 || N % 8 != 0 || (epilogue == SPG_EPI_SWIGLU && N % 16 != 0) ||
+      T > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(sfA) || !aligned16(gA) || !aligned16(W) || !aligned16(sfW) ||
+      !aligned16(gW) || !aligned16(Y) || (epilogue == SPG_EPI_ADD && !aligned16(residual)))
+    return SPG_ERR_MISALIGNED;
+
+  const spg_route r = select_route_internal(SPG_KIND_NVFP4, T, N, K, epilogue, 1);
+  const int64_t kh = K / 2;
+  const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
+  GemmMaps maps;
+  if (!make_tmap_3d(&maps.a, A, false, kh, T, 1, kh, kh * T, 128, 128, 128) ||
+      !make_tmap_3d(&maps.b, W, false, kh, N, 1, kh, kh * N, 128, r.block_n, 128) ||
+      !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
+    return SPG_ERR_CUDA;
+  GemmParams p;
+  fill_common_params(p, r, T, N, kh, K, n_out, 1);
+  if (!p.err) return SPG_ERR_CUDA;
+  p.scalar_a = gA;
+  p.scalar_b = gW;
+  p.residual = static_cast<const __nv_bfloat16*>(residual);
+  p.sfa = sfA;
+  p.sfb = sfW;
+  p.sf_tiles_per_row_block = static_cast<int>(K / 64);
+  switch (epilogue) {
+    case SPG_EPI_LINEAR: return launch<SPG_EPI_LINEAR>(maps, p, r.grid, stream);
+    case SPG_EPI_ADD: return launch<SPG_EPI_ADD>(maps, p, r.grid, stream);
+    default: return launch<SPG_EPI_SWIGLU>(maps, p, r.grid, stream);
+  }
+}

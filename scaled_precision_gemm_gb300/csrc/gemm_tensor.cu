@@ -1,0 +1,77 @@
+// Per-tensor-scaled FP8 GEMM entry point, NT / NN / TN / TT, batched
+// (AstrAI commit log of csrc/kernels/fp8/gemm.cuh: layout tags instead of
+// copies, batch strides with stride 0 broadcasting, bf16 output).
+// Non-K-major operands are read as MN-major shared-memory tiles, which the
+// tensor core consumes directly (no transpose pass).
+#include "gemm_launch.cuh"
+
+using namespace spg;
+
+namespace {
+
+template <bool A_MN, bool B_MN>
+spg_status dispatch_bn(int bn, const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  if (bn == 256)
+    return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 256, 4, A_MN, B_MN, kScaleScalar>(m, p, grid, s);
+  return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 128, 6, A_MN, B_MN, kScaleScalar>(m, p, grid, s);
+}
+
+}  // namespace
+
+extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batch,
+                                      const uint8_t* A, int64_t strideA, const float* sA,
+                                      const uint8_t* B, int64_t strideB, const float* sB, void* C,
+                                      int64_t strideC, int64_t M, int64_t N, int64_t K,
+                                      spg_stream_t stream) {
+  if ((layout_a != 'N' && layout_a != 'T') || (layout_b != 'N' && layout_b != 'T'))
+    return SPG_ERR_INVALID_ARG;
+  if (batch < 0 || M < 0 || N < 0 || K < 0 || strideA < 0 || strideB < 0 || strideC < 0)
+    return SPG_ERR_INVALID_ARG;
+  if (batch == 0 || M == 0 || N == 0) return SPG_OK;
+  if (!A || !B || !C || !sA || !sB) return SPG_ERR_INVALID_ARG;
+  const bool a_mn = layout_a == 'T';
+  const bool b_mn = layout_b == 'N';
+  if (K == 0 || K % 16 != 0 || N % 8 != 0 || (a_mn && M % 16 != 0) || (b_mn && N % 16 != 0) ||
+      M > kMaxDim || N > kMaxDim || K > kMaxDim || batch > 65535)
+    return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (batch > 1) {
+    if (strideA % 16 != 0 || strideB % 16 != 0 || strideC % 8 != 0 || strideC < M * N ||
+        (strideA != 0 && strideA < M * K) || (strideB != 0 && strideB < N * K))
+      return SPG_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA) || !aligned16(sB))
+    return SPG_ERR_MISALIGNED;
+
+  const spg_route r = select_route_internal(SPG_KIND_FP8_TENSOR, M, N, K, SPG_EPI_LINEAR, batch);
+  const bool a_batched = batch > 1 && strideA != 0;
+  const bool b_batched = batch > 1 && strideB != 0;
+  const int64_t nba = a_batched ? batch : 1, nbb = b_batched ? batch : 1;
+  GemmMaps maps;
+  bool ok;
+  if (a_mn)
+    ok = make_tmap_3d(&maps.a, A, false, M, K, nba, M, a_batched ? strideA : M * K, 128, 128, 128);
+  else
+    ok = make_tmap_3d(&maps.a, A, false, K, M, nba, K, a_batched ? strideA : M * K, 128, 128, 128);
+  if (ok) {
+    if (b_mn)
+      ok = make_tmap_3d(&maps.b, B, false, N, K, nbb, N, b_batched ? strideB : N * K, 128, 128, 128);
+    else
+      ok = make_tmap_3d(&maps.b, B, false, K, N, nbb, K, b_batched ? strideB : N * K, 128,
+                        r.block_n, 128);
+  }
+  if (ok)
+    ok = make_tmap_3d(&maps.y, C, true, N, M, batch, N * 2, (batch > 1 ? strideC : M * N) * 2, 32,
+                      32, 64);
+  if (!ok) return SPG_ERR_CUDA;
+  GemmParams p;
+  fill_common_params(p, r, M, N, K, K, N, batch);
+  if (!p.err) return SPG_ERR_CUDA;
+  p.a_batch_mul = a_batched ? 1 : 0;
+  p.b_batch_mul = b_batched ? 1 : 0;
+  p.scalar_a = sA;
+  p.scalar_b = sB;
+  if (!a_mn && !b_mn) return dispatch_bn<false, false>(r.block_n, maps, p, r.grid, stream);
+  if (!a_mn && b_mn) return dispatch_bn<false, true>(r.block_n, maps, p, r.grid, stream);
+  if (a_mn && !b_mn) return dispatch_bn<true, false>(r.block_n, maps, p, r.grid, stream);
+  return dispatch_bn<true, true>(r.block_n, maps, p, r.grid, stream);
+}

@@ -1,0 +1,22 @@
+// Host-side helpers shared by the GEMM launchers.
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "spg.h"
+
+namespace spg {
+
+// Encode a 3-D tiled TMA descriptor (uint8 or bf16 elements).  d0 is the
+// contiguous dimension; strides are in bytes; the box is box0 x box1 x 1.
+bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                  uint32_t box1, int swizzle_bytes);
+
+// The selector behind spg_select_route (no validation).
+spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
+                                int64_t batch);
+
+}  // namespace spg

@@ -1,0 +1,270 @@
+// Activation / weight quantizers: bf16 -> E4M3 codes with row or tensor
+// scales, and bf16 -> NVFP4 (E2M1 codes, E4M3 block-16 scales in the blocked
+// tile layout, fp32 global scale).
+//
+// All of them are HBM-bound streaming kernels: 16-byte vector loads of the
+// bf16 input, every fp32 step as one IEEE-rounded operation (__fdiv_rn,
+// __fmul_rn) so that codes and scales are bit-for-bit those of the plain
+// definition, and hardware cvt.rn.satfinite conversions for the codes.
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace spg {
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kRowRegVecs = 9;  // 16-byte vectors per thread kept in registers
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float vec_amax(const uint4& v) {
+  float a = 0.f;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  return a;
+}
+
+// Eight bf16 divided by s (IEEE) -> eight E4M3 codes.
+__device__ __forceinline__ uint2 vec_encode_e4m3(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c[i] = cvt_e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int THREADS>
+__device__ __forceinline__ float block_max(float v, float* red) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = (threadIdx.x < THREADS / 32) ? red[threadIdx.x] : 0.f;
+  if (w == 0) r = warp_max(r);
+  if (threadIdx.x == 0) red[0] = r;
+  __syncthreads();
+  r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// One CTA per row: amax over the row, s = amax/448, codes = E4M3(x/s).
+__global__ void __launch_bounds__(kRowThreads) quantize_fp8_rows_kernel(
+    const uint4* __restrict__ x, int64_t K, uint2* __restrict__ codes, float* __restrict__ scales) {
+  __shared__ float red[kRowThreads / 32];
+  const int64_t row = blockIdx.x;
+  const int64_t nvec = K / 8;
+  const uint4* xr = x + row * nvec;
+  uint2* cr = codes + row * nvec;
+  uint4 cache[kRowRegVecs];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowRegVecs; ++j) {
+    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRowThreads;
+    if (i < nvec) {
+      cache[j] = __ldg(xr + i);
+      amax = fmaxf(amax, vec_amax(cache[j]));
+    }
+  }
+  for (int64_t i = threadIdx.x + int64_t(kRowRegVecs) * kRowThreads; i < nvec; i += kRowThreads)
+    amax = fmaxf(amax, vec_amax(__ldg(xr + i)));
+  amax = block_max<kRowThreads>(amax, red);
+  const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+#pragma unroll
+  for (int j = 0; j < kRowRegVecs; ++j) {
+    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRowThreads;
+    if (i < nvec) cr[i] = vec_encode_e4m3(cache[j], s);
+  }
+  for (int64_t i = threadIdx.x + int64_t(kRowRegVecs) * kRowThreads; i < nvec; i += kRowThreads)
+    cr[i] = vec_encode_e4m3(__ldg(xr + i), s);
+  if (threadIdx.x == 0) scales[row] = s;
+}
+
+// amax over a whole tensor into *amax (which the host zeroes first).
+// Non-negative floats order like their bit patterns, so an unsigned
+// atomicMax on the bits is a float max.
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                   float* __restrict__ amax) {
+  __shared__ float red[8];
+  float a = 0.f;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
+       i += int64_t(gridDim.x) * blockDim.x)
+    a = fmaxf(a, vec_amax(__ldg(x + i)));
+  a = block_max<256>(a, red);
+  if (threadIdx.x == 0 && a > 0.f)
+    atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(a));
+}
+
+// Per-tensor E4M3 encode with s = amax/448 (1 when amax = 0).
+__global__ void __launch_bounds__(256) encode_fp8_tensor_kernel(const uint4* __restrict__ x,
+                                                                int64_t nvec,
+                                                                const float* __restrict__ amax,
+                                                                uint2* __restrict__ codes,
+                                                                float* __restrict__ scale) {
+  const float a = *amax;
+  const float s = (a == 0.f) ? 1.f : __fdiv_rn(a, 448.f);
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
+       i += int64_t(gridDim.x) * blockDim.x)
+    codes[i] = vec_encode_e4m3(__ldg(x + i), s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+}
+
+// g = amax / (448 * 6), 1 when amax = 0.
+__global__ void nvfp4_global_finalize_kernel(const float* __restrict__ amax, float* __restrict__ g) {
+  const float a = *amax;
+  *g = (a == 0.f) ? 1.f : __fdiv_rn(a, 2688.f);
+}
+
+// NVFP4 block quantizer.  One thread per 64 consecutive elements of a row
+// (four 16-element blocks, so one 32-bit word of scales).  Threads past the
+// last row write the zero scales of the padding rows of the blocked layout.
+__global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
+    const uint4* __restrict__ x, int64_t rows, int64_t rows_pad, int64_t K,
+    const float* __restrict__ gptr, uint4* __restrict__ codes, uint32_t* __restrict__ sf) {
+  const int64_t units_per_row = K / 64;
+  const int64_t u = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (u >= rows_pad * units_per_row) return;
+  const int64_t r = u / units_per_row;
+  const int64_t cb = u - r * units_per_row;  // 64-element group = scale-tile column
+  const int64_t sf_word = ((r >> 7) * units_per_row + cb) * 128 + (r & 31) * 4 + ((r >> 5) & 3);
+  if (r >= rows) {
+    sf[sf_word] = 0u;
+    return;
+  }
+  const float g = *gptr;
+  const uint4* xp = x + (r * K + cb * 64) / 8;
+  uint32_t sf_bytes = 0;
+  uint4 out[2];
+  uint32_t* ow = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint4 v0 = __ldg(xp + 2 * b), v1 = __ldg(xp + 2 * b + 1);
+    const float amax_b = fmaxf(vec_amax(v0), vec_amax(v1));
+    const float t = __fdiv_rn(__fdiv_rn(amax_b, 6.f), g);
+    const uint32_t sfc = cvt_e4m3x2(t, t) & 0xFFu;
+    sf_bytes |= sfc << (8 * b);
+    const float2 dec = e4m3x2_to_float2(static_cast<uint16_t>(sfc));  // one byte is zero
+    const float d = __fmul_rn(fmaxf(dec.x, dec.y), g);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
+      q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
+    }
+    const float(&q0)[8] = *reinterpret_cast<const float(*)[8]>(&q[0]);
+    const float(&q1)[8] = *reinterpret_cast<const float(*)[8]>(&q[8]);
+    ow[2 * b] = cvt_e2m1x8(q0);
+    ow[2 * b + 1] = cvt_e2m1x8(q1);
+  }
+  uint4* cp = codes + (r * (K / 2) + cb * 32) / 16;
+  cp[0] = out[0];
+  cp[1] = out[1];
+  sf[sf_word] = sf_bytes;
+}
+
+int grid_for(int64_t work, int threads) {
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  int64_t g = (work + threads - 1) / threads;
+  if (g > cap) g = cap;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+}  // namespace spg
+
+using namespace spg;
+
+extern "C" spg_status spg_quantize_fp8_rows(const void* x, int64_t rows, int64_t K,
+                                            uint8_t* codes, float* scales, spg_stream_t stream) {
+  if (rows < 0 || K < 0) return SPG_ERR_INVALID_ARG;
+  if (rows == 0) return SPG_OK;
+  if (!x || !codes || !scales) return SPG_ERR_INVALID_ARG;
+  if (K == 0 || K % 8 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (rows > 0x7FFFFFFF) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return SPG_ERR_MISALIGNED;
+  quantize_fp8_rows_kernel<<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(
+      static_cast<const uint4*>(x), K, reinterpret_cast<uint2*>(codes), scales);
+  return launch_status();
+}
+
+extern "C" spg_status spg_quantize_fp8_tensor(const void* x, int64_t numel, uint8_t* codes,
+                                              float* scale, float* amax_scratch,
+                                              spg_stream_t stream) {
+  if (numel < 0) return SPG_ERR_INVALID_ARG;
+  if (!scale || !amax_scratch) return SPG_ERR_INVALID_ARG;
+  if (numel > 0 && (!x || !codes)) return SPG_ERR_INVALID_ARG;
+  if (numel % 8 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if ((numel > 0 && (!aligned16(x) || !aligned16(codes))) || !aligned16(scale) ||
+      !aligned16(amax_scratch))
+    return SPG_ERR_MISALIGNED;
+  const int64_t nvec = numel / 8;
+  if (cudaMemsetAsync(amax_scratch, 0, sizeof(float), stream) != cudaSuccess) return SPG_ERR_CUDA;
+  if (nvec > 0) {
+    amax_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(static_cast<const uint4*>(x), nvec,
+                                                          amax_scratch);
+    if (launch_status() != SPG_OK) return SPG_ERR_CUDA;
+  }
+  encode_fp8_tensor_kernel<<<grid_for(nvec > 0 ? nvec : 1, 256), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), nvec, amax_scratch, reinterpret_cast<uint2*>(codes), scale);
+  return launch_status();
+}
+
+extern "C" spg_status spg_nvfp4_global_scale(const void* x, int64_t numel, float* g,
+                                             float* amax_scratch, spg_stream_t stream) {
+  if (numel < 0 || !g || !amax_scratch) return SPG_ERR_INVALID_ARG;
+  if (numel > 0 && !x) return SPG_ERR_INVALID_ARG;
+  if (numel % 8 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if ((numel > 0 && !aligned16(x)) || !aligned16(g) || !aligned16(amax_scratch))
+    return SPG_ERR_MISALIGNED;
+  const int64_t nvec = numel / 8;
+  if (cudaMemsetAsync(amax_scratch, 0, sizeof(float), stream) != cudaSuccess) return SPG_ERR_CUDA;
+  if (nvec > 0) {
+    amax_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(static_cast<const uint4*>(x), nvec,
+                                                          amax_scratch);
+    if (launch_status() != SPG_OK) return SPG_ERR_CUDA;
+  }
+  nvfp4_global_finalize_kernel<<<1, 1, 0, stream>>>(amax_scratch, g);
+  return launch_status();
+}
+
+extern "C" spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K, const float* g,
+                                         uint8_t* codes, uint8_t* sf, spg_stream_t stream) {
+  if (rows < 0 || K < 0) return SPG_ERR_INVALID_ARG;
+  if (rows == 0) return SPG_OK;
+  if (!x || !g || !codes || !sf) return SPG_ERR_INVALID_ARG;
+  if (K == 0 || K % 64 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || !aligned16(g))
+    return SPG_ERR_MISALIGNED;
+  const int64_t rows_pad = (rows + 127) / 128 * 128;
+  const int64_t units = rows_pad * (K / 64);
+  const int64_t blocks = (units + 255) / 256;
+  if (blocks > 0x7FFFFFFF) return SPG_ERR_UNSUPPORTED_SHAPE;
+  quantize_nvfp4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), rows, rows_pad, K, g, reinterpret_cast<uint4*>(codes),
+      reinterpret_cast<uint32_t*>(sf));
+  return launch_status();
+}
+
+extern "C" size_t spg_nvfp4_sf_bytes(int64_t rows, int64_t K) {
+  if (rows <= 0 || K <= 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>((K + 63) / 64 * 4);
+}
+
+extern "C" int64_t spg_nvfp4_sf_offset(int64_t row, int64_t kb, int64_t K) {
+  if (row < 0 || kb < 0 || K <= 0 || kb >= (K + 15) / 16) return -1;
+  const int64_t tiles_per_row_block = (K + 63) / 64;
+  return ((row / 128) * tiles_per_row_block + kb / 4) * 512 + (row % 32) * 16 +
+         ((row % 128) / 32) * 4 + (kb % 4);
+}

@@ -1,0 +1,115 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-only
+logic (status strings, scale-layout arithmetic, route selector, argument
+validation that returns before any launch) behaves as the header states.
+No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import scaled_precision_gemm_gb300 as spg
+from tests.helpers import sf_blocked_to_rowmajor, sf_rowmajor_to_blocked
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from scaled_precision_gemm_gb300 import build
+    build.build()
+    return spg.load_library()
+
+
+def declared_symbols():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^SPG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert spg.status_string(0) == "SPG_OK"
+    assert spg.status_string(5) == "SPG_ERR_TIMEOUT"
+    assert spg.status_string(99) == "SPG_ERR_UNKNOWN"
+    assert lib.spg_version() >= 100
+
+
+@pytest.mark.parametrize("rows,K", [(1, 64), (128, 256), (129, 17408), (300, 5120), (64, 320)])
+def test_sf_layout_matches_definition(lib, rows, K):
+    assert spg.nvfp4_sf_bytes(rows, K) == ((rows + 127) // 128 * 128) * ((K + 63) // 64 * 4)
+    rng = np.random.default_rng(rows + K)
+    sf = rng.integers(0, 0x7F, size=(rows, K // 16), dtype=np.uint8)
+    blocked = sf_rowmajor_to_blocked(sf, rows, K)
+    assert blocked.size == spg.nvfp4_sf_bytes(rows, K)
+    for r in {0, rows - 1, rows // 2, min(rows - 1, 37)}:
+        for kb in {0, K // 16 - 1, (K // 16) // 2}:
+            assert blocked[spg.nvfp4_sf_offset(r, kb, K)] == sf[r, kb]
+    assert np.array_equal(sf_blocked_to_rowmajor(blocked, rows, K), sf)
+    # every (row, kb) maps to a distinct byte
+    offs = {spg.nvfp4_sf_offset(r, kb, K) for r in range(min(rows, 130)) for kb in range(K // 16)}
+    assert len(offs) == min(rows, 130) * (K // 16)
+    assert spg.nvfp4_sf_offset(-1, 0, K) == -1 and spg.nvfp4_sf_offset(0, K // 16, K) == -1
+
+
+def test_route_selector(lib):
+    r = spg.select_route("fp8_rowscaled", 4096, 5120, 17408, "add")
+    assert r["block_m"] == 128 and r["block_n"] in (128, 256)
+    assert r["tiles"] == 32 * (5120 // r["block_n"])
+    assert 1 <= r["grid"] <= r["tiles"]
+    small = spg.select_route("fp8_rowscaled", 64, 128, 256, "linear")
+    assert small["tiles"] == 1 and small["grid"] == 1
+    nv = spg.select_route("nvfp4", 256, 5120, 17408, "add")
+    assert nv["block_n"] == 128 and nv["tiles"] == 2 * 40
+    b = spg.select_route("fp8_tensor", 512, 512, 512, "linear", batch=64)
+    assert b["tiles"] % 64 == 0
+    with pytest.raises(spg.SpgError):
+        spg.select_route(7, 1, 1, 1)
+
+
+def _vp(x):
+    return ctypes.c_void_p(x)
+
+
+def test_argument_validation_before_launch(lib):
+    A, Wt, Y = _vp(0x10000), _vp(0x20000), _vp(0x30000)
+    sa, sw = _vp(0x40000), _vp(0x50000)
+    f = lib.fp8_rowscaled_gemm
+    assert f(A, sa, Wt, sw, None, Y, -1, 8, 16, 0, None) == 1
+    assert f(A, sa, Wt, sw, None, Y, 4, 8, 16, 3, None) == 1
+    assert f(A, sa, Wt, sw, None, Y, 0, 8, 16, 0, None) == 0          # empty: no-op
+    assert f(None, sa, Wt, sw, None, Y, 4, 8, 16, 0, None) == 1
+    assert f(A, sa, Wt, sw, None, Y, 4, 8, 24, 0, None) == 2          # K % 16
+    assert f(A, sa, Wt, sw, None, Y, 4, 12, 16, 0, None) == 2         # N % 8
+    assert f(A, sa, Wt, sw, None, Y, 4, 24, 16, 2, None) == 2         # SwiGLU N % 16
+    assert f(A, sa, Wt, sw, None, Y, 4, 8, 16, 1, None) == 1          # ADD without residual
+    assert f(_vp(0x10008), sa, Wt, sw, None, Y, 4, 8, 16, 0, None) == 3
+    g = lib.nvfp4_gemm
+    assert g(A, A, sa, Wt, Wt, sw, None, Y, 4, 8, 128, 0, None) == 2   # K % 256
+    t = lib.fp8_tensor_gemm
+    assert t(b"X", b"T", 1, A, 0, sa, Wt, 0, sw, Y, 0, 4, 8, 16, None) == 1
+    assert t(b"T", b"N", 1, A, 0, sa, Wt, 0, sw, Y, 0, 8, 8, 16, None) == 2   # M % 16 for 'T'
+    assert t(b"N", b"T", 0, A, 0, sa, Wt, 0, sw, Y, 0, 4, 8, 16, None) == 0   # empty batch
+    q = lib.spg_quantize_fp8_rows
+    assert q(A, 4, 12, Y, sa, None) == 2
+    assert q(A, 0, 16, Y, sa, None) == 0
+    qn = lib.spg_quantize_nvfp4
+    assert qn(A, 4, 96, sa, Y, Wt, None) == 2
+
+
+def test_oracle_is_not_imported_by_the_package():
+    import sys
+    src = open(os.path.join(ROOT, "scaled_precision_gemm_gb300", "__init__.py")).read()
+    assert "oracle" not in re.sub(r'""".*?"""', "", src, flags=re.S)
+    assert all("oracle" not in open(os.path.join(ROOT, "scaled_precision_gemm_gb300", "csrc", f)).read()
+               for f in os.listdir(os.path.join(ROOT, "scaled_precision_gemm_gb300", "csrc")))
