@@ -1,0 +1,558 @@
+"""Benchmark of the scaled-precision GEMM hot path on one GB300.
+
+Default workload (one "step"): the FP8 E4M3 row-scaled linear_add layer at
+T in {1024, 4096, 8192} for the two weight shapes (K=17408, N=5120) and
+(K=6144, N=5120).  For each of the six (T, K) cases a step quantizes the bf16
+activations to E4M3 codes with per-row scales and runs the row-scaled GEMM
+with the fused bf16 residual add.  Weights are quantized once, outside the
+timed region, as a deployment does offline.  L2 is flushed (a 512 MB write)
+before every case, outside the CUDA-event brackets; the reported time is the
+sum of the bracketed segments.
+
+Metric: TFLOP/s = sum(2 T N K) / step time, plus each case's GEMM-only rate
+and its fraction of the dense FP8 tensor peak.
+
+Other workloads (--workload): fp8_swiglu (T in {1024, 4096}, K=5120,
+N=34816 and the plain-linear widths 14336/16384/34816), nvfp4 (linear_add
+and linear_swiglu at T in {256, 1024, 4096, 8192}), fp8_tensor (the
+per-tensor training shapes).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "scaled GEMM TFLOP/s and % of GB300 FP8/FP4 tensor peak at T=1024/4096/8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense ratios to bf16 (2.25 PF): fp8 4.5 PF, fp4 13.5 PF
+NOMINAL_RATIO = {"fp8": 2.0, "fp4": 6.0, "bf16": 1.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return {"hbm_gbs": float(d.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                    "bf16_tflops": float(d.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                    "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained",
+                                                         d.get("bf16_tflops", 1700.0))),
+                    "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ------------------------------------------------------------ workloads
+def workload_cases(name):
+    if name == "fp8_linear_add":
+        return [dict(kind="fp8", T=T, K=K, N=5120, epi="add", w_std=0.02)
+                for T in (1024, 4096, 8192) for K in (17408, 6144)]
+    if name == "fp8_swiglu":
+        cases = [dict(kind="fp8", T=T, K=5120, N=34816, epi="swiglu", w_std=1.0) for T in (1024, 4096)]
+        cases += [dict(kind="fp8", T=T, K=5120, N=N, epi="linear", w_std=1.0)
+                  for T in (1024, 4096) for N in (14336, 16384, 34816)]
+        return cases
+    if name == "nvfp4":
+        cases = []
+        for T in (256, 1024, 4096, 8192):
+            cases += [dict(kind="nvfp4", T=T, K=17408, N=5120, epi="add"),
+                      dict(kind="nvfp4", T=T, K=6144, N=5120, epi="add"),
+                      dict(kind="nvfp4", T=T, K=5120, N=34816, epi="swiglu")]
+        return cases
+    if name == "fp8_tensor":
+        return [dict(kind="tensor", layout=l, M=M, N=N, K=K, batch=b) for (l, M, N, K, b) in [
+            ("NT", 2048, 6912, 1536, 1), ("NT", 2048, 1536, 6912, 1), ("NN", 2048, 1536, 6912, 1),
+            ("NN", 2048, 6912, 1536, 1), ("TN", 6912, 1536, 2048, 1), ("TN", 1536, 6912, 2048, 1),
+            ("NT", 512, 512, 512, 1), ("NT", 4096, 4096, 4096, 1), ("NT", 8192, 8192, 8192, 1),
+            ("NT", 64, 8192, 2048, 1), ("NT", 1024, 1536, 2048, 1), ("NT", 1024, 1024, 2048, 8),
+            ("NT", 512, 512, 512, 64)]]
+    raise SystemExit(f"unknown workload {name}")
+
+
+def case_flops(c):
+    if c["kind"] == "tensor":
+        return 2.0 * c["M"] * c["N"] * c["K"] * c["batch"]
+    return 2.0 * c["T"] * c["N"] * c["K"]
+
+
+def case_bytes(c):
+    """Algorithmic HBM bytes of the GEMM launch (inputs read once, output written once)."""
+    if c["kind"] == "tensor":
+        return c["batch"] * (c["M"] * c["K"] + c["N"] * c["K"] + 2 * c["M"] * c["N"]) + 8
+    T, N, K = c["T"], c["N"], c["K"]
+    n_out = N // 2 if c["epi"] == "swiglu" else N
+    res = 2 * T * N if c["epi"] == "add" else 0
+    if c["kind"] == "nvfp4":
+        return T * K // 2 + N * K // 2 + (T + N) * K // 16 + 8 + 2 * T * n_out + res
+    return T * K + N * K + 4 * (T + N) + 2 * T * n_out + res
+
+
+def case_name(c):
+    if c["kind"] == "tensor":
+        return f"tensor_{c['layout']}_b{c['batch']}_{c['M']}x{c['N']}x{c['K']}"
+    return f"{c['kind']}_{c['epi']}_T{c['T']}_K{c['K']}_N{c['N']}"
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9 or parts[0] != "0" and not parts[0].isdigit():
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+
+    import scaled_precision_gemm_gb300 as spg
+    from scaled_precision_gemm_gb300 import build as spg_build
+    from synthetic_inputs import normal_bf16
+
+    spg_build.build()
+    spg.load_library()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def to_dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    cases = workload_cases(args.workload)
+    if args.case:
+        cases = [c for c in cases if case_name(c) == args.case]
+        if not cases:
+            raise SystemExit(f"no case {args.case} in workload {args.workload}")
+    # synthetic inputs, generated once per distinct shape (largest T, sliced)
+    inputs = {}
+    for c in cases:
+        if c["kind"] == "tensor":
+            key = ("tensor", c["layout"], c["M"], c["N"], c["K"], c["batch"])
+            if key not in inputs:
+                a_shape = (c["batch"], c["K"], c["M"]) if c["layout"][0] == "T" else (c["batch"], c["M"], c["K"])
+                b_shape = (c["batch"], c["K"], c["N"]) if c["layout"][1] == "N" else (c["batch"], c["N"], c["K"])
+                a = to_dev_bf16(normal_bf16(a_shape, seed=0))
+                b = to_dev_bf16(normal_bf16(b_shape, seed=1))
+                inputs[key] = (a, b)
+            continue
+        kx = ("x", c["K"])
+        if kx not in inputs:
+            tmax = max(cc["T"] for cc in cases if cc["kind"] != "tensor" and cc["K"] == c["K"])
+            inputs[kx] = to_dev_bf16(normal_bf16((tmax, c["K"]), seed=0))
+        kw = ("w", c["kind"], c["K"], c["N"])
+        if kw not in inputs:
+            w = to_dev_bf16(normal_bf16((c["N"], c["K"]), seed=1, std=c.get("w_std", 1.0)))
+            if c["kind"] == "fp8":
+                inputs[kw] = spg.quantize_fp8_rows(w)            # offline weight quantization
+            else:
+                gw = spg.nvfp4_global_scale(w)
+                inputs[kw] = (*spg.quantize_nvfp4(w, gw), gw)
+            del w
+        kr = ("r", c["N"])
+        if c["epi"] == "add" and kr not in inputs:
+            tmax = max(cc["T"] for cc in cases if cc["kind"] != "tensor" and cc["N"] == c["N"])
+            inputs[kr] = to_dev_bf16(normal_bf16((tmax, c["N"]), seed=2))
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(4, dtype=torch.float32, device=dev)
+
+    # Per case: preallocated buffers, quant(x, res) (activation quantization of
+    # the given device activations) and gemm() (the GEMM with its fused
+    # epilogue, reading what quant() wrote).  `launches` counts library kernels.
+    class Case:
+        pass
+
+    prepared = []
+    for c in cases:
+        k = Case()
+        k.c = c
+        if c["kind"] == "tensor":
+            a, b = inputs[("tensor", c["layout"], c["M"], c["N"], c["K"], c["batch"])]
+            k.x, k.res = a, None
+            ac = torch.empty(a.shape, dtype=torch.uint8, device=dev)
+            bc = torch.empty(b.shape, dtype=torch.uint8, device=dev)
+            sa = torch.empty(1, dtype=torch.float32, device=dev)
+            sb = torch.empty(1, dtype=torch.float32, device=dev)
+            k.out = torch.empty((c["batch"], c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
+            spg.quantize_fp8_tensor(b, bc, sb, scratch)   # weight-side operand, offline
+            k.quant = lambda x, res, ac=ac, sa=sa: spg.quantize_fp8_tensor(x, ac, sa, scratch)
+            k.gemm = lambda c=c, ac=ac, sa=sa, bc=bc, sb=sb, out=k.out: spg.fp8_tensor_gemm(
+                c["layout"], ac, sa, bc, sb, c["M"], c["N"], c["K"], batch=c["batch"], out=out)
+            k.launches = 3
+            prepared.append(k)
+            continue
+        T, K, N = c["T"], c["K"], c["N"]
+        k.x = inputs[("x", K)][:T]
+        n_out = N // 2 if c["epi"] == "swiglu" else N
+        k.out = torch.empty((T, n_out), dtype=torch.bfloat16, device=dev)
+        k.res = inputs[("r", N)][:T] if c["epi"] == "add" else None
+        k.res_dev = k.res
+        if c["kind"] == "fp8":
+            W, sw = inputs[("w", "fp8", K, N)]
+            A = torch.empty((T, K), dtype=torch.uint8, device=dev)
+            sa = torch.empty((T,), dtype=torch.float32, device=dev)
+            k.quant = lambda x, res, A=A, sa=sa, k=k: (spg.quantize_fp8_rows(x, A, sa),
+                                                       setattr(k, "res_dev", res))
+            k.gemm = lambda A=A, sa=sa, W=W, sw=sw, k=k, epi=c["epi"]: spg.fp8_rowscaled_gemm(
+                A, sa, W, sw, residual=k.res_dev, epilogue=epi, out=k.out)
+            k.launches = 2
+        else:
+            Wc, sfW, gW = inputs[("w", "nvfp4", K, N)]
+            A = torch.empty((T, K // 2), dtype=torch.uint8, device=dev)
+            sfA = torch.empty((spg.nvfp4_sf_bytes(T, K),), dtype=torch.uint8, device=dev)
+            gA = torch.empty((1,), dtype=torch.float32, device=dev)
+
+            def quant(x, res, A=A, sfA=sfA, gA=gA, k=k):
+                spg.nvfp4_global_scale(x, gA, scratch)
+                spg.quantize_nvfp4(x, gA, A, sfA)
+                k.res_dev = res
+            k.quant = quant
+            k.gemm = lambda A=A, sfA=sfA, gA=gA, Wc=Wc, sfW=sfW, gW=gW, k=k, epi=c["epi"]: \
+                spg.nvfp4_gemm(A, sfA, gA, Wc, sfW, gW, residual=k.res_dev, epilogue=epi,
+                               out=k.out)
+            k.launches = 5     # memset + amax + finalize + quantize + GEMM
+        prepared.append(k)
+
+    def one_step(timed):
+        """Run every case once; returns (segment events, gemm-only events, launches)."""
+        seg, gem, launches = [], [], 0
+        for k in prepared:
+            flush.zero_()                                  # L2 flush, outside the brackets
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e2 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            k.quant(k.x, k.res)
+            e1.record(stream)
+            k.gemm()
+            e2.record(stream)
+            seg.append((e0, e2))
+            gem.append((e1, e2))
+            launches += k.launches
+        return seg, gem, launches
+
+    for _ in range(args.warmup):
+        one_step(False)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = ClockSampler()
+    clocks.start()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    all_seg, all_gemm, launches = [], [], 0
+    for _ in range(args.steps):
+        s, g, nl = one_step(True)
+        all_seg.append(s)
+        all_gemm.append(g)
+        launches += nl
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+
+    step_ms = [sum(a.elapsed_time(b) for a, b in s) for s in all_seg]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops_step = sum(case_flops(k.c) for k in prepared)
+    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    per_case = []
+    for i, k in enumerate(prepared):
+        c = k.c
+        gms = statistics.median(all_gemm[k][i][0].elapsed_time(all_gemm[k][i][1])
+                                for k in range(args.steps))
+        sms = statistics.median(all_seg[k][i][0].elapsed_time(all_seg[k][i][1])
+                                for k in range(args.steps))
+        dtype = "fp4" if c["kind"] == "nvfp4" else "fp8"
+        peak = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
+        tf = case_flops(c) / (gms * 1e-3) / 1e12
+        per_case.append({"case": case_name(c), "gemm_us": round(gms * 1e3, 2),
+                         "step_us": round(sms * 1e3, 2), "gemm_tflops": round(tf, 1),
+                         "frac_of_peak": round(tf / peak, 4),
+                         "gemm_gbs": round(case_bytes(c) / (gms * 1e-3) / 1e9, 1)})
+    # dominant kernel: the case with the longest GEMM
+    dom_i = max(range(len(per_case)), key=lambda i: per_case[i]["gemm_us"])
+    dc = prepared[dom_i].c
+    dtype = "fp4" if dc["kind"] == "nvfp4" else "fp8"
+    dom_ms = per_case[dom_i]["gemm_us"] * 1e-3
+    dom_peak = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
+    achieved = case_flops(dc) / (dom_ms * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(case_name(dc))
+        except Exception:
+            traffic = None
+
+    # ---------------- e2e: host buffers through the public API
+    e2e = None if args.no_e2e else run_e2e(args, spg, torch, dev, prepared, inputs)
+
+    dtype_line = "e2m1" if args.workload == "nvfp4" else "e4m3"
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_line, "data": "synthetic",
+        "config": {"workload": args.workload,
+                   "cases": [case_name(k.c) for k in prepared],
+                   "step": "activation quantization + GEMM with fused epilogue per case",
+                   "l2": "flushed (512 MB write) before every case, outside the timed brackets",
+                   "inputs": "bf16 N(0,1) activations/residual, N(0,0.02) weights (splitmix64 "
+                             "Box-Muller, seeds 0/1/2); weights quantized once offline"},
+        "roofline": {"bound": "tensor", "kernel": case_name(dc), "achieved": round(achieved, 1),
+                     "peak": round(dom_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / dom_peak, 4), "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
+                                    f"nominal {dtype} ratio {NOMINAL_RATIO[dtype]}",
+                     "algorithmic_bytes": case_bytes(dc)},
+        "per_case": per_case,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, rows=args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, spg, torch, dev, prepared, inputs):
+    """Same workload through the public API with HOST buffers: per case the
+    bf16 activations (and residual) are copied from pinned host memory, the
+    step runs on those device copies, and the bf16 output is copied back to
+    pinned host memory; all copies are inside the timed region."""
+    h2d = d2h = 0
+    for k in prepared:
+        k.x_host = k.x.cpu().pin_memory()
+        k.res_host = None if k.res is None else k.res.cpu().pin_memory()
+        k.out_host = torch.empty(k.out.shape, dtype=k.out.dtype).pin_memory()
+        k.x_d = torch.empty_like(k.x)
+        k.res_d = None if k.res is None else torch.empty_like(k.res)
+        h2d += k.x_host.numel() * 2 + (0 if k.res_host is None else k.res_host.numel() * 2)
+        d2h += k.out_host.numel() * 2
+    stream = torch.cuda.current_stream(dev)
+
+    def e2e_step():
+        for k in prepared:
+            k.x_d.copy_(k.x_host, non_blocking=True)
+            if k.res_d is not None:
+                k.res_d.copy_(k.res_host, non_blocking=True)
+            k.quant(k.x_d, k.res_d)
+            k.gemm()
+            k.out_host.copy_(k.out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 3))
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    for k in prepared:          # restore the device-resident inputs
+        k.quant(k.x, k.res)
+    flops = sum(case_flops(k.c) for k in prepared)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------ CPU oracle
+_CPU_INPUTS = {}
+
+
+def _cpu_case_inputs(c, rows):
+    """Oracle-side inputs of one case (weights quantized once, cached)."""
+    import oracle
+    from synthetic_inputs import normal_bf16
+
+    key = (case_name(c), rows)
+    if key in _CPU_INPUTS:
+        return _CPU_INPUTS[key]
+    if c["kind"] == "tensor":
+        K, N = c["K"], c["N"]
+        B, sB = oracle.quantize_fp8_tensor(normal_bf16((N, K), seed=1))
+        d = dict(x=normal_bf16((rows, K), seed=0), B=B, sB=sB)
+    else:
+        K, N = c["K"], c["N"]
+        w = normal_bf16((N, K), seed=1, std=c.get("w_std", 1.0))
+        d = dict(x=normal_bf16((rows, K), seed=0),
+                 res=normal_bf16((rows, N), seed=2) if c["epi"] == "add" else None)
+        if c["kind"] == "fp8":
+            d["W"], d["sw"] = oracle.quantize_fp8_rows(w)
+        else:
+            d["gw"] = oracle.nvfp4_global_scale(w)
+            d["W"], d["sfW"] = oracle.quantize_nvfp4(w, d["gw"])
+    _CPU_INPUTS[key] = d
+    return d
+
+
+def cpu_baseline(workload, rows=32):
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    workload: for every case, the activation quantizer and the exact-integer
+    GEMM with its epilogue on `rows` activation rows (all N columns).  Weight
+    quantization is offline and untimed, as on the GPU side."""
+    import oracle
+
+    oracle.build()
+    cases = workload_cases(workload)
+    cores = os.cpu_count() or 1
+    done_flops = 0.0
+    t_total = 0.0
+    for c in cases:
+        d = _cpu_case_inputs(c, rows)
+        t0 = time.perf_counter()
+        if c["kind"] == "tensor":
+            A, sA = oracle.quantize_fp8_tensor(d["x"])
+            oracle.fp8_tensor_gemm("NT", A, sA, d["B"], d["sB"], rows, c["N"], c["K"])
+        elif c["kind"] == "fp8":
+            A, sa = oracle.quantize_fp8_rows(d["x"])
+            oracle.fp8_rowscaled_gemm(A, sa, d["W"], d["sw"], d["res"], c["epi"])
+        else:
+            ga = oracle.nvfp4_global_scale(d["x"])
+            A, sfA = oracle.quantize_nvfp4(d["x"], ga)
+            oracle.nvfp4_gemm(A, sfA, ga, d["W"], d["sfW"], d["gw"], d["res"], c["epi"])
+        t_total += time.perf_counter() - t0
+        done_flops += 2.0 * rows * c["N"] * c["K"]
+    return {"value": round(done_flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{rows} activation rows (all N) of each of the {len(cases)} cases of "
+                      f"{workload}: activation quantization + exact GEMM + epilogue; "
+                      f"{t_total:.1f} s of CPU work on {cores} threads"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    per_step = []
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        cpu_baseline(args.workload, rows=rows)
+    base = None
+    flops = work_s = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        base = cpu_baseline(args.workload, rows=rows)
+        per_step.append(time.perf_counter() - t0)
+        flops += sum(2.0 * rows * c["N"] * c["K"] * c.get("batch", 1)
+                     for c in workload_cases(args.workload))
+        work_s += per_step[-1]
+    value = round(flops / work_s / 1e12, 6)
+    base["value"] = value
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(per_step) / len(per_step), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int64 exact dot products, fp64 scales", "data": "synthetic",
+            "config": {"workload": args.workload}, "impl": "reference",
+            "cpu_baseline": dict(base),
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="spg", choices=["spg", "reference"])
+    ap.add_argument("--workload", default="fp8_linear_add",
+                    choices=["fp8_linear_add", "fp8_swiglu", "nvfp4", "fp8_tensor"])
+    ap.add_argument("--cpu-rows", type=int, default=32,
+                    help="activation rows per case in the CPU-oracle baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=4,
+                    help="activation rows per case in each step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--case", default=None, help="run only this case of the workload")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
