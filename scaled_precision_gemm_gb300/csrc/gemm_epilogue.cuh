@@ -1,0 +1,169 @@
+// Epilogue warps of the tcgen05 GEMMs: drain the fp32 accumulator from TMEM,
+// apply the scales and the fused epilogue, and write bf16 through
+// 64-byte-swizzled shared memory with TMA stores.
+//
+// Per output tile each epilogue warp owns 32 rows (one TMEM lane quarter);
+// each thread owns one row.  The global operands of the epilogue (row scale,
+// column scales, the first residual chunk) are requested before the
+// accumulator is ready so their latency overlaps the main loop; the residual
+// of chunk c+1 is requested while chunk c is being processed.
+#pragma once
+
+#include "gemm_kernel_common.cuh"
+
+namespace spg {
+
+template <int EPI, int SCALE, int BN>
+struct EpilogueCfg {
+  static constexpr int kAccColsPerChunk = EPI == SPG_EPI_SWIGLU ? 64 : 32;
+  static constexpr int kChunks = BN / kAccColsPerChunk;
+  static constexpr int kBufBytes = 32 * 64;  // 32 rows x 32 bf16
+  static constexpr int kSwRegs = BN / 32;    // column scales held per lane
+};
+
+// Residual of one 32-column chunk of this thread's row (zeros outside).
+__device__ __forceinline__ void load_residual_chunk(const GemmParams& p, int m, int n_c0,
+                                                    bool row_ok, uint4 (&r)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) r[g] = make_uint4(0u, 0u, 0u, 0u);
+  if (row_ok) {
+    const uint4* rp = reinterpret_cast<const uint4*>(p.residual + int64_t(m) * p.N + n_c0);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (n_c0 + g * 8 < p.N) r[g] = __ldg(rp + g);
+  }
+}
+
+// TileFn(tile) -> TileCoord with mb already offset for this CTA's rows;
+// ArriveEmpty(buf) releases accumulator buffer `buf` to the MMA issuer.
+template <int EPI, int SCALE, int BN, typename TileFn, typename ArriveEmpty>
+__device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtensorMap* tmY,
+                                              uint32_t tmem_base, uint64_t* acc_full,
+                                              ArriveEmpty arrive_empty, uint8_t* epi_smem,
+                                              int tile_begin, int tile_step, TileFn tile_fn,
+                                              const WaitCtl& ctl) {
+  using E = EpilogueCfg<EPI, SCALE, BN>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int e = warp - 2;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  uint8_t* stage0 = epi_smem + (e * 2) * E::kBufBytes;
+  int it = 0;
+  int chunk_ctr = 0;
+  float scalar = 1.f;
+  if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
+  const bool have_k = p.num_k_blocks > 0;
+
+  for (int tile = tile_begin; tile < p.total_tiles; tile += tile_step, ++it) {
+    const int buf = it & 1;
+    const uint32_t acc_ph = (it >> 1) & 1;
+    const TileCoord tc = tile_fn(tile);
+    const int m0 = tc.mb * 128;
+    const int n0 = tc.nb * BN;
+    const int m = m0 + q * 32 + lane;
+    const bool row_ok = m < p.M;
+
+    // Epilogue operands, requested before the accumulator is ready.
+    float row_s = scalar;
+    if constexpr (SCALE == kScaleRow) row_s = row_ok ? __ldg(p.row_scale + m) : 0.f;
+    float swr[E::kSwRegs];
+    if constexpr (SCALE == kScaleRow) {
+#pragma unroll
+      for (int j = 0; j < E::kSwRegs; ++j) {
+        const int n = n0 + 32 * j + lane;
+        swr[j] = n < p.N ? __ldg(p.col_scale + n) : 0.f;
+      }
+    }
+    uint4 res_cur[4];
+    if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n0, row_ok, res_cur);
+
+    if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
+    tc_fence_after();
+    const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+
+#pragma unroll
+    for (int c = 0; c < E::kChunks; ++c, ++chunk_ctr) {
+      const int acc_c0 = c * E::kAccColsPerChunk;
+      uint32_t raw[E::kAccColsPerChunk];
+      if (have_k) {
+        tmem_ld_32x32b_x32(t_row + acc_c0, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
+        if constexpr (E::kAccColsPerChunk == 64)
+          tmem_ld_32x32b_x32(t_row + acc_c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < E::kAccColsPerChunk; ++i) raw[i] = 0u;
+      }
+      uint4 res_next[4];
+      if constexpr (EPI == SPG_EPI_ADD) {
+        if (c + 1 < E::kChunks) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
+      }
+      if (have_k) tmem_wait_ld();
+      if (c == E::kChunks - 1) {
+        // Every column of this accumulator buffer has been read: hand it back.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_empty(buf);
+      }
+      float v[E::kAccColsPerChunk];
+#pragma unroll
+      for (int i = 0; i < E::kAccColsPerChunk; ++i) {
+        float s = row_s;
+        if constexpr (SCALE == kScaleRow) {
+          const int col = acc_c0 + i;  // column inside the tile
+          s = row_s * __shfl_sync(0xffffffffu, swr[col >> 5], col & 31);
+        }
+        v[i] = __uint_as_float(raw[i]) * s;
+      }
+      float o[32];
+      if constexpr (EPI == SPG_EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float gate = v[2 * j], up = v[2 * j + 1];
+          o[j] = __fdividef(gate, 1.f + __expf(-gate)) * up;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = v[j];
+        if constexpr (EPI == SPG_EPI_ADD) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t w[4] = {res_cur[g].x, res_cur[g].y, res_cur[g].z, res_cur[g].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              o[g * 8 + 2 * h] += __uint_as_float(w[h] << 16);
+              o[g * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xFFFF0000u);
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) res_cur[g] = res_next[g];
+        }
+      }
+      // Stage the 32 x 32 bf16 block (64-byte swizzle) and TMA-store it.
+      uint8_t* sbuf = stage0 + (chunk_ctr & 1) * E::kBufBytes;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        uint4 pk;
+        pk.x = pack_bf16x2(o[jj * 8 + 0], o[jj * 8 + 1]);
+        pk.y = pack_bf16x2(o[jj * 8 + 2], o[jj * 8 + 3]);
+        pk.z = pack_bf16x2(o[jj * 8 + 4], o[jj * 8 + 5]);
+        pk.w = pack_bf16x2(o[jj * 8 + 6], o[jj * 8 + 7]);
+        const int phys = jj ^ ((lane >> 1) & 3);
+        *reinterpret_cast<uint4*>(sbuf + lane * 64 + phys * 16) = pk;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int out_x = (EPI == SPG_EPI_SWIGLU ? n0 / 2 : n0) + c * 32;
+      const int out_y = m0 + q * 32;
+      if (lane == 0) {
+        if (out_y < p.M && out_x < p.n_out) tma_store_3d(tmY, sbuf, out_x, out_y, tc.b);
+        bulk_commit();
+      }
+    }
+  }
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
+}
+
+}  // namespace spg

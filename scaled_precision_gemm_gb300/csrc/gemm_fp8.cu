@@ -7,9 +7,12 @@ using namespace spg;
 namespace {
 
 template <int EPI>
-spg_status dispatch_bn(int bn, const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
-  if (bn == 256) return launch_gemm_variant<kKindFp8, EPI, 256, 4, false, false, kScaleRow>(m, p, grid, s);
-  return launch_gemm_variant<kKindFp8, EPI, 128, 6, false, false, kScaleRow>(m, p, grid, s);
+spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
+  if (r.block_m == 256)
+    return launch_gemm_2sm_variant<EPI, 256, 6, false, false, kScaleRow>(m, p, r.grid, s);
+  if (r.block_n == 256)
+    return launch_gemm_variant<kKindFp8, EPI, 256, 4, false, false, kScaleRow>(m, p, r.grid, s);
+  return launch_gemm_variant<kKindFp8, EPI, 128, 6, false, false, kScaleRow>(m, p, r.grid, s);
 }
 
 }  // namespace
@@ -29,11 +32,12 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
       (epilogue == SPG_EPI_ADD && !aligned16(residual)))
     return SPG_ERR_MISALIGNED;
 
-  const spg_route r = select_route_internal(SPG_KIND_FP8_ROWSCALED, T, N, K, epilogue, 1);
+  const spg_route r = select_route_internal(SPG_KIND_FP8_ROWSCALED, T, N, K, epilogue, 1, false);
+  const int b_rows = r.block_m == 256 ? r.block_n / 2 : r.block_n;  // B rows staged per CTA
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;
   if (!make_tmap_3d(&maps.a, A, false, K, T, 1, K, K * T, 128, 128, 128) ||
-      !make_tmap_3d(&maps.b, W, false, K, N, 1, K, K * N, 128, r.block_n, 128) ||
+      !make_tmap_3d(&maps.b, W, false, K, N, 1, K, K * N, 128, b_rows, 128) ||
       !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
     return SPG_ERR_CUDA;
   GemmParams p;
@@ -43,8 +47,8 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
   p.col_scale = sw;
   p.residual = static_cast<const __nv_bfloat16*>(residual);
   switch (epilogue) {
-    case SPG_EPI_LINEAR: return dispatch_bn<SPG_EPI_LINEAR>(r.block_n, maps, p, r.grid, stream);
-    case SPG_EPI_ADD: return dispatch_bn<SPG_EPI_ADD>(r.block_n, maps, p, r.grid, stream);
-    default: return dispatch_bn<SPG_EPI_SWIGLU>(r.block_n, maps, p, r.grid, stream);
+    case SPG_EPI_LINEAR: return dispatch<SPG_EPI_LINEAR>(r, maps, p, stream);
+    case SPG_EPI_ADD: return dispatch<SPG_EPI_ADD>(r, maps, p, stream);
+    default: return dispatch<SPG_EPI_SWIGLU>(r, maps, p, stream);
   }
 }

@@ -24,49 +24,10 @@
 // code in the device error word and every role drains and returns.
 #pragma once
 
-#include <cuda_bf16.h>
-
-#include "common.h"
-#include "ptx.cuh"
+#include "gemm_epilogue.cuh"
+#include "gemm_kernel_common.cuh"
 
 namespace spg {
-
-enum GemmKind : int { kKindFp8 = 0, kKindNvfp4 = 1 };
-enum ScaleMode : int { kScaleRow = 0, kScaleScalar = 1 };
-
-// Error codes written to the device error word (first one wins).
-enum : unsigned int {
-  kErrWaitEmpty = 0x101,
-  kErrWaitFull = 0x102,
-  kErrWaitAccEmpty = 0x103,
-  kErrWaitAccFull = 0x104,
-  kErrDrain = 0x105,
-};
-
-struct GemmParams {
-  int M;             // output rows (T)
-  int N;             // accumulator columns
-  int K;             // reduction length in elements
-  int n_out;         // output columns (N, or N/2 for SwiGLU)
-  int num_m_blocks;  // ceil(M / 128)
-  int num_n_blocks;  // ceil(N / BN)
-  int num_k_blocks;  // ceil(K_bytes / 128)
-  int tiles_per_batch;
-  int total_tiles;
-  int group_m;      // m-blocks per rasterization group
-  int a_batch_mul;  // 0 broadcasts A matrix 0 over the batch, else 1
-  int b_batch_mul;
-  const float* row_scale;  // kScaleRow: sa [M]
-  const float* col_scale;  // kScaleRow: sw [N]
-  const float* scalar_a;   // kScaleScalar: device scalars
-  const float* scalar_b;
-  const __nv_bfloat16* residual;  // SPG_EPI_ADD: [M, N] row-major
-  const uint8_t* sfa;             // NVFP4 scales, blocked layout
-  const uint8_t* sfb;
-  int sf_tiles_per_row_block;  // K / 64
-  uint64_t timeout_ns;
-  unsigned int* err;
-};
 
 template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
 struct GemmCfg {
@@ -119,44 +80,6 @@ struct GemmCfg {
     }
   }
 };
-
-struct TileCoord {
-  int b, mb, nb;
-};
-
-__device__ __forceinline__ TileCoord tile_coord(int tile, const GemmParams& p) {
-  TileCoord c;
-  c.b = tile / p.tiles_per_batch;
-  const int t = tile - c.b * p.tiles_per_batch;
-  const int span = p.group_m * p.num_n_blocks;
-  const int g = t / span;
-  const int first_m = g * p.group_m;
-  const int rem = p.num_m_blocks - first_m;
-  const int gsize = rem < p.group_m ? rem : p.group_m;
-  const int local = t - g * span;
-  c.mb = first_m + local % gsize;
-  c.nb = local / gsize;
-  return c;
-}
-
-// Drain-mode wait: bounded, but not cut short by the abort flag.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
-                                                uint64_t timeout_ns, unsigned int* err) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((i & 15u) == 15u && (globaltimer_ns() - t0 > timeout_ns || i > (1u << 30))) {
-      atomicCAS(err, 0u, kErrDrain);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
 __global__ void __launch_bounds__(192, 1)
@@ -346,120 +269,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int e = warp - 2;
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r_local = q * 32 + lane;
-    uint8_t* stage0 = epi + (e * 2) * Cfg::kEpiBufBytes;
-    int it = 0;
-    int chunk_ctr = 0;
-    float scalar = 1.f;
-    if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
-      const int buf = it & 1;
-      const uint32_t acc_ph = (it >> 1) & 1;
-      if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
-      tc_fence_after();
-      const TileCoord tc = tile_coord(tile, p);
-      const int m0 = tc.mb * Cfg::kBM;
-      const int n0 = tc.nb * BN;
-      const int m = m0 + r_local;
-      const bool row_ok = m < p.M;
-      float row_s = scalar;
-      if constexpr (SCALE == kScaleRow) row_s = row_ok ? __ldg(p.row_scale + m) : 0.f;
-      const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-      const bool have_k = p.num_k_blocks > 0;
-
-#pragma unroll 1
-      for (int c = 0; c < Cfg::kChunks; ++c, ++chunk_ctr) {
-        const int acc_c0 = c * Cfg::kAccColsPerChunk;  // first accumulator column
-        uint32_t raw[Cfg::kAccColsPerChunk];
-        if (have_k) {
-          tmem_ld_32x32b_x32(t_row + acc_c0, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
-          if constexpr (Cfg::kAccColsPerChunk == 64)
-            tmem_ld_32x32b_x32(t_row + acc_c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < Cfg::kAccColsPerChunk; ++i) raw[i] = 0u;
-        }
-        if (c == Cfg::kChunks - 1) {
-          // The whole accumulator buffer has been read: hand it back.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        }
-        float v[Cfg::kAccColsPerChunk];
-#pragma unroll
-        for (int i = 0; i < Cfg::kAccColsPerChunk; ++i) v[i] = __uint_as_float(raw[i]);
-        const int n_c0 = n0 + acc_c0;  // first accumulator column of the chunk (global)
-        if constexpr (SCALE == kScaleRow) {
-#pragma unroll
-          for (int i = 0; i < Cfg::kAccColsPerChunk; i += 4) {
-            float4 sw = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (n_c0 + i < p.N) sw = __ldg(reinterpret_cast<const float4*>(p.col_scale + n_c0 + i));
-            v[i + 0] *= row_s * sw.x;
-            v[i + 1] *= row_s * sw.y;
-            v[i + 2] *= row_s * sw.z;
-            v[i + 3] *= row_s * sw.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < Cfg::kAccColsPerChunk; ++i) v[i] *= scalar;
-        }
-        float o[32];
-        if constexpr (EPI == SPG_EPI_SWIGLU) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float gate = v[2 * j], up = v[2 * j + 1];
-            o[j] = gate / (1.f + __expf(-gate)) * up;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = v[j];
-          if constexpr (EPI == SPG_EPI_ADD) {
-            if (row_ok) {
-              const uint4* rp = reinterpret_cast<const uint4*>(p.residual + int64_t(m) * p.N + n_c0);
-#pragma unroll
-              for (int g8 = 0; g8 < 4; ++g8) {
-                if (n_c0 + g8 * 8 < p.N) {
-                  const uint4 rv = __ldg(rp + g8);
-                  const uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-                  for (int h = 0; h < 4; ++h) {
-                    o[g8 * 8 + 2 * h] += __uint_as_float(w[h] << 16);
-                    o[g8 * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xFFFF0000u);
-                  }
-                }
-              }
-            }
-          }
-        }
-        // Stage the 32 x 32 bf16 block (64-byte swizzle) and TMA-store it.
-        uint8_t* sbuf = stage0 + (chunk_ctr & 1) * Cfg::kEpiBufBytes;
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint4 pk;
-          pk.x = pack_bf16x2(o[jj * 8 + 0], o[jj * 8 + 1]);
-          pk.y = pack_bf16x2(o[jj * 8 + 2], o[jj * 8 + 3]);
-          pk.z = pack_bf16x2(o[jj * 8 + 4], o[jj * 8 + 5]);
-          pk.w = pack_bf16x2(o[jj * 8 + 6], o[jj * 8 + 7]);
-          const int phys = jj ^ ((lane >> 1) & 3);
-          *reinterpret_cast<uint4*>(sbuf + lane * 64 + phys * 16) = pk;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int out_x = (EPI == SPG_EPI_SWIGLU ? n0 / 2 : n0) + c * Cfg::kOutColsPerChunk;
-        const int out_y = m0 + q * 32;
-        if (lane == 0 && out_y < p.M && out_x < p.n_out) {
-          tma_store_3d(&tmY, sbuf, out_x, out_y, tc.b);
-        }
-        if (lane == 0) bulk_commit();
-      }
-    }
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
+    epilogue_loop<EPI, SCALE, BN>(
+        p, &tmY, tmem_base, acc_full, [&](int b) { mbar_arrive(&acc_empty[b]); }, epi, blockIdx.x,
+        gridDim.x, [&](int tile) { return tile_coord(tile, p); }, ctl);
   }
 
   tc_fence_before();

@@ -1,0 +1,222 @@
+// Two-SM (CTA-pair) tcgen05 GEMM for FP8 operands, sm_103a.
+//
+// A cluster of two CTAs computes one 256 x BN output tile with
+// tcgen05.mma.cta_group::2: each CTA stages its own 128 rows of A and its
+// half (BN/2 rows) of B in shared memory, the leader CTA issues the MMA for
+// the pair, and each CTA's TMEM receives its own 128 x BN accumulator.  Per
+// SM this halves the B bytes staged per MMA compared with a one-CTA
+// 128 x BN tile, which is what lets the ring run six stages deep and keeps
+// the operand feed below the shared-memory and L2 limits.
+//
+// Synchronisation of the pair:
+//   full[s]      leader only; the leader's producer posts the byte count of
+//                both CTAs' loads, both CTAs' TMA loads complete on it.
+//   empty[s]     in both CTAs; released by one multicast tcgen05.commit.
+//   acc_full[b]  in both CTAs; released by one multicast tcgen05.commit.
+//   acc_empty[b] leader only; the 4 epilogue warps of each CTA arrive on it.
+// Every wait is bounded in time, as in the one-CTA kernel.
+#pragma once
+
+#include "gemm_epilogue.cuh"
+#include "gemm_kernel_common.cuh"
+
+namespace spg {
+
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+struct Gemm2smCfg {
+  static constexpr int kBM = 128;  // rows per CTA (the pair covers 256)
+  static constexpr int kBKBytes = 128;
+  static constexpr int kKSteps = 4;
+  static constexpr int kBHalf = BN / 2;
+  static constexpr int kABytes = kBM * kBKBytes;
+  static constexpr int kBBytes = kBHalf * kBKBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * 32 * 64;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kThreads = 192;
+
+  static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
+  static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
+  static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
+  static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+  static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+
+  // kind::f8f6f4, E4M3 x E4M3 -> f32, M = 256 (pair), N = BN.
+  __host__ __device__ static constexpr uint32_t idesc() {
+    return (1u << 4) | (uint32_t(A_MN) << 15) | (uint32_t(B_MN) << 16) |
+           (uint32_t(BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
+  }
+};
+
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* epi = smem + STAGES * Cfg::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + Cfg::kEpiBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * Cfg::kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmY);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl ctl{p.timeout_ns, p.err, abort_flag};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.total_tiles; tile += num_pairs) {
+        const TileCoord tc = tile_coord(tile, p);
+        const int m0 = tc.mb * 256 + int(rank) * 128;
+        const int nb0 = tc.nb * BN + int(rank) * Cfg::kBHalf;
+        const int za = tc.b * p.a_batch_mul;
+        const int zb = tc.b * p.b_batch_mul;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, ctl, kErrWaitEmpty)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = ring + s * Cfg::kStageBytes;
+          uint8_t* sb = sa + Cfg::kABytes;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kStageBytes);
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          const int kx = kb * Cfg::kBKBytes;
+          if constexpr (A_MN)
+            tma_load_3d_pair(sa, &tmA, bar, m0, kx, za);
+          else
+            tma_load_3d_pair(sa, &tmA, bar, kx, m0, za);
+          if constexpr (B_MN)
+            tma_load_3d_pair(sb, &tmB, bar, nb0, kx, zb);
+          else
+            tma_load_3d_pair(sb, &tmB, bar, kx, nb0, zb);
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // The leader's full barriers count both CTAs' bytes: waiting on the
+      // last ones means no TMA write of the pair is still in flight.
+      if (rank == 0) {
+        const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
+        for (uint32_t i = 0; i < outstanding; ++i) {
+          const uint32_t idx = issued - 1 - i;
+          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.timeout_ns, p.err);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t kIdesc = Cfg::idesc();
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.total_tiles; tile += num_pairs, ++it) {
+        const int buf = it & 1;
+        const uint32_t acc_ph = (it >> 1) & 1;
+        if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(ring + s * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int j = 0; j < Cfg::kKSteps; ++j) {
+            uint64_t adesc, bdesc;
+            if constexpr (A_MN)
+              adesc = smem_desc(sa + j * 32 * 128, 16384, 1024, kSwizzle128B);
+            else
+              adesc = smem_desc(sa + j * 32, 16, 1024, kSwizzle128B);
+            if constexpr (B_MN)
+              bdesc = smem_desc(sb + j * 32 * 128, 16384, 1024, kSwizzle128B);
+            else
+              bdesc = smem_desc(sb + j * 32, 16, 1024, kSwizzle128B);
+            mma_f8f6f4_pair(d_tmem, adesc, bdesc, kIdesc, (kb | j) != 0);
+          }
+          tc_commit_pair_multicast(&empty[s], 0x3);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(&acc_full[buf], 0x3);
+      }
+      tc_commit_pair(drain);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.err);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    epilogue_loop<EPI, SCALE, BN>(
+        p, &tmY, tmem_base, acc_full,
+        [&](int b) { mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0)); }, epi, pair,
+        num_pairs,
+        [&](int tile) {
+          TileCoord tc = tile_coord(tile, p);
+          tc.mb = tc.mb * 2 + int(rank);
+          return tc;
+        },
+        ctl);
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+}
+
+}  // namespace spg

@@ -1,0 +1,86 @@
+// Shared definitions of the tcgen05 GEMM kernels: parameters, error codes,
+// tile rasterization and small device helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace spg {
+enum GemmKind : int { kKindFp8 = 0, kKindNvfp4 = 1 };
+enum ScaleMode : int { kScaleRow = 0, kScaleScalar = 1 };
+
+// Error codes written to the device error word (first one wins).
+enum : unsigned int {
+  kErrWaitEmpty = 0x101,
+  kErrWaitFull = 0x102,
+  kErrWaitAccEmpty = 0x103,
+  kErrWaitAccFull = 0x104,
+  kErrDrain = 0x105,
+};
+
+struct GemmParams {
+  int M;             // output rows (T)
+  int N;             // accumulator columns
+  int K;             // reduction length in elements
+  int n_out;         // output columns (N, or N/2 for SwiGLU)
+  int num_m_blocks;  // ceil(M / 128)
+  int num_n_blocks;  // ceil(N / BN)
+  int num_k_blocks;  // ceil(K_bytes / 128)
+  int tiles_per_batch;
+  int total_tiles;
+  int group_m;      // m-blocks per rasterization group
+  int a_batch_mul;  // 0 broadcasts A matrix 0 over the batch, else 1
+  int b_batch_mul;
+  const float* row_scale;  // kScaleRow: sa [M]
+  const float* col_scale;  // kScaleRow: sw [N]
+  const float* scalar_a;   // kScaleScalar: device scalars
+  const float* scalar_b;
+  const __nv_bfloat16* residual;  // SPG_EPI_ADD: [M, N] row-major
+  const uint8_t* sfa;             // NVFP4 scales, blocked layout
+  const uint8_t* sfb;
+  int sf_tiles_per_row_block;  // K / 64
+  uint64_t timeout_ns;
+  unsigned int* err;
+};
+
+struct TileCoord {
+  int b, mb, nb;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int tile, const GemmParams& p) {
+  TileCoord c;
+  c.b = tile / p.tiles_per_batch;
+  const int t = tile - c.b * p.tiles_per_batch;
+  const int span = p.group_m * p.num_n_blocks;
+  const int g = t / span;
+  const int first_m = g * p.group_m;
+  const int rem = p.num_m_blocks - first_m;
+  const int gsize = rem < p.group_m ? rem : p.group_m;
+  const int local = t - g * span;
+  c.mb = first_m + local % gsize;
+  c.nb = local / gsize;
+  return c;
+}
+
+// Drain-mode wait: bounded, but not cut short by the abort flag.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t timeout_ns, unsigned int* err) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 15u) == 15u && (globaltimer_ns() - t0 > timeout_ns || i > (1u << 30))) {
+      atomicCAS(err, 0u, kErrDrain);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace spg

@@ -5,6 +5,7 @@
 #include <atomic>
 
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_2sm.cuh"
 #include "host.h"
 
 namespace spg {
@@ -32,6 +33,38 @@ spg_status launch_gemm_variant(const GemmMaps& maps, const GemmParams& p, int gr
   return launch_status();
 }
 
+// Two-SM variant: clusters of 2 CTAs, grid = 2 x pairs.
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, int grid,
+                                   cudaStream_t stream) {
+  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  auto kern = gemm_kernel_2sm<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmemBytes) != cudaSuccess)
+      return SPG_ERR_CUDA;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, p) != cudaSuccess) return SPG_ERR_CUDA;
+  return launch_status();
+}
+
 template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
 constexpr int variant_smem() {
   return GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE>::kSmemBytes;
@@ -44,7 +77,7 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.n_out = static_cast<int>(n_out);
-  p.num_m_blocks = static_cast<int>((M + 127) / 128);
+  p.num_m_blocks = static_cast<int>((M + r.block_m - 1) / r.block_m);
   p.num_n_blocks = static_cast<int>((N + r.block_n - 1) / r.block_n);
   p.num_k_blocks = static_cast<int>((K_bytes + 127) / 128);
   p.tiles_per_batch = p.num_m_blocks * p.num_n_blocks;

@@ -29,7 +29,7 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
       !aligned16(gW) || !aligned16(Y) || (epilogue == SPG_EPI_ADD && !aligned16(residual)))
     return SPG_ERR_MISALIGNED;
 
-  const spg_route r = select_route_internal(SPG_KIND_NVFP4, T, N, K, epilogue, 1);
+  const spg_route r = select_route_internal(SPG_KIND_NVFP4, T, N, K, epilogue, 1, false);
   const int64_t kh = K / 2;
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;

@@ -10,10 +10,12 @@ using namespace spg;
 namespace {
 
 template <bool A_MN, bool B_MN>
-spg_status dispatch_bn(int bn, const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
-  if (bn == 256)
-    return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 256, 4, A_MN, B_MN, kScaleScalar>(m, p, grid, s);
-  return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 128, 6, A_MN, B_MN, kScaleScalar>(m, p, grid, s);
+spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
+  if (r.block_m == 256)
+    return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 256, 6, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
+  if (r.block_n == 256)
+    return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 256, 4, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
+  return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 128, 6, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
 }
 
 }  // namespace
@@ -42,7 +44,9 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA) || !aligned16(sB))
     return SPG_ERR_MISALIGNED;
 
-  const spg_route r = select_route_internal(SPG_KIND_FP8_TENSOR, M, N, K, SPG_EPI_LINEAR, batch);
+  const spg_route r =
+      select_route_internal(SPG_KIND_FP8_TENSOR, M, N, K, SPG_EPI_LINEAR, batch, b_mn);
+  const int b_rows = r.block_m == 256 ? r.block_n / 2 : r.block_n;  // B rows staged per CTA
   const bool a_batched = batch > 1 && strideA != 0;
   const bool b_batched = batch > 1 && strideB != 0;
   const int64_t nba = a_batched ? batch : 1, nbb = b_batched ? batch : 1;
@@ -57,7 +61,7 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
       ok = make_tmap_3d(&maps.b, B, false, N, K, nbb, N, b_batched ? strideB : N * K, 128, 128, 128);
     else
       ok = make_tmap_3d(&maps.b, B, false, K, N, nbb, K, b_batched ? strideB : N * K, 128,
-                        r.block_n, 128);
+                        b_rows, 128);
   }
   if (ok)
     ok = make_tmap_3d(&maps.y, C, true, N, M, batch, N * 2, (batch > 1 ? strideC : M * N) * 2, 32,
@@ -70,8 +74,8 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
   p.b_batch_mul = b_batched ? 1 : 0;
   p.scalar_a = sA;
   p.scalar_b = sB;
-  if (!a_mn && !b_mn) return dispatch_bn<false, false>(r.block_n, maps, p, r.grid, stream);
-  if (!a_mn && b_mn) return dispatch_bn<false, true>(r.block_n, maps, p, r.grid, stream);
-  if (a_mn && !b_mn) return dispatch_bn<true, false>(r.block_n, maps, p, r.grid, stream);
-  return dispatch_bn<true, true>(r.block_n, maps, p, r.grid, stream);
+  if (!a_mn && !b_mn) return dispatch<false, false>(r, maps, p, stream);
+  if (!a_mn && b_mn) return dispatch<false, true>(r, maps, p, stream);
+  if (a_mn && !b_mn) return dispatch<true, false>(r, maps, p, stream);
+  return dispatch<true, true>(r, maps, p, stream);
 }

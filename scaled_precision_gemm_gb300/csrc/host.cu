@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -103,50 +104,82 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
 // ---------------------------------------------------------------- routes
 // Per-shape selection.  The cost compared is the one the ninfer FP8 route
 // model uses ("Routing": waves needed times the work one SM carries through
-// a wave), re-derived for 152 SMs and tcgen05 tiles: for each candidate tile
-// width, time ~ ceil(tiles / SMs) * (tile work + fixed per-tile cost), and
-// the cheapest wins.  Narrow problems (fewer tiles than SMs) prefer the
-// narrower tile, which is the AstrAI "small CTA below a tile-count
-// threshold" rule in the same terms.
+// a wave), re-derived for 152 SMs and tcgen05 tiles:
+//   cost = ceil(tiles / units) * (per-SM tile work) / (per-tile efficiency)
+// where a unit is an SM (one-CTA tiles) or an SM pair (two-SM tiles), the
+// per-SM tile work is 128 x BN x K (plus a fixed per-tile cost for the
+// epilogue tail and pipeline fill) and the efficiencies are the measured
+// steady-state tensor-pipe fractions of each tile shape on GB300.  Narrow
+// problems therefore fall back to narrower or one-CTA tiles, which is the
+// AstrAI "small CTA below a tile-count threshold" rule in the same terms.
+namespace {
+struct Candidate {
+  int block_m, block_n, stages;
+  double eff;
+  bool mn_b_ok;  // may take an N-major B operand
+};
+}  // namespace
+
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
-                                int64_t batch) {
+                                int64_t batch, bool b_mn_major) {
   spg_route r;
   std::memset(&r, 0, sizeof r);
   r.kind = kind;
-  r.block_m = 128;
   r.acc_buffers = 2;
+  r.group_m = 16;
   const int sms = num_sms();
-  const int64_t mblocks = (T + 127) / 128;
-  auto tiles_for = [&](int bn) { return mblocks * ((N + bn - 1) / bn) * (batch > 0 ? batch : 1); };
-  int bn = 256;
+  const int64_t nb = batch > 0 ? batch : 1;
   if (kind == SPG_KIND_NVFP4) {
-    bn = 128;
+    r.block_m = 128;
+    r.block_n = 128;
+    r.block_k = 256;
+    r.stages = 5;
+    r.variant = 0;
   } else {
-    // Candidate widths 256 and 128: waves x (per-tile MMA work + a fixed
-    // per-tile overhead of about 1/8 of a 256-wide K=4096 tile).
+    static const Candidate cands[] = {
+        {256, 256, 6, 1.00, true},   // two-SM pair tile
+        {128, 256, 4, 0.70, true},   // one-CTA tile
+        {128, 128, 6, 0.55, true},   // one-CTA narrow tile
+    };
     const double kb = static_cast<double>((K + 127) / 128);
-    const double overhead = 4.0;  // in units of one 128x128x128 MMA block
+    const double fixed = 6.0;  // per-tile fixed cost in 128-deep K blocks
     double best = 1e300;
-    for (int cand : {256, 128}) {
-      const int64_t tiles = tiles_for(cand);
-      const int64_t waves = (tiles + sms - 1) / sms;
-      const double cost = static_cast<double>(waves) * (kb * (cand / 128) + overhead);
-      if (cost < best - 1e-9) {
+    int best_i = 1;
+    // SPG_FORCE_VARIANT=2sm|1sm256|1sm128 pins the tile shape (A/B runs, tests).
+    int forced = -1;
+    if (const char* f = std::getenv("SPG_FORCE_VARIANT")) {
+      if (!std::strcmp(f, "2sm")) forced = 0;
+      else if (!std::strcmp(f, "1sm256")) forced = 1;
+      else if (!std::strcmp(f, "1sm128")) forced = 2;
+    }
+    for (int i = 0; i < 3; ++i) {
+      if (forced >= 0 && i != forced) continue;
+      const Candidate& c = cands[i];
+      if (b_mn_major && !c.mn_b_ok) continue;
+      const int units = c.block_m == 256 ? sms / 2 : sms;
+      const int64_t tiles = ((T + c.block_m - 1) / c.block_m) * ((N + c.block_n - 1) / c.block_n) * nb;
+      const int64_t waves = (tiles + units - 1) / units;
+      const double cost = static_cast<double>(waves) * (c.block_n / 128.0) * (kb + fixed) / c.eff;
+      if (cost < best * (1.0 - 1e-9)) {
         best = cost;
-        bn = cand;
+        best_i = i;
       }
     }
+    r.block_m = cands[best_i].block_m;
+    r.block_n = cands[best_i].block_n;
+    r.stages = cands[best_i].stages;
+    r.block_k = 128;
+    r.variant = best_i;
   }
-  r.block_n = bn;
-  r.block_k = (kind == SPG_KIND_NVFP4) ? 256 : 128;
-  if (kind == SPG_KIND_NVFP4)
-    r.stages = 5;
-  else
-    r.stages = (bn == 256) ? 4 : 6;
-  r.group_m = 16;
-  r.tiles = tiles_for(bn);
-  r.grid = static_cast<int>(r.tiles < sms ? r.tiles : sms);
-  if (r.grid < 1) r.grid = 1;
+  const int64_t tiles = ((T + r.block_m - 1) / r.block_m) * ((N + r.block_n - 1) / r.block_n) * nb;
+  r.tiles = tiles;
+  const int units = r.block_m == 256 ? sms / 2 : sms;
+  const int64_t g = tiles < units ? tiles : units;
+  r.grid = static_cast<int>((g < 1 ? 1 : g) * (r.block_m == 256 ? 2 : 1));
+  const int stage_bytes = (kind == SPG_KIND_NVFP4)
+                              ? 128 * 128 + r.block_n * 128 + 2048 + (r.block_n / 128) * 2048
+                              : 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
+  r.smem_bytes = 1024 + r.stages * stage_bytes + 4 * 2 * 2048 + 256;
   (void)epilogue;
   return r;
 }
@@ -193,6 +226,6 @@ extern "C" spg_status spg_select_route(int kind, int64_t T, int64_t N, int64_t K
   if (!out || kind < 0 || kind > 2 || T < 0 || N < 0 || K < 0 || batch < 0 || epilogue < 0 ||
       epilogue > 2)
     return SPG_ERR_INVALID_ARG;
-  *out = select_route_internal(kind, T, N, K, epilogue, batch);
+  *out = select_route_internal(kind, T, N, K, epilogue, batch, false);
   return SPG_OK;
 }

@@ -16,7 +16,8 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
                   uint32_t box1, int swizzle_bytes);
 
 // The selector behind spg_select_route (no validation).
+// b_mn_major: the B operand is N-major (per-tensor GEMM with layout_b 'N').
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
-                                int64_t batch);
+                                int64_t batch, bool b_mn_major);
 
 }  // namespace spg

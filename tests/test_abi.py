@@ -64,9 +64,12 @@ def test_sf_layout_matches_definition(lib, rows, K):
 
 def test_route_selector(lib):
     r = spg.select_route("fp8_rowscaled", 4096, 5120, 17408, "add")
-    assert r["block_m"] == 128 and r["block_n"] in (128, 256)
-    assert r["tiles"] == 32 * (5120 // r["block_n"])
-    assert 1 <= r["grid"] <= r["tiles"]
+    assert r["block_m"] in (128, 256) and r["block_n"] in (128, 256)
+    assert r["tiles"] == (4096 // r["block_m"]) * (5120 // r["block_n"])
+    per_unit = 2 if r["block_m"] == 256 else 1          # two-SM tiles run on CTA pairs
+    assert r["grid"] % per_unit == 0 and 1 <= r["grid"] // per_unit <= r["tiles"]
+    assert r["grid"] <= 152
+    assert r["smem_bytes"] <= 232448
     small = spg.select_route("fp8_rowscaled", 64, 128, 256, "linear")
     assert small["tiles"] == 1 and small["grid"] == 1
     nv = spg.select_route("nvfp4", 256, 5120, 17408, "add")
@@ -75,6 +78,17 @@ def test_route_selector(lib):
     assert b["tiles"] % 64 == 0
     with pytest.raises(spg.SpgError):
         spg.select_route(7, 1, 1, 1)
+
+
+def test_route_selector_forced_variants(lib, monkeypatch):
+    for v, (bm, bn) in {"2sm": (256, 256), "1sm256": (128, 256), "1sm128": (128, 128)}.items():
+        monkeypatch.setenv("SPG_FORCE_VARIANT", v)
+        r = spg.select_route("fp8_rowscaled", 1000, 5120, 6144, "linear")
+        assert (r["block_m"], r["block_n"]) == (bm, bn)
+    monkeypatch.delenv("SPG_FORCE_VARIANT")
+    # large square problems take the two-SM pair tile; one tiny tile takes one CTA
+    assert spg.select_route("fp8_tensor", 8192, 8192, 8192)["block_m"] == 256
+    assert spg.select_route("fp8_rowscaled", 64, 128, 256)["grid"] == 1
 
 
 def _vp(x):
