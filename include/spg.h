@@ -129,6 +129,25 @@ SPG_API spg_status spg_quantize_fp8_rows(const void* x, int64_t rows, int64_t K,
 SPG_API spg_status spg_quantize_fp8_tensor(const void* x, int64_t numel, uint8_t* codes, float* scale,
                                    float* amax_scratch, spg_stream_t stream);
 
+/* Allocation-free variant of spg_quantize_fp8_tensor (same codes and scale,
+ * bit for bit).  No counterpart on the source pages: it exists for callers
+ * that cannot allocate device memory for the amax scratch -- latency-critical
+ * paths where an allocator call may block or fail, programs running under a
+ * device-memory budget that forbids new allocations, and foreign-language
+ * callers that reach this library through its C ABI with no device allocator
+ * of their own.  The scratch is instead a file-scope device array of
+ * 4096 + 64 floats (about 16 KB) that every GPU loading the library holds
+ * until the process exits.  The caller still passes x, codes and scale.  The
+ * first call on each device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.
+ * All calls share the array: calls that overlap on the GPU (for example on
+ * two streams) race and must be ordered by the caller.  Nothing in the array
+ * needs clearing between calls.  Requires numel % 8 == 0 and
+ * numel <= 4096 * 65536 = 268,435,456 elements (SPG_ERR_UNSUPPORTED_SHAPE
+ * beyond).  Calls no allocating routine. */
+SPG_API spg_status spg_quantize_fp8_tensor_noalloc(const void* x, int64_t numel, uint8_t* codes,
+                                                   float* scale, spg_stream_t stream);
+
 /* NVFP4 global scale g = amax(x) / (448 * 6) (g = 1 when amax = 0), written
  * to the device scalar g.  The largest 16-element block scale of the tensor
  * then encodes to the E4M3 maximum 448.  ninfer PR #160 body (an E4M3 scale

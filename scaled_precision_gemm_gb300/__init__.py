@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "SpgError", "EPILOGUES", "load_library", "library_path",
-    "quantize_fp8_rows", "quantize_fp8_tensor", "nvfp4_global_scale", "quantize_nvfp4",
+    "quantize_fp8_rows", "quantize_fp8_tensor", "quantize_fp8_tensor_noalloc",
+    "nvfp4_global_scale", "quantize_nvfp4",
     "nvfp4_sf_bytes", "nvfp4_sf_offset", "fp8_rowscaled_gemm", "nvfp4_gemm", "fp8_tensor_gemm",
     "select_route", "last_device_error", "set_wait_timeout_ns", "status_string",
 ]
@@ -71,6 +72,7 @@ def load_library():
             "spg_last_device_error": (st, [vp]),
             "spg_quantize_fp8_rows": (st, [vp, i64, i64, vp, vp, vp]),
             "spg_quantize_fp8_tensor": (st, [vp, i64, vp, vp, vp, vp]),
+            "spg_quantize_fp8_tensor_noalloc": (st, [vp, i64, vp, vp, vp]),
             "spg_nvfp4_global_scale": (st, [vp, i64, vp, vp, vp]),
             "spg_quantize_nvfp4": (st, [vp, i64, i64, vp, vp, vp, vp]),
             "spg_nvfp4_sf_bytes": (ctypes.c_size_t, [i64, i64]),
@@ -164,6 +166,18 @@ def quantize_fp8_tensor(x: torch.Tensor, codes=None, scale=None, amax_scratch=No
     _check(load_library().spg_quantize_fp8_tensor(_ptr(x), x.numel(), _ptr(codes), _ptr(scale),
                                                    _ptr(scratch), _stream(x)),
            "spg_quantize_fp8_tensor")
+    return codes, scale
+
+
+def quantize_fp8_tensor_noalloc(x: torch.Tensor, codes: torch.Tensor, scale: torch.Tensor):
+    """Per-tensor FP8 quantizer whose scratch is the library's static device
+    array; the caller passes preallocated codes and scale, nothing is allocated."""
+    _need(x, "x", torch.bfloat16)
+    _need(codes, "codes", torch.uint8)
+    _need(scale, "scale", torch.float32)
+    _check(load_library().spg_quantize_fp8_tensor_noalloc(_ptr(x), x.numel(), _ptr(codes),
+                                                          _ptr(scale), _stream(x)),
+           "spg_quantize_fp8_tensor_noalloc")
     return codes, scale
 
 

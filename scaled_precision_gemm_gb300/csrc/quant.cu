@@ -8,6 +8,8 @@
 // definition, and hardware cvt.rn.satfinite conversions for the codes.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "common.h"
 #include "ptx.cuh"
 
@@ -174,6 +176,42 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
   sf[sf_word] = sf_bytes;
 }
 
+// ----------------------------------------------------------------------
+// Allocation-free variant of the per-tensor quantizer.  Its amax scratch is
+// this file-scope device array instead of a caller-provided buffer: slots
+// [0, kStaticPartials) hold one partial maximum per CTA of the first pass,
+// slot kStaticPartials holds the reduced maximum.  Every slot a call reads is
+// written earlier in the same call, so nothing has to be cleared between
+// calls; calls that overlap on the GPU share the array and race.
+constexpr int kStaticPartials = 4096;               // 16 KB of partial maxima
+constexpr int64_t kStaticElemsPerPartial = 65536;   // elements one CTA reduces
+constexpr int64_t kStaticMaxNumel = kStaticPartials * kStaticElemsPerPartial;
+static __device__ __align__(256) float g_fp8_tensor_static_scratch[kStaticPartials + 64];
+
+// Partial amax: CTA b reduces elements [b*65536, (b+1)*65536) into partials[b].
+__global__ void __launch_bounds__(256) partial_amax_kernel(const uint4* __restrict__ x,
+                                                           int64_t nvec,
+                                                           float* __restrict__ partials) {
+  __shared__ float red[8];
+  constexpr int64_t kVecPerCta = kStaticElemsPerPartial / 8;
+  const int64_t v0 = int64_t(blockIdx.x) * kVecPerCta;
+  const int64_t v1 = v0 + kVecPerCta < nvec ? v0 + kVecPerCta : nvec;
+  float a = 0.f;
+  for (int64_t i = v0 + threadIdx.x; i < v1; i += blockDim.x) a = fmaxf(a, vec_amax(__ldg(x + i)));
+  a = block_max<256>(a, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = a;
+}
+
+// Reduce partials[0, nparts) into partials[kStaticPartials] (0 when nparts == 0).
+__global__ void __launch_bounds__(1024) reduce_partials_kernel(float* __restrict__ partials,
+                                                               int nparts) {
+  __shared__ float red[32];
+  float a = 0.f;
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) a = fmaxf(a, partials[i]);
+  a = block_max<1024>(a, red);
+  if (threadIdx.x == 0) partials[kStaticPartials] = a;
+}
+
 int grid_for(int64_t work, int threads) {
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   int64_t g = (work + threads - 1) / threads;
@@ -267,4 +305,50 @@ extern "C" int64_t spg_nvfp4_sf_offset(int64_t row, int64_t kb, int64_t K) {
   const int64_t tiles_per_row_block = (K + 63) / 64;
   return ((row / 128) * tiles_per_row_block + kb / 4) * 512 + (row % 32) * 16 +
          ((row % 128) / 32) * 4 + (kb % 4);
+}
+
+// Allocation-free per-tensor FP8 quantizer (see include/spg.h).  The device
+// address of the static scratch is looked up once per device, with that
+// device current, on the first call made on it.
+namespace {
+std::mutex g_static_mu;
+float* g_static_scratch[64] = {};
+
+float* static_scratch_for_current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_scratch[d]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, spg::g_fp8_tensor_static_scratch) != cudaSuccess) return nullptr;
+    g_static_scratch[d] = static_cast<float*>(ptr);
+  }
+  return g_static_scratch[d];
+}
+}  // namespace
+
+extern "C" spg_status spg_quantize_fp8_tensor_noalloc(const void* x, int64_t numel,
+                                                      uint8_t* codes, float* scale,
+                                                      spg_stream_t stream) {
+  if (numel < 0 || !scale) return SPG_ERR_INVALID_ARG;
+  if (numel > 0 && (!x || !codes)) return SPG_ERR_INVALID_ARG;
+  if (numel % 8 != 0 || numel > spg::kStaticMaxNumel) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if ((numel > 0 && (!aligned16(x) || !aligned16(codes))) || !aligned16(scale))
+    return SPG_ERR_MISALIGNED;
+  float* scratch = static_scratch_for_current_device();
+  if (!scratch) return SPG_ERR_CUDA;
+  const int64_t nvec = numel / 8;
+  const int nparts = static_cast<int>((numel + spg::kStaticElemsPerPartial - 1) /
+                                      spg::kStaticElemsPerPartial);
+  if (nparts > 0) {
+    spg::partial_amax_kernel<<<nparts, 256, 0, stream>>>(static_cast<const uint4*>(x), nvec,
+                                                          scratch);
+    if (launch_status() != SPG_OK) return SPG_ERR_CUDA;
+  }
+  spg::reduce_partials_kernel<<<1, 1024, 0, stream>>>(scratch, nparts);
+  if (launch_status() != SPG_OK) return SPG_ERR_CUDA;
+  spg::encode_fp8_tensor_kernel<<<spg::grid_for(nvec > 0 ? nvec : 1, 256), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), nvec, scratch + spg::kStaticPartials,
+      reinterpret_cast<uint2*>(codes), scale);
+  return launch_status();
 }
