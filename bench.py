@@ -106,6 +106,30 @@ def case_name(c):
     return f"{c['kind']}_{c['epi']}_T{c['T']}_K{c['K']}_N{c['N']}"
 
 
+def gemm_source_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_precision_gemm_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "gemm_*"))) + [os.path.join(csrc, "ptx.cuh")]:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(case):
+    """DRAM bytes per launch recorded from ncu for this case, or None when no
+    capture exists or the GEMM sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = gemm_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == case and parts[2] == cur:
+            return int(parts[1])
+    return None
+
+
 # ------------------------------------------------------------ clocks
 class ClockSampler:
     """Samples the SM clock and the clock-event reasons of the benchmarked GPU
@@ -409,13 +433,7 @@ def run_gpu(args):
     dom_ms = per_case[dom_i]["gemm_us"] * 1e-3
     dom_peak = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
     achieved = case_flops(dc) / (dom_ms * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(case_name(dc))
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic(case_name(dc))
 
     # ---------------- e2e: host buffers through the public API
     e2e = None if args.no_e2e else run_e2e(args, spg, torch, dev, prepared, inputs)
