@@ -167,3 +167,139 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
 }
 
 }  // namespace spg
+
+namespace spg {
+
+// Register-drain epilogue for a single TMEM accumulator of 256 columns:
+// eight epilogue warps, two per TMEM lane quarter, each owning 128 columns.
+// A warp copies its 128 fp32 columns into registers, hands the accumulator
+// back to the MMA issuer at once, and only then scales, applies the
+// epilogue and stores -- so the next tile's main loop overlaps the math and
+// the stores although TMEM holds one accumulator (the rest of TMEM holds the
+// block scales of the NVFP4 pipeline).
+template <int EPI, int SCALE, typename TileFn, typename ArriveEmpty>
+__device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, const CUtensorMap* tmY,
+                                                       uint32_t tmem_base, uint64_t* acc_full,
+                                                       ArriveEmpty arrive_empty, uint8_t* epi_smem,
+                                                       int tile_begin, int tile_step, TileFn tile_fn,
+                                                       const WaitCtl& ctl) {
+  constexpr int kCols = 128;                 // accumulator columns per warp
+  constexpr int kBufBytes = 32 * 64;
+  constexpr int kOutChunks = EPI == SPG_EPI_SWIGLU ? 2 : 4;  // 32-wide output chunks
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int e = warp - 2;
+  const int q = warp & 3;
+  const int half = e >> 2;
+  uint8_t* stage0 = epi_smem + (e * 2) * kBufBytes;
+  int it = 0;
+  int chunk_ctr = 0;
+  float scalar = 1.f;
+  if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
+  const bool have_k = p.num_k_blocks > 0;
+
+  for (int tile = tile_begin; tile < p.total_tiles; tile += tile_step, ++it) {
+    const TileCoord tc = tile_fn(tile);
+    const int m0 = tc.mb * 128;
+    const int n_acc0 = tc.nb * 256 + half * kCols;  // first accumulator column of this warp
+    const int m = m0 + q * 32 + lane;
+    const bool row_ok = m < p.M;
+    float row_s = scalar;
+    if constexpr (SCALE == kScaleRow) row_s = row_ok ? __ldg(p.row_scale + m) : 0.f;
+    float swr[kCols / 32];
+    if constexpr (SCALE == kScaleRow) {
+#pragma unroll
+      for (int j = 0; j < kCols / 32; ++j) {
+        const int n = n_acc0 + 32 * j + lane;
+        swr[j] = n < p.N ? __ldg(p.col_scale + n) : 0.f;
+      }
+    }
+    uint4 res_cur[4];
+    if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
+
+    if (!mbar_wait(&acc_full[0], it & 1, ctl, kErrWaitAccFull)) break;
+    tc_fence_after();
+    uint32_t acc[kCols];
+    const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(half * kCols);
+    if (have_k) {
+#pragma unroll
+      for (int j = 0; j < kCols / 32; ++j)
+        tmem_ld_32x32b_x32(t_row + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(&acc[32 * j]));
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) acc[i] = 0u;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive_empty(0);
+
+#pragma unroll
+    for (int c = 0; c < kOutChunks; ++c, ++chunk_ctr) {
+      float o[32];
+      if constexpr (EPI == SPG_EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int cg = c * 64 + 2 * j;  // gate column inside this warp's 128
+          float sg = row_s, su = row_s;
+          if constexpr (SCALE == kScaleRow) {
+            sg *= __shfl_sync(0xffffffffu, swr[cg >> 5], cg & 31);
+            su *= __shfl_sync(0xffffffffu, swr[(cg + 1) >> 5], (cg + 1) & 31);
+          }
+          const float gate = __uint_as_float(acc[cg]) * sg;
+          const float up = __uint_as_float(acc[cg + 1]) * su;
+          o[j] = __fdividef(gate, 1.f + __expf(-gate)) * up;
+        }
+      } else {
+        uint4 res_next[4];
+        if constexpr (EPI == SPG_EPI_ADD) {
+          if (c + 1 < kOutChunks) load_residual_chunk(p, m, n_acc0 + 32 * (c + 1), row_ok, res_next);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float s = row_s;
+          if constexpr (SCALE == kScaleRow) s *= __shfl_sync(0xffffffffu, swr[c], j);
+          o[j] = __uint_as_float(acc[c * 32 + j]) * s;
+        }
+        if constexpr (EPI == SPG_EPI_ADD) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t w[4] = {res_cur[g].x, res_cur[g].y, res_cur[g].z, res_cur[g].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              o[g * 8 + 2 * h] += __uint_as_float(w[h] << 16);
+              o[g * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xFFFF0000u);
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) res_cur[g] = res_next[g];
+        }
+      }
+      uint8_t* sbuf = stage0 + (chunk_ctr & 1) * kBufBytes;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        uint4 pk;
+        pk.x = pack_bf16x2(o[jj * 8 + 0], o[jj * 8 + 1]);
+        pk.y = pack_bf16x2(o[jj * 8 + 2], o[jj * 8 + 3]);
+        pk.z = pack_bf16x2(o[jj * 8 + 4], o[jj * 8 + 5]);
+        pk.w = pack_bf16x2(o[jj * 8 + 6], o[jj * 8 + 7]);
+        const int phys = jj ^ ((lane >> 1) & 3);
+        *reinterpret_cast<uint4*>(sbuf + lane * 64 + phys * 16) = pk;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int out_x = (EPI == SPG_EPI_SWIGLU ? n_acc0 / 2 : n_acc0) + c * 32;
+      const int out_y = m0 + q * 32;
+      if (lane == 0) {
+        if (out_y < p.M && out_x < p.n_out) tma_store_3d(tmY, sbuf, out_x, out_y, tc.b);
+        bulk_commit();
+      }
+    }
+  }
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
+}
+
+}  // namespace spg

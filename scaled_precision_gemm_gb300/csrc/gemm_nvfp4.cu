@@ -8,8 +8,9 @@ using namespace spg;
 namespace {
 
 template <int EPI>
-spg_status launch(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm_variant<kKindNvfp4, EPI, 128, 5, false, false, kScaleScalar>(m, p, grid, s);
+spg_status launch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
+  if (r.block_m == 256) return launch_nvfp4_2sm_variant<EPI, 5>(m, p, r.grid, s);
+  return launch_gemm_variant<kKindNvfp4, EPI, 128, 5, false, false, kScaleScalar>(m, p, r.grid, s);
 }
 
 }  // namespace
@@ -34,7 +35,7 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;
   if (!make_tmap_3d(&maps.a, A, false, kh, T, 1, kh, kh * T, 128, 128, 128) ||
-      !make_tmap_3d(&maps.b, W, false, kh, N, 1, kh, kh * N, 128, r.block_n, 128) ||
+      !make_tmap_3d(&maps.b, W, false, kh, N, 1, kh, kh * N, 128, 128, 128) ||
       !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
     return SPG_ERR_CUDA;
   GemmParams p;
@@ -47,8 +48,8 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
   p.sfb = sfW;
   p.sf_tiles_per_row_block = static_cast<int>(K / 64);
   switch (epilogue) {
-    case SPG_EPI_LINEAR: return launch<SPG_EPI_LINEAR>(maps, p, r.grid, stream);
-    case SPG_EPI_ADD: return launch<SPG_EPI_ADD>(maps, p, r.grid, stream);
-    default: return launch<SPG_EPI_SWIGLU>(maps, p, r.grid, stream);
+    case SPG_EPI_LINEAR: return launch<SPG_EPI_LINEAR>(r, maps, p, stream);
+    case SPG_EPI_ADD: return launch<SPG_EPI_ADD>(r, maps, p, stream);
+    default: return launch<SPG_EPI_SWIGLU>(r, maps, p, stream);
   }
 }

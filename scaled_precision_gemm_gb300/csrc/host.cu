@@ -129,12 +129,22 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   r.group_m = 16;
   const int sms = num_sms();
   const int64_t nb = batch > 0 ? batch : 1;
+  // SPG_FORCE_VARIANT=2sm|1sm256|1sm128 pins the tile shape (A/B runs, tests).
+  int forced = -1;
+  if (const char* f = std::getenv("SPG_FORCE_VARIANT")) {
+    if (!std::strcmp(f, "2sm")) forced = 0;
+    else if (!std::strcmp(f, "1sm256")) forced = 1;
+    else if (!std::strcmp(f, "1sm128")) forced = 2;
+  }
   if (kind == SPG_KIND_NVFP4) {
-    r.block_m = 128;
-    r.block_n = 128;
+    // Two-SM 256x256 pair tile unless pinned to the one-CTA 128x128 tile.
+    const bool one_cta = forced == 1 || forced == 2;
+    r.block_m = one_cta ? 128 : 256;
+    r.block_n = one_cta ? 128 : 256;
     r.block_k = 256;
     r.stages = 5;
-    r.variant = 0;
+    r.acc_buffers = one_cta ? 2 : 1;
+    r.variant = one_cta ? 2 : 0;
   } else {
     static const Candidate cands[] = {
         {256, 256, 6, 1.00, true},   // two-SM pair tile
@@ -145,13 +155,6 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     const double fixed = 6.0;  // per-tile fixed cost in 128-deep K blocks
     double best = 1e300;
     int best_i = 1;
-    // SPG_FORCE_VARIANT=2sm|1sm256|1sm128 pins the tile shape (A/B runs, tests).
-    int forced = -1;
-    if (const char* f = std::getenv("SPG_FORCE_VARIANT")) {
-      if (!std::strcmp(f, "2sm")) forced = 0;
-      else if (!std::strcmp(f, "1sm256")) forced = 1;
-      else if (!std::strcmp(f, "1sm128")) forced = 2;
-    }
     for (int i = 0; i < 3; ++i) {
       if (forced >= 0 && i != forced) continue;
       const Candidate& c = cands[i];
@@ -176,10 +179,16 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const int units = r.block_m == 256 ? sms / 2 : sms;
   const int64_t g = tiles < units ? tiles : units;
   r.grid = static_cast<int>((g < 1 ? 1 : g) * (r.block_m == 256 ? 2 : 1));
-  const int stage_bytes = (kind == SPG_KIND_NVFP4)
-                              ? 128 * 128 + r.block_n * 128 + 2048 + (r.block_n / 128) * 2048
-                              : 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
-  r.smem_bytes = 1024 + r.stages * stage_bytes + 4 * 2 * 2048 + 256;
+  int stage_bytes, epi_warps = 4;
+  if (kind == SPG_KIND_NVFP4 && r.block_m == 256) {
+    stage_bytes = 128 * 128 + 128 * 128 + 2048 + 4096;
+    epi_warps = 8;
+  } else if (kind == SPG_KIND_NVFP4) {
+    stage_bytes = 128 * 128 + 128 * 128 + 2048 + 2048;
+  } else {
+    stage_bytes = 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
+  }
+  r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + 256;
   (void)epilogue;
   return r;
 }

@@ -366,3 +366,40 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
 }
 
 }  // namespace spg
+
+namespace spg {
+
+// Pair-wide copy of 32 rows x 128 bits from shared memory into TMEM
+// (replicated into the four lane quarters), issued by the leader CTA and
+// performed in both CTAs of the pair at the same shared offset and TMEM
+// column.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// 2-SM block-scaled E2M1 MMA with UE4M3 scales per 16 K-elements.
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Bulk copy into this CTA's shared memory completing on an mbarrier of
+// either CTA of the pair (cluster address).
+__device__ __forceinline__ void bulk_load_pair(void* dst, const void* src, uint32_t bytes,
+                                               uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(bar_cluster_addr)
+      : "memory");
+}
+
+}  // namespace spg

@@ -149,6 +149,16 @@ def test_fp8_k5120_full_size_sampled(T, N, epi):
 
 
 # ----------------------------------------------------------------- NVFP4
+@pytest.fixture(params=["auto", "1sm128"])
+def nv_variant(request, monkeypatch):
+    """Pin the NVFP4 tile shape (two-SM 256x256 or one-CTA 128x128)."""
+    if request.param == "auto":
+        monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+    else:
+        monkeypatch.setenv("SPG_FORCE_VARIANT", request.param)
+    return request.param
+
+
 def nvfp4_inputs(T, N, K, seed=0):
     x = normal_bf16((T, K), seed=seed)
     w = normal_bf16((N, K), seed=seed + 1)
@@ -176,8 +186,8 @@ def run_nvfp4(A, sfA, gA, W, sfW, gW, res, epi):
 
 @pytest.mark.parametrize("epi", ["linear", "add", "swiglu"])
 @pytest.mark.parametrize("T,N,K", [(64, 128, 256), (128, 256, 512), (200, 272, 1280),
-                                   (1, 16, 256), (333, 400, 2304)])
-def test_nvfp4_ragged(T, N, K, epi):
+                                   (1, 16, 256), (333, 400, 2304), (520, 784, 768)])
+def test_nvfp4_ragged(T, N, K, epi, nv_variant):
     A, sfA, gA, W, sfW, gW = nvfp4_inputs(T, N, K, seed=T + N)
     res = normal_bf16((T, N), seed=2) if epi == "add" else None
     y = run_nvfp4(A, sfA, gA, W, sfW, gW, res, epi)
@@ -185,7 +195,7 @@ def test_nvfp4_ragged(T, N, K, epi):
     assert_within_tol(to_f64(y), ref, f"nvfp4 {epi} {T}x{N}x{K}")
 
 
-def test_nvfp4_uniform_scales_and_linearity():
+def test_nvfp4_uniform_scales_and_linearity(nv_variant):
     # all block scales equal: isolates the E2M1 data path from the scale layout
     T, N, K = 128, 128, 512
     rng = np.random.default_rng(3)
