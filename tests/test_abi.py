@@ -73,7 +73,8 @@ def test_route_selector(lib):
     small = spg.select_route("fp8_rowscaled", 64, 128, 256, "linear")
     assert small["tiles"] == 1 and small["grid"] == 1
     nv = spg.select_route("nvfp4", 256, 5120, 17408, "add")
-    assert nv["block_n"] == 128 and nv["tiles"] == 2 * 40
+    assert (nv["block_m"], nv["block_n"]) == (256, 256) and nv["tiles"] == 20
+    assert nv["grid"] == 40 and nv["acc_buffers"] == 1
     b = spg.select_route("fp8_tensor", 512, 512, 512, "linear", batch=64)
     assert b["tiles"] % 64 == 0
     with pytest.raises(spg.SpgError):
