@@ -103,6 +103,11 @@ SPG_API void spg_set_wait_timeout_ns(uint64_t ns);
  * earlier launch) or SPG_ERR_CUDA (the stream reported an error). */
 SPG_API spg_status spg_last_device_error(spg_stream_t stream);
 
+/* Same as spg_last_device_error, and stores the raw code of the first wait
+ * that ran out (0 if none) in *code: 0x101 ring slot free, 0x102 ring slot
+ * full, 0x103 accumulator free, 0x104 accumulator full, 0x105 drain. */
+SPG_API spg_status spg_last_device_error_code(spg_stream_t stream, uint32_t* code);
+
 /* ---------------------------------------------------------------------
  * Quantizers
  * ------------------------------------------------------------------- */

@@ -70,6 +70,7 @@ def load_library():
             "spg_version": (i32, []),
             "spg_set_wait_timeout_ns": (None, [u64]),
             "spg_last_device_error": (st, [vp]),
+            "spg_last_device_error_code": (st, [vp, ctypes.POINTER(ctypes.c_uint32)]),
             "spg_quantize_fp8_rows": (st, [vp, i64, i64, vp, vp, vp]),
             "spg_quantize_fp8_tensor": (st, [vp, i64, vp, vp, vp, vp]),
             "spg_quantize_fp8_tensor_noalloc": (st, [vp, i64, vp, vp, vp]),
@@ -130,6 +131,14 @@ def last_device_error(device=None) -> int:
     """Synchronize the current stream and return (and clear) the device error status."""
     s = torch.cuda.current_stream(device)
     return int(load_library().spg_last_device_error(ctypes.c_void_p(s.cuda_stream)))
+
+
+def last_device_error_code(device=None) -> int:
+    """Synchronize, then return (and clear) the raw code of the first in-kernel wait that ran out."""
+    s = torch.cuda.current_stream(device)
+    code = ctypes.c_uint32(0)
+    load_library().spg_last_device_error_code(ctypes.c_void_p(s.cuda_stream), ctypes.byref(code))
+    return int(code.value)
 
 
 def select_route(kind, T, N, K, epilogue="linear", batch=1) -> dict:

@@ -4,7 +4,7 @@
 // tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
 // per instruction).  Per 128-byte K slice (256 E2M1 elements) each CTA
 // stages its 128 rows of A, its 128 rows of B, the 4 scale tiles of its A
-// rows (2 KB, one bulk copy) and the 4 scale tiles of each of the two
+// rows (2 KB, one TMA box) and the 4 scale tiles of each of the two
 // 128-row blocks of B (2 x 2 KB): the B scales of all 256 columns, because
 // each CTA's tensor core produces its 128 rows for every column.  The leader
 // copies the stage's scale tiles into per-stage TMEM columns of both CTAs
@@ -56,7 +56,9 @@ template <int EPI, int STAGES>
 __global__ void __maxnreg__(200)
     gemm_kernel_nvfp4_2sm(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tmY,
+                          const __grid_constant__ CUtensorMap tmSFA,
+                          const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
   using Cfg = Nvfp4PairCfg<EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -93,6 +95,8 @@ __global__ void __maxnreg__(200)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmY);
+    prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
@@ -139,10 +143,12 @@ __global__ void __maxnreg__(200)
           const int kx = kb * Cfg::kBKBytes;
           tma_load_3d_pair(sa, &tmA, bar, kx, m0, 0);
           tma_load_3d_pair(sb, &tmB, bar, kx, n0, 0);
-          const int64_t k_tile = int64_t(kb) * 4;
-          bulk_load_pair(ssfa, p.sfa + (int64_t(a_rb_sf) * tpr + k_tile) * 512, Cfg::kSfaBytes, bar);
-          bulk_load_pair(ssfb, p.sfb + (int64_t(b_rb0) * tpr + k_tile) * 512, 2048, bar);
-          bulk_load_pair(ssfb + 2048, p.sfb + (int64_t(b_rb1) * tpr + k_tile) * 512, 2048, bar);
+          // Scale tiles: 4 consecutive 512-byte tiles (one row of 128 uint32
+          // per tile in the 2-D view) = one 2 KB TMA box per 128-row block.
+          const int k_tile = kb * 4;
+          tma_load_3d_pair(ssfa, &tmSFA, bar, 0, a_rb_sf * int(tpr) + k_tile, 0);
+          tma_load_3d_pair(ssfb, &tmSFB, bar, 0, b_rb0 * int(tpr) + k_tile, 0);
+          tma_load_3d_pair(ssfb + 2048, &tmSFB, bar, 0, b_rb1 * int(tpr) + k_tile, 0);
           ++issued;
           if (++s == STAGES) {
             s = 0;

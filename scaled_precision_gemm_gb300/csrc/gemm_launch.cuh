@@ -13,6 +13,7 @@ namespace spg {
 
 struct GemmMaps {
   CUtensorMap a, b, y;
+  CUtensorMap sfa, sfb;  // NVFP4 two-SM kernel only
 };
 
 template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
@@ -94,7 +95,8 @@ spg_status launch_nvfp4_2sm_variant(const GemmMaps& maps, const GemmParams& p, i
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, p) != cudaSuccess) return SPG_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, maps.sfa, maps.sfb, p) != cudaSuccess)
+    return SPG_ERR_CUDA;
   return launch_status();
 }
 

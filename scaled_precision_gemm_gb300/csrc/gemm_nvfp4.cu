@@ -38,6 +38,15 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
       !make_tmap_3d(&maps.b, W, false, kh, N, 1, kh, kh * N, 128, 128, 128) ||
       !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
     return SPG_ERR_CUDA;
+  if (r.block_m == 256) {
+    // Scale buffers as 2-D [tiles, 128 x uint32] views: one row per 512-byte tile.
+    const uint64_t tpr = static_cast<uint64_t>(K / 64);
+    const uint64_t tiles_a = static_cast<uint64_t>((T + 127) / 128) * tpr;
+    const uint64_t tiles_b = static_cast<uint64_t>((N + 127) / 128) * tpr;
+    if (!make_tmap_2d_u32(&maps.sfa, sfA, 128, tiles_a, 512, 128, 4) ||
+        !make_tmap_2d_u32(&maps.sfb, sfW, 128, tiles_b, 512, 128, 4))
+      return SPG_ERR_CUDA;
+  }
   GemmParams p;
   fill_common_params(p, r, T, N, kh, K, n_out, 1);
   if (!p.err) return SPG_ERR_CUDA;

@@ -101,6 +101,21 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t stride1_bytes, uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  // Encoded with a third dimension of extent 1 so the kernels' 3-D TMA
+  // instruction form applies to it as to every other operand.
+  const cuuint64_t dims[3] = {d0, d1, 1};
+  const cuuint64_t strides[2] = {stride1_bytes, stride1_bytes * d1};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- routes
 // Per-shape selection.  The cost compared is the one the ninfer FP8 route
 // model uses ("Routing": waves needed times the work one SM carries through
@@ -221,6 +236,24 @@ extern "C" spg_status spg_last_device_error(spg_stream_t stream) {
   if (!p) return SPG_ERR_CUDA;
   unsigned int v = 0;
   if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SPG_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return SPG_ERR_CUDA;
+    return SPG_ERR_TIMEOUT;
+  }
+  return SPG_OK;
+}
+
+extern "C" spg_status spg_last_device_error_code(spg_stream_t stream, uint32_t* code) {
+  if (!code) return SPG_ERR_INVALID_ARG;
+  *code = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SPG_ERR_CUDA;
+  unsigned int* p = device_error_word();
+  if (!p) return SPG_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SPG_ERR_CUDA;
+  *code = v;
   if (v != 0) {
     const unsigned int zero = 0;
     if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)

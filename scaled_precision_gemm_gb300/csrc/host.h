@@ -15,6 +15,12 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
                   uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
                   uint32_t box1, int swizzle_bytes);
 
+// TMA descriptor of a 2-D array of 32-bit elements (no swizzle): d0
+// contiguous elements per row, d1 rows of stride1_bytes; box box0 x box1.
+// Encoded as rank 3 with a unit third dimension.
+bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
+
 // The selector behind spg_select_route (no validation).
 // b_mn_major: the B operand is N-major (per-tensor GEMM with layout_b 'N').
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,

@@ -391,15 +391,4 @@ __device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
-// Bulk copy into this CTA's shared memory completing on an mbarrier of
-// either CTA of the pair (cluster address).
-__device__ __forceinline__ void bulk_load_pair(void* dst, const void* src, uint32_t bytes,
-                                               uint32_t bar_cluster_addr) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(bar_cluster_addr)
-      : "memory");
-}
-
 }  // namespace spg
