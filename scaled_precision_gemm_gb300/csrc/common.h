@@ -21,9 +21,11 @@ int num_sms();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Map a CUDA error to a status; with SPG_DEBUG set in the environment the
+// error string is printed to stderr.
+spg_status cuda_status(cudaError_t e, const char* where);
+
 // Map the last launch error to a status.
-inline spg_status launch_status() {
-  return cudaGetLastError() == cudaSuccess ? SPG_OK : SPG_ERR_CUDA;
-}
+inline spg_status launch_status() { return cuda_status(cudaGetLastError(), "launch"); }
 
 }  // namespace spg

@@ -53,7 +53,9 @@ struct Nvfp4PairCfg {
 };
 
 template <int EPI, int STAGES>
-__global__ void __maxnreg__(200)
+// 10 warps: the 4 SM sub-partitions hold 3, 3, 2, 2 of them, so a thread may
+// use at most 16384 / (3 * 32) -> 168 registers.
+__global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
     gemm_kernel_nvfp4_2sm(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmY,

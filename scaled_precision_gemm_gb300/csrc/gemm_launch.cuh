@@ -26,8 +26,9 @@ spg_status launch_gemm_variant(const GemmMaps& maps, const GemmParams& p, int gr
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::kSmemBytes) != cudaSuccess)
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes),
+                    "cudaFuncSetAttribute") != SPG_OK)
       return SPG_ERR_CUDA;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -46,8 +47,9 @@ spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, in
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::kSmemBytes) != cudaSuccess)
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes),
+                    "cudaFuncSetAttribute") != SPG_OK)
       return SPG_ERR_CUDA;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -63,7 +65,9 @@ spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, p) != cudaSuccess) return SPG_ERR_CUDA;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, p), "cudaLaunchKernelEx") !=
+      SPG_OK)
+    return SPG_ERR_CUDA;
   return launch_status();
 }
 
@@ -78,8 +82,9 @@ spg_status launch_nvfp4_2sm_variant(const GemmMaps& maps, const GemmParams& p, i
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::kSmemBytes) != cudaSuccess)
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes),
+                    "cudaFuncSetAttribute") != SPG_OK)
       return SPG_ERR_CUDA;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -95,7 +100,8 @@ spg_status launch_nvfp4_2sm_variant(const GemmMaps& maps, const GemmParams& p, i
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, maps.sfa, maps.sfb, p) != cudaSuccess)
+  if (cuda_status(cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, maps.sfa, maps.sfb, p),
+                  "cudaLaunchKernelEx") != SPG_OK)
     return SPG_ERR_CUDA;
   return launch_status();
 }

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -40,6 +41,12 @@ unsigned int* device_error_word() {
     g_err_ptr[d] = static_cast<unsigned int*>(p);
   }
   return g_err_ptr[d];
+}
+
+spg_status cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return SPG_OK;
+  if (std::getenv("SPG_DEBUG")) std::fprintf(stderr, "spg: %s: %s\n", where, cudaGetErrorString(e));
+  return SPG_ERR_CUDA;
 }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
