@@ -34,14 +34,16 @@ __device__ __forceinline__ void load_residual_chunk(const GemmParams& p, int m, 
   }
 }
 
-// TileFn(tile) -> TileCoord with mb already offset for this CTA's rows;
-// ArriveEmpty(buf) releases accumulator buffer `buf` to the MMA issuer.
-template <int EPI, int SCALE, int BN, typename TileFn, typename ArriveEmpty>
+// ItemFn(item) -> WorkItem with mb already offset for this CTA's rows (a
+// whole tile has n_off = 0, width = BN); the loop runs over items
+// [item_begin, item_end) with stride item_step.  ArriveEmpty(buf) releases
+// accumulator buffer `buf` to the MMA issuer.
+template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtensorMap* tmY,
                                               uint32_t tmem_base, uint64_t* acc_full,
                                               ArriveEmpty arrive_empty, uint8_t* epi_smem,
-                                              int tile_begin, int tile_step, TileFn tile_fn,
-                                              const WaitCtl& ctl) {
+                                              int item_begin, int item_end, int item_step,
+                                              ItemFn item_fn, const WaitCtl& ctl) {
   using E = EpilogueCfg<EPI, SCALE, BN>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -54,12 +56,13 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
   const bool have_k = p.num_k_blocks > 0;
 
-  for (int tile = tile_begin; tile < p.total_tiles; tile += tile_step, ++it) {
+  for (int item = item_begin; item < item_end; item += item_step, ++it) {
     const int buf = it & 1;
     const uint32_t acc_ph = (it >> 1) & 1;
-    const TileCoord tc = tile_fn(tile);
+    const WorkItem tc = item_fn(item);
     const int m0 = tc.mb * 128;
-    const int n0 = tc.nb * BN;
+    const int n0 = tc.nb * BN + tc.n_off;  // first accumulator column of the item (global)
+    const int nch = tc.width / E::kAccColsPerChunk;
     const int m = m0 + q * 32 + lane;
     const bool row_ok = m < p.M;
 
@@ -71,7 +74,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
 #pragma unroll
       for (int j = 0; j < E::kSwRegs; ++j) {
         const int n = n0 + 32 * j + lane;
-        swr[j] = n < p.N ? __ldg(p.col_scale + n) : 0.f;
+        swr[j] = (32 * j < tc.width && n < p.N) ? __ldg(p.col_scale + n) : 0.f;
       }
     }
     uint4 res_cur[4];
@@ -82,7 +85,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
     const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
 
 #pragma unroll
-    for (int c = 0; c < E::kChunks; ++c, ++chunk_ctr) {
+    for (int c = 0; c < E::kChunks; ++c) {
+      if (c >= nch) break;
       const int acc_c0 = c * E::kAccColsPerChunk;
       uint32_t raw[E::kAccColsPerChunk];
       if (have_k) {
@@ -95,10 +99,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       }
       uint4 res_next[4];
       if constexpr (EPI == SPG_EPI_ADD) {
-        if (c + 1 < E::kChunks) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
+        if (c + 1 < nch) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
       }
       if (have_k) tmem_wait_ld();
-      if (c == E::kChunks - 1) {
+      if (c == nch - 1) {
         // Every column of this accumulator buffer has been read: hand it back.
         tc_fence_before();
         __syncwarp();
@@ -140,6 +144,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       }
       // Stage the 32 x 32 bf16 block (64-byte swizzle) and TMA-store it.
       uint8_t* sbuf = stage0 + (chunk_ctr & 1) * E::kBufBytes;
+      ++chunk_ctr;
       if (lane == 0) bulk_wait_read<1>();
       __syncwarp();
 #pragma unroll

@@ -43,12 +43,18 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
   GemmParams p;
   fill_common_params(p, r, T, N, K, K, n_out, 1);
   if (!p.err) return SPG_ERR_CUDA;
+  spg_route rr = r;
+  if (r.block_m == 256) {
+    const int pairs = num_sms() / 2;
+    plan_tail_split(p, pairs, true);
+    rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+  }
   p.row_scale = sa;
   p.col_scale = sw;
   p.residual = static_cast<const __nv_bfloat16*>(residual);
   switch (epilogue) {
-    case SPG_EPI_LINEAR: return dispatch<SPG_EPI_LINEAR>(r, maps, p, stream);
-    case SPG_EPI_ADD: return dispatch<SPG_EPI_ADD>(r, maps, p, stream);
-    default: return dispatch<SPG_EPI_SWIGLU>(r, maps, p, stream);
+    case SPG_EPI_LINEAR: return dispatch<SPG_EPI_LINEAR>(rr, maps, p, stream);
+    case SPG_EPI_ADD: return dispatch<SPG_EPI_ADD>(rr, maps, p, stream);
+    default: return dispatch<SPG_EPI_SWIGLU>(rr, maps, p, stream);
   }
 }

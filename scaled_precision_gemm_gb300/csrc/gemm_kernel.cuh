@@ -271,7 +271,12 @@ __global__ void __launch_bounds__(192, 1)
     // -------------------------------------------------------------- epilogue
     epilogue_loop<EPI, SCALE, BN>(
         p, &tmY, tmem_base, acc_full, [&](int b) { mbar_arrive(&acc_empty[b]); }, epi, blockIdx.x,
-        gridDim.x, [&](int tile) { return tile_coord(tile, p); }, ctl);
+        p.total_tiles, gridDim.x,
+        [&](int tile) {
+          const TileCoord tc = tile_coord(tile, p);
+          return WorkItem{tc.b, tc.mb, tc.nb, 0, BN};
+        },
+        ctl);
   }
 
   tc_fence_before();

@@ -15,6 +15,10 @@
 //   acc_full[b]  in both CTAs; released by one multicast tcgen05.commit.
 //   acc_empty[b] leader only; the 4 epilogue warps of each CTA arrive on it.
 // Every wait is bounded in time, as in the one-CTA kernel.
+//
+// Schedule: pair p processes work items p, p + pairs, ...; the last partial
+// wave of tiles is split along N into narrower items (work_item), whose
+// MMAs carry the narrower N in the instruction descriptor.
 #pragma once
 
 #include "gemm_epilogue.cuh"
@@ -111,10 +115,12 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.total_tiles; tile += num_pairs) {
-        const TileCoord tc = tile_coord(tile, p);
+      for (int item = pair; ok && item < p.total_items; item += num_pairs) {
+        const WorkItem tc = work_item(item, p, BN);
         const int m0 = tc.mb * 256 + int(rank) * 128;
-        const int nb0 = tc.nb * BN + int(rank) * Cfg::kBHalf;
+        // Each CTA stages its half of the item's columns (a whole 128-row box;
+        // rows past the item's half are loaded but not read by the MMA).
+        const int nb0 = tc.nb * BN + tc.n_off + int(rank) * (tc.width / 2);
         const int za = tc.b * p.a_batch_mul;
         const int zb = tc.b * p.b_batch_mul;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
@@ -160,9 +166,12 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.total_tiles; tile += num_pairs, ++it) {
+      for (int item = pair; ok && item < p.total_items; item += num_pairs, ++it) {
         const int buf = it & 1;
         const uint32_t acc_ph = (it >> 1) & 1;
+        const int width = work_item(item, p, BN).width;
+        // The instruction descriptor's N field carries the item's width.
+        const uint32_t idesc = (kIdesc & ~(0x3Fu << 17)) | (uint32_t(width >> 3) << 17);
         if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
@@ -185,7 +194,7 @@ __global__ void __launch_bounds__(192, 1)
               bdesc = smem_desc(sb + j * 32 * 128, 16384, 1024, kSwizzle128B);
             else
               bdesc = smem_desc(sb + j * 32, 16, 1024, kSwizzle128B);
-            mma_f8f6f4_pair(d_tmem, adesc, bdesc, kIdesc, (kb | j) != 0);
+            mma_f8f6f4_pair(d_tmem, adesc, bdesc, idesc, (kb | j) != 0);
           }
           tc_commit_pair_multicast(&empty[s], 0x3);
           if (++s == STAGES) {
@@ -204,11 +213,11 @@ __global__ void __launch_bounds__(192, 1)
     epilogue_loop<EPI, SCALE, BN>(
         p, &tmY, tmem_base, acc_full,
         [&](int b) { mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0)); }, epi, pair,
-        num_pairs,
-        [&](int tile) {
-          TileCoord tc = tile_coord(tile, p);
-          tc.mb = tc.mb * 2 + int(rank);
-          return tc;
+        p.total_items, num_pairs,
+        [&](int item) {
+          WorkItem w = work_item(item, p, BN);
+          w.mb = w.mb * 2 + int(rank);
+          return w;
         },
         ctl);
   }

@@ -41,8 +41,21 @@ struct GemmParams {
   const uint8_t* sfa;             // NVFP4 scales, blocked layout
   const uint8_t* sfb;
   int sf_tiles_per_row_block;  // K / 64
+  // Tail split (two-SM kernels): work items [0, split_full) are whole tiles;
+  // the remaining tiles are each split along N into split_ways pieces so the
+  // last, partial wave is split_ways times shorter.  total_items counts both.
+  int split_full;
+  int split_ways;
+  int total_items;
   uint64_t timeout_ns;
   unsigned int* err;
+};
+
+// One unit of work of the persistent schedule: a tile, or a piece of one.
+struct WorkItem {
+  int b, mb, nb;  // batch, m-block, n-block of the tile
+  int n_off;      // first accumulator column of the piece inside the tile
+  int width;      // accumulator columns of the piece
 };
 
 struct TileCoord {
@@ -62,6 +75,23 @@ __device__ __forceinline__ TileCoord tile_coord(int tile, const GemmParams& p) {
   c.mb = first_m + local % gsize;
   c.nb = local / gsize;
   return c;
+}
+
+__device__ __forceinline__ WorkItem work_item(int item, const GemmParams& p, int bn) {
+  WorkItem w;
+  int tile = item, piece = 0, ways = 1;
+  if (item >= p.split_full) {
+    ways = p.split_ways;
+    tile = p.split_full + (item - p.split_full) / ways;
+    piece = (item - p.split_full) % ways;
+  }
+  const TileCoord tc = tile_coord(tile, p);
+  w.b = tc.b;
+  w.mb = tc.mb;
+  w.nb = tc.nb;
+  w.width = bn / ways;
+  w.n_off = piece * w.width;
+  return w;
 }
 
 // Drain-mode wait: bounded, but not cut short by the abort flag.

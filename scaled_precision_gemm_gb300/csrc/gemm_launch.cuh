@@ -130,10 +130,25 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
   p.residual = nullptr;
   p.sfa = p.sfb = nullptr;
   p.sf_tiles_per_row_block = 0;
+  p.split_full = p.total_tiles;
+  p.split_ways = 1;
+  p.total_items = p.total_tiles;
   p.timeout_ns = wait_timeout_ns();
   p.err = device_error_word();
 }
 
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+// Split the last partial wave of a two-SM schedule along N: with U pairs and
+// P tiles, the P mod U tiles of the last wave become 2 or 4 narrower items
+// each (the most that still fit in that wave), so the wave ends 2 or 4 times
+// sooner.  A problem of fewer than U tiles is one partial wave.
+inline void plan_tail_split(GemmParams& p, int units, bool allowed) {
+  const int tiles = p.total_tiles;
+  const int ways = allowed ? tail_split_ways(tiles, units) : 1;
+  p.split_ways = ways;
+  p.split_full = ways > 1 ? tiles - tiles % units : tiles;
+  p.total_items = p.split_full + (tiles - p.split_full) * p.split_ways;
+}
 
 }  // namespace spg

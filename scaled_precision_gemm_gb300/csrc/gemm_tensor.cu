@@ -70,12 +70,19 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
   GemmParams p;
   fill_common_params(p, r, M, N, K, K, N, batch);
   if (!p.err) return SPG_ERR_CUDA;
+  // An N-major B half is one 128-byte swizzle row: keep whole tiles there.
+  spg_route rr = r;
+  if (r.block_m == 256) {
+    const int pairs = num_sms() / 2;
+    plan_tail_split(p, pairs, !b_mn);
+    rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+  }
   p.a_batch_mul = a_batched ? 1 : 0;
   p.b_batch_mul = b_batched ? 1 : 0;
   p.scalar_a = sA;
   p.scalar_b = sB;
-  if (!a_mn && !b_mn) return dispatch<false, false>(r, maps, p, stream);
-  if (!a_mn && b_mn) return dispatch<false, true>(r, maps, p, stream);
-  if (a_mn && !b_mn) return dispatch<true, false>(r, maps, p, stream);
-  return dispatch<true, true>(r, maps, p, stream);
+  if (!a_mn && !b_mn) return dispatch<false, false>(rr, maps, p, stream);
+  if (!a_mn && b_mn) return dispatch<false, true>(rr, maps, p, stream);
+  if (a_mn && !b_mn) return dispatch<true, false>(rr, maps, p, stream);
+  return dispatch<true, true>(rr, maps, p, stream);
 }

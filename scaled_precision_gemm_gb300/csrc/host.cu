@@ -183,8 +183,12 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
       if (b_mn_major && !c.mn_b_ok) continue;
       const int units = c.block_m == 256 ? sms / 2 : sms;
       const int64_t tiles = ((T + c.block_m - 1) / c.block_m) * ((N + c.block_n - 1) / c.block_n) * nb;
-      const int64_t waves = (tiles + units - 1) / units;
-      const double cost = static_cast<double>(waves) * (c.block_n / 128.0) * (kb + fixed) / c.eff;
+      // Whole waves, plus the last partial wave shortened by the tail split
+      // of the two-SM kernel (when B is K-major).
+      const int ways = (c.block_m == 256 && !b_mn_major) ? tail_split_ways(tiles, units) : 1;
+      const double waves =
+          static_cast<double>(tiles / units) + ((tiles % units) ? 1.0 / ways : 0.0);
+      const double cost = waves * (c.block_n / 128.0) * (kb + fixed) / c.eff;
       if (cost < best * (1.0 - 1e-9)) {
         best = cost;
         best_i = i;
@@ -199,7 +203,12 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const int64_t tiles = ((T + r.block_m - 1) / r.block_m) * ((N + r.block_n - 1) / r.block_n) * nb;
   r.tiles = tiles;
   const int units = r.block_m == 256 ? sms / 2 : sms;
-  const int64_t g = tiles < units ? tiles : units;
+  int64_t items = tiles;
+  if (r.block_m == 256 && kind != SPG_KIND_NVFP4 && !b_mn_major) {
+    const int ways = tail_split_ways(tiles, units);
+    items = tiles - tiles % units + (tiles % units) * ways;
+  }
+  const int64_t g = items < units ? items : units;
   r.grid = static_cast<int>((g < 1 ? 1 : g) * (r.block_m == 256 ? 2 : 1));
   int stage_bytes, epi_warps = 4;
   if (kind == SPG_KIND_NVFP4 && r.block_m == 256) {

@@ -21,6 +21,17 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
 bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
 
+// Tail split of a two-SM schedule (see plan_tail_split): with `units` CTA
+// pairs and `tiles` tiles, the tiles of the last partial wave are split into
+// `ways` (1, 2 or 4) narrower items.
+inline int tail_split_ways(int64_t tiles, int64_t units) {
+  if (units <= 0) return 1;
+  const int64_t rem = tiles % units;
+  if (rem > 0 && rem * 4 <= units) return 4;
+  if (rem > 0 && rem * 2 <= units) return 2;
+  return 1;
+}
+
 // The selector behind spg_select_route (no validation).
 // b_mn_major: the B operand is N-major (per-tensor GEMM with layout_b 'N').
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
