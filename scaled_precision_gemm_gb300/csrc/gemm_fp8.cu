@@ -8,8 +8,17 @@ namespace {
 
 template <int EPI>
 spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
-  if (r.block_m == 256)
+  if (r.block_m == 256) {
+    if (r.block_n == 192)
+      return launch_gemm_2sm_variant<EPI, 192, 7, false, false, kScaleRow>(m, p, r.grid, s);
+    if constexpr (EPI != SPG_EPI_SWIGLU) {
+      if (r.block_n == 160)
+        return launch_gemm_2sm_variant<EPI, 160, 7, false, false, kScaleRow>(m, p, r.grid, s);
+    }
+    if (r.block_n == 128)
+      return launch_gemm_2sm_variant<EPI, 128, 8, false, false, kScaleRow>(m, p, r.grid, s);
     return launch_gemm_2sm_variant<EPI, 256, 6, false, false, kScaleRow>(m, p, r.grid, s);
+  }
   if (r.block_n == 256)
     return launch_gemm_variant<kKindFp8, EPI, 256, 4, false, false, kScaleRow>(m, p, r.grid, s);
   return launch_gemm_variant<kKindFp8, EPI, 128, 6, false, false, kScaleRow>(m, p, r.grid, s);
@@ -46,7 +55,7 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
   spg_route rr = r;
   if (r.block_m == 256) {
     const int pairs = num_sms() / 2;
-    plan_tail_split(p, pairs, true);
+    plan_tail_split(p, pairs, r.block_n, epilogue, true);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
   }
   p.row_scale = sa;

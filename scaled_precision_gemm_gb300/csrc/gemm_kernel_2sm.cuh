@@ -42,7 +42,9 @@ struct Gemm2smCfg {
   static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
   static constexpr int kThreads = 192;
 
-  static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
+  static_assert(BN == 128 || BN == 160 || BN == 192 || BN == 256,
+                "pair tiles are 256 x {128, 160, 192, 256}");
+  static_assert(EPI != SPG_EPI_SWIGLU || BN % 64 == 0, "SwiGLU tiles hold whole 64-column chunks");
   static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");

@@ -143,9 +143,9 @@ constexpr int64_t kMaxDim = 0x7FFFFFFF;
 // P tiles, the P mod U tiles of the last wave become 2 or 4 narrower items
 // each (the most that still fit in that wave), so the wave ends 2 or 4 times
 // sooner.  A problem of fewer than U tiles is one partial wave.
-inline void plan_tail_split(GemmParams& p, int units, bool allowed) {
+inline void plan_tail_split(GemmParams& p, int units, int bn, int epilogue, bool allowed) {
   const int tiles = p.total_tiles;
-  const int ways = allowed ? tail_split_ways(tiles, units) : 1;
+  const int ways = allowed ? tail_split_ways(tiles, units, bn, epilogue) : 1;
   p.split_ways = ways;
   p.split_full = ways > 1 ? tiles - tiles % units : tiles;
   p.total_items = p.split_full + (tiles - p.split_full) * p.split_ways;

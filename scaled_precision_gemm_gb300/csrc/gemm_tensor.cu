@@ -11,8 +11,17 @@ namespace {
 
 template <bool A_MN, bool B_MN>
 spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
-  if (r.block_m == 256)
+  if (r.block_m == 256) {
+    if constexpr (!B_MN) {
+      if (r.block_n == 192)
+        return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 192, 7, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
+      if (r.block_n == 160)
+        return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 160, 7, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
+      if (r.block_n == 128)
+        return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 128, 8, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
+    }
     return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 256, 6, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
+  }
   if (r.block_n == 256)
     return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 256, 4, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
   return launch_gemm_variant<kKindFp8, SPG_EPI_LINEAR, 128, 6, A_MN, B_MN, kScaleScalar>(m, p, r.grid, s);
@@ -74,7 +83,7 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
   spg_route rr = r;
   if (r.block_m == 256) {
     const int pairs = num_sms() / 2;
-    plan_tail_split(p, pairs, !b_mn);
+    plan_tail_split(p, pairs, r.block_n, SPG_EPI_LINEAR, !b_mn);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
   }
   p.a_batch_mul = a_batched ? 1 : 0;

@@ -151,16 +151,15 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   r.group_m = 16;
   const int sms = num_sms();
   const int64_t nb = batch > 0 ? batch : 1;
-  // SPG_FORCE_VARIANT=2sm|1sm256|1sm128 pins the tile shape (A/B runs, tests).
-  int forced = -1;
-  if (const char* f = std::getenv("SPG_FORCE_VARIANT")) {
-    if (!std::strcmp(f, "2sm")) forced = 0;
-    else if (!std::strcmp(f, "1sm256")) forced = 1;
-    else if (!std::strcmp(f, "1sm128")) forced = 2;
-  }
+  // SPG_FORCE_VARIANT pins the tile shape for A/B runs and tests:
+  // 2sm | 2sm192 | 2sm160 | 2sm128 (pair tiles), 1sm256 | 1sm128 (one CTA).
+  const char* forced_name = std::getenv("SPG_FORCE_VARIANT");
+  if (forced_name && !*forced_name) forced_name = nullptr;
+  const bool force_one_cta =
+      forced_name && (!std::strcmp(forced_name, "1sm256") || !std::strcmp(forced_name, "1sm128"));
   if (kind == SPG_KIND_NVFP4) {
     // Two-SM 256x256 pair tile unless pinned to the one-CTA 128x128 tile.
-    const bool one_cta = forced == 1 || forced == 2;
+    const bool one_cta = force_one_cta;
     r.block_m = one_cta ? 128 : 256;
     r.block_n = one_cta ? 128 : 256;
     r.block_k = 256;
@@ -168,24 +167,31 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     r.acc_buffers = one_cta ? 2 : 1;
     r.variant = one_cta ? 2 : 0;
   } else {
+    // Pair tiles first (widths 256/192/160/128), then one-CTA tiles.  The
+    // efficiencies are steady-state tensor-pipe fractions measured on GB300
+    // relative to the 256-wide pair tile.
     static const Candidate cands[] = {
-        {256, 256, 6, 1.00, true},   // two-SM pair tile
-        {128, 256, 4, 0.70, true},   // one-CTA tile
-        {128, 128, 6, 0.55, true},   // one-CTA narrow tile
+        {256, 256, 6, 1.00, true},  {256, 192, 7, 0.97, false}, {256, 160, 7, 0.94, false},
+        {256, 128, 8, 0.88, false}, {128, 256, 4, 0.62, true},  {128, 128, 6, 0.50, true},
     };
+    constexpr int kCands = sizeof(cands) / sizeof(cands[0]);
+    static const char* const kNames[kCands] = {"2sm", "2sm192", "2sm160", "2sm128", "1sm256",
+                                               "1sm128"};
     const double kb = static_cast<double>((K + 127) / 128);
     const double fixed = 6.0;  // per-tile fixed cost in 128-deep K blocks
     double best = 1e300;
-    int best_i = 1;
-    for (int i = 0; i < 3; ++i) {
-      if (forced >= 0 && i != forced) continue;
+    int best_i = 0;
+    for (int i = 0; i < kCands; ++i) {
       const Candidate& c = cands[i];
+      if (forced_name && std::strcmp(forced_name, kNames[i]) != 0) continue;
       if (b_mn_major && !c.mn_b_ok) continue;
+      if (epilogue == SPG_EPI_SWIGLU && c.block_n % 64 != 0) continue;
       const int units = c.block_m == 256 ? sms / 2 : sms;
       const int64_t tiles = ((T + c.block_m - 1) / c.block_m) * ((N + c.block_n - 1) / c.block_n) * nb;
       // Whole waves, plus the last partial wave shortened by the tail split
       // of the two-SM kernel (when B is K-major).
-      const int ways = (c.block_m == 256 && !b_mn_major) ? tail_split_ways(tiles, units) : 1;
+      const int ways =
+          (c.block_m == 256 && !b_mn_major) ? tail_split_ways(tiles, units, c.block_n, epilogue) : 1;
       const double waves =
           static_cast<double>(tiles / units) + ((tiles % units) ? 1.0 / ways : 0.0);
       const double cost = waves * (c.block_n / 128.0) * (kb + fixed) / c.eff;
@@ -205,7 +211,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const int units = r.block_m == 256 ? sms / 2 : sms;
   int64_t items = tiles;
   if (r.block_m == 256 && kind != SPG_KIND_NVFP4 && !b_mn_major) {
-    const int ways = tail_split_ways(tiles, units);
+    const int ways = tail_split_ways(tiles, units, r.block_n, epilogue);
     items = tiles - tiles % units + (tiles % units) * ways;
   }
   const int64_t g = items < units ? items : units;
@@ -218,6 +224,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     stage_bytes = 128 * 128 + 128 * 128 + 2048 + 2048;
   } else {
     stage_bytes = 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
+    if (r.block_m == 256) epi_warps = 4;
   }
   r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + 256;
   (void)epilogue;

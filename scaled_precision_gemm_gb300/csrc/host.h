@@ -22,13 +22,16 @@ bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t 
                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
 
 // Tail split of a two-SM schedule (see plan_tail_split): with `units` CTA
-// pairs and `tiles` tiles, the tiles of the last partial wave are split into
-// `ways` (1, 2 or 4) narrower items.
-inline int tail_split_ways(int64_t tiles, int64_t units) {
+// pairs and `tiles` tiles of width bn, the tiles of the last partial wave
+// are split into `ways` (1, 2 or 4) narrower items, each a whole number of
+// epilogue chunks wide (32 columns, 64 for SwiGLU).
+inline int tail_split_ways(int64_t tiles, int64_t units, int bn, int epilogue) {
   if (units <= 0) return 1;
   const int64_t rem = tiles % units;
-  if (rem > 0 && rem * 4 <= units) return 4;
-  if (rem > 0 && rem * 2 <= units) return 2;
+  const int chunk = epilogue == SPG_EPI_SWIGLU ? 64 : 32;
+  for (int ways : {4, 2}) {
+    if (rem > 0 && rem * ways <= units && bn % (ways * chunk) == 0) return ways;
+  }
   return 1;
 }
 

@@ -83,7 +83,8 @@ def test_route_selector(lib):
 
 
 def test_route_selector_forced_variants(lib, monkeypatch):
-    for v, (bm, bn) in {"2sm": (256, 256), "1sm256": (128, 256), "1sm128": (128, 128)}.items():
+    for v, (bm, bn) in {"2sm": (256, 256), "2sm192": (256, 192), "2sm160": (256, 160),
+                        "2sm128": (256, 128), "1sm256": (128, 256), "1sm128": (128, 128)}.items():
         monkeypatch.setenv("SPG_FORCE_VARIANT", v)
         r = spg.select_route("fp8_rowscaled", 1000, 5120, 6144, "linear")
         assert (r["block_m"], r["block_n"]) == (bm, bn)
@@ -91,9 +92,11 @@ def test_route_selector_forced_variants(lib, monkeypatch):
     # large square problems take the two-SM pair tile; one tiny tile takes one CTA
     assert spg.select_route("fp8_tensor", 8192, 8192, 8192)["block_m"] == 256
     assert spg.select_route("fp8_rowscaled", 64, 128, 256)["tiles"] == 1
-    # tail split: 80 pair tiles on 76 pairs -> the 4 tail tiles become 16 items
+    # T=1024 x N=5120: a pair tile narrower than 256 fills the 76 pairs better
+    # than the 80 tiles of the 256-wide one (one full wave + 4 tiles)
     r = spg.select_route("fp8_rowscaled", 1024, 5120, 17408, "add")
-    assert (r["block_m"], r["tiles"], r["grid"]) == (256, 80, 152)
+    assert r["block_m"] == 256 and r["grid"] == 152
+    assert r["tiles"] == 4 * ((5120 + r["block_n"] - 1) // r["block_n"])
 
 
 def _vp(x):

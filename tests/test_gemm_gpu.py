@@ -20,12 +20,15 @@ from tests.helpers import assert_within_tol, sf_rowmajor_to_blocked
 
 pytestmark = pytest.mark.gpu
 GUARD = 64
-VARIANTS = ["auto", "2sm", "1sm256", "1sm128"]
+VARIANTS = ["auto", "2sm", "2sm192", "2sm160", "2sm128", "1sm256", "1sm128"]
 
 
 @pytest.fixture(params=VARIANTS)
 def variant(request, monkeypatch):
-    """Pin the FP8 tile shape (two-SM 256x256, one-CTA 128x256, one-CTA 128x128)."""
+    """Pin the FP8 tile shape: two-SM 256 x {256, 192, 160, 128}, one-CTA 128 x {256, 128}.
+
+    A pin the shape cannot take (SwiGLU needs 64-column multiples; an N-major B
+    needs the 256-wide pair tile) falls back to the selector's choice."""
     if request.param == "auto":
         monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
     else:
