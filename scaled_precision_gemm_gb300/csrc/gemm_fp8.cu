@@ -57,6 +57,9 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
     const int pairs = num_sms() / 2;
     plan_tail_split(p, pairs, r.block_n, epilogue, true);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+    const uint32_t narrow_rows = static_cast<uint32_t>(r.block_n / p.split_ways / 2);
+    if (!make_tmap_3d(&maps.b_narrow, W, false, K, N, 1, K, K * N, 128, narrow_rows, 128))
+      return SPG_ERR_CUDA;
   }
   p.row_scale = sa;
   p.col_scale = sw;

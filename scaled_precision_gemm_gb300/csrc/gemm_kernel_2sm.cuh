@@ -60,7 +60,8 @@ struct Gemm2smCfg {
 template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmY,
+                    const __grid_constant__ CUtensorMap tmBnarrow, const GemmParams p) {
   using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmY);
+    if (p.split_ways > 1) prefetch_tmap(&tmBnarrow);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
@@ -120,8 +122,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int item = pair; ok && item < p.total_items; item += num_pairs) {
         const WorkItem tc = work_item(item, p, BN);
         const int m0 = tc.mb * 256 + int(rank) * 128;
-        // Each CTA stages its half of the item's columns (a whole 128-row box;
-        // rows past the item's half are loaded but not read by the MMA).
+        // Each CTA stages its half of the item's columns.
         const int nb0 = tc.nb * BN + tc.n_off + int(rank) * (tc.width / 2);
         const int za = tc.b * p.a_batch_mul;
         const int zb = tc.b * p.b_batch_mul;
@@ -132,7 +133,10 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* sa = ring + s * Cfg::kStageBytes;
           uint8_t* sb = sa + Cfg::kABytes;
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kStageBytes);
+          // A narrower item stages only its B rows (the narrow box map).
+          const bool narrow = tc.width < BN;
+          const uint32_t b_bytes = narrow ? uint32_t(tc.width / 2) * Cfg::kBKBytes : Cfg::kBBytes;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (Cfg::kABytes + b_bytes));
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
           const int kx = kb * Cfg::kBKBytes;
           if constexpr (A_MN)
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (B_MN)
             tma_load_3d_pair(sb, &tmB, bar, nb0, kx, zb);
           else
-            tma_load_3d_pair(sb, &tmB, bar, kx, nb0, zb);
+            tma_load_3d_pair(sb, narrow ? &tmBnarrow : &tmB, bar, kx, nb0, zb);
           ++issued;
           if (++s == STAGES) {
             s = 0;

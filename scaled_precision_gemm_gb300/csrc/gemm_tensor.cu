@@ -85,6 +85,14 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
     const int pairs = num_sms() / 2;
     plan_tail_split(p, pairs, r.block_n, SPG_EPI_LINEAR, !b_mn);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+    if (!b_mn) {
+      const uint32_t narrow_rows = static_cast<uint32_t>(r.block_n / p.split_ways / 2);
+      if (!make_tmap_3d(&maps.b_narrow, B, false, K, N, nbb, K, b_batched ? strideB : N * K, 128,
+                        narrow_rows, 128))
+        return SPG_ERR_CUDA;
+    } else {
+      maps.b_narrow = maps.b;
+    }
   }
   p.a_batch_mul = a_batched ? 1 : 0;
   p.b_batch_mul = b_batched ? 1 : 0;

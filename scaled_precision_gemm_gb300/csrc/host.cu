@@ -171,8 +171,8 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     // efficiencies are steady-state tensor-pipe fractions measured on GB300
     // relative to the 256-wide pair tile.
     static const Candidate cands[] = {
-        {256, 256, 6, 1.00, true},  {256, 192, 7, 0.97, false}, {256, 160, 7, 0.94, false},
-        {256, 128, 8, 0.88, false}, {128, 256, 4, 0.62, true},  {128, 128, 6, 0.50, true},
+        {256, 256, 6, 1.00, true},  {256, 192, 7, 0.87, false}, {256, 160, 7, 0.75, false},
+        {256, 128, 8, 0.62, false}, {128, 256, 4, 0.80, true},  {128, 128, 6, 0.62, true},
     };
     constexpr int kCands = sizeof(cands) / sizeof(cands[0]);
     static const char* const kNames[kCands] = {"2sm", "2sm192", "2sm160", "2sm128", "1sm256",
@@ -193,7 +193,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
       const int ways =
           (c.block_m == 256 && !b_mn_major) ? tail_split_ways(tiles, units, c.block_n, epilogue) : 1;
       const double waves =
-          static_cast<double>(tiles / units) + ((tiles % units) ? 1.0 / ways : 0.0);
+          static_cast<double>(tiles / units) + ((tiles % units) ? tail_item_time(ways) : 0.0);
       const double cost = waves * (c.block_n / 128.0) * (kb + fixed) / c.eff;
       if (cost < best * (1.0 - 1e-9)) {
         best = cost;

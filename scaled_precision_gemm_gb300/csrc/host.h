@@ -35,6 +35,10 @@ inline int tail_split_ways(int64_t tiles, int64_t units, int bn, int epilogue) {
   return 1;
 }
 
+// Relative duration of a tail item split `ways` ways: its MMAs shrink with
+// the width but the A operand it stages does not (measured on GB300).
+inline double tail_item_time(int ways) { return ways <= 1 ? 1.0 : 0.45 + 0.55 / ways; }
+
 // The selector behind spg_select_route (no validation).
 // b_mn_major: the B operand is N-major (per-tensor GEMM with layout_b 'N').
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
