@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
       for (uint32_t i = 0; i < outstanding; ++i) {
         const uint32_t idx = issued - 1 - i;
-        mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.timeout_ns, p.err);
+        mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
       }
     }
   } else if (warp == 1) {
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       // All MMAs (and scale copies) must be complete before TMEM is freed.
       tc_commit(drain);
-      mbar_wait_drain(drain, 0, p.timeout_ns, p.err);
+      mbar_wait_drain(drain, 0, p.drain_ns, p.err);
     }
   } else {
     // -------------------------------------------------------------- epilogue

@@ -47,7 +47,8 @@ struct GemmParams {
   int split_full;
   int split_ways;
   int total_items;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // bound of every pipeline wait
+  uint64_t drain_ns;    // bound of the exit waits for copies / MMAs in flight
   unsigned int* err;
 };
 

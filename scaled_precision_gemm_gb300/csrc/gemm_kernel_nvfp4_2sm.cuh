@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
         const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
         for (uint32_t i = 0; i < outstanding; ++i) {
           const uint32_t idx = issued - 1 - i;
-          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.timeout_ns, p.err);
+          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
         }
       }
     }
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
         tc_commit_pair_multicast(acc_full, 0x3);
       }
       tc_commit_pair(drain);
-      mbar_wait_drain(drain, 0, p.timeout_ns, p.err);
+      mbar_wait_drain(drain, 0, p.drain_ns, p.err);
     }
   } else {
     // -------------------------------------------------------------- epilogue

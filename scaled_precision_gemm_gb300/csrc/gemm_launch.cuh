@@ -135,6 +135,9 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
   p.split_ways = 1;
   p.total_items = p.total_tiles;
   p.timeout_ns = wait_timeout_ns();
+  // Exit waits keep a generous bound even under a short pipeline bound, so a
+  // CTA never leaves with a copy or an MMA still writing its memory.
+  p.drain_ns = p.timeout_ns > 1000000000ull ? p.timeout_ns : 1000000000ull;
   p.err = device_error_word();
 }
 

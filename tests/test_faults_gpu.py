@@ -1,0 +1,60 @@
+"""Failure detection without a GPU fault.
+
+Every in-kernel wait is bounded in time.  Shrinking the bound to 1 ns makes
+the waits of a normal GEMM run out (the epilogue's wait for the accumulator
+cannot be satisfied within a few polls); the kernel must then record the
+time-out in the device error word, drain the copies and MMAs it has in flight,
+free its tensor memory and return, so that the host reads SPG_ERR_TIMEOUT and
+the context stays usable.  The one-CTA kernel is pinned: its drain covers all
+of its own copies.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_precision_gemm_gb300 as spg
+from synthetic_inputs import normal_bf16
+from tests.gpu_common import DEV, cuda, to_f64
+from tests.helpers import assert_within_tol
+
+pytestmark = pytest.mark.gpu
+
+WAIT_CODES = {0x101, 0x102, 0x103, 0x104}
+
+
+def _inputs(T, N, K):
+    A, sa = oracle.quantize_fp8_rows(normal_bf16((T, K), seed=0))
+    W, sw = oracle.quantize_fp8_rows(normal_bf16((N, K), seed=1))
+    return A, sa, W, sw
+
+
+def test_wait_timeout_is_reported_and_context_survives(monkeypatch):
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "1sm256")
+    T, N, K = 512, 512, 4096
+    A, sa, W, sw = _inputs(T, N, K)
+    args = (cuda(A), cuda(sa), cuda(W), cuda(sw))
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    spg.set_wait_timeout_ns(1)
+    try:
+        spg.fp8_rowscaled_gemm(*args)
+        code = spg.last_device_error_code()
+    finally:
+        spg.set_wait_timeout_ns(2_000_000_000)
+    assert code in WAIT_CODES, hex(code)
+    assert spg.last_device_error() == 0          # reading the code cleared it
+    # the context is intact: the same call now completes and is correct
+    y = spg.fp8_rowscaled_gemm(*args)
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    assert_within_tol(to_f64(y), oracle.fp8_rowscaled_gemm(A, sa, W, sw), "after time-out")
+
+
+def test_status_codes_are_distinct_for_host_errors():
+    with pytest.raises(spg.SpgError) as e:
+        spg.fp8_rowscaled_gemm(torch.zeros((4, 24), dtype=torch.uint8, device=DEV),
+                               torch.ones(4, device=DEV),
+                               torch.zeros((8, 24), dtype=torch.uint8, device=DEV),
+                               torch.ones(8, device=DEV))
+    assert e.value.status == 2          # K % 16
