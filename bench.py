@@ -532,6 +532,8 @@ def run_e2e(args, spg, torch, dev, prepared, inputs):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(compute)
+    for st in (s_h2d, s_d2h):      # copies start after the opening event
+        st.wait_stream(compute)
     for _ in range(reps):
         e2e_step()
     for st in (s_h2d, s_d2h):
