@@ -98,6 +98,13 @@ SPG_API int spg_version(void);
  * launches. */
 SPG_API void spg_set_wait_timeout_ns(uint64_t ns);
 
+/* Test hook for failure detection: while enabled, every launch of the
+ * one-CTA GEMM kernels makes its epilogue wait on a barrier that nothing
+ * arrives on, so that wait runs out after the bound set above, the kernel
+ * records code 0x106 and every role drains and returns without a fault.
+ * Host-side setting; not thread-safe against concurrent launches. */
+SPG_API void spg_debug_inject_stall(int enable);
+
 /* Synchronizes `stream`, then reads and clears the library's device error
  * word.  Returns SPG_OK, SPG_ERR_TIMEOUT (a bounded wait ran out in some
  * earlier launch) or SPG_ERR_CUDA (the stream reported an error). */
@@ -105,7 +112,8 @@ SPG_API spg_status spg_last_device_error(spg_stream_t stream);
 
 /* Same as spg_last_device_error, and stores the raw code of the first wait
  * that ran out (0 if none) in *code: 0x101 ring slot free, 0x102 ring slot
- * full, 0x103 accumulator free, 0x104 accumulator full, 0x105 drain. */
+ * full, 0x103 accumulator free, 0x104 accumulator full, 0x105 drain,
+ * 0x106 injected stall (spg_debug_inject_stall). */
 SPG_API spg_status spg_last_device_error_code(spg_stream_t stream, uint32_t* code);
 
 /* ---------------------------------------------------------------------

@@ -69,6 +69,7 @@ def load_library():
             "spg_status_string": (ctypes.c_char_p, [i32]),
             "spg_version": (i32, []),
             "spg_set_wait_timeout_ns": (None, [u64]),
+            "spg_debug_inject_stall": (None, [i32]),
             "spg_last_device_error": (st, [vp]),
             "spg_last_device_error_code": (st, [vp, ctypes.POINTER(ctypes.c_uint32)]),
             "spg_quantize_fp8_rows": (st, [vp, i64, i64, vp, vp, vp]),
@@ -125,6 +126,11 @@ def _need(t: torch.Tensor, name: str, dtype, dim=None):
 # ---------------------------------------------------------------- control
 def set_wait_timeout_ns(ns: int):
     load_library().spg_set_wait_timeout_ns(int(ns))
+
+
+def debug_inject_stall(enable: bool):
+    """Test hook: make one-CTA GEMM launches stall on a barrier nothing arrives on."""
+    load_library().spg_debug_inject_stall(1 if enable else 0)
 
 
 def last_device_error(device=None) -> int:

@@ -16,6 +16,9 @@ unsigned int* device_error_word();
 // Bound of every in-kernel wait, in nanoseconds.
 uint64_t wait_timeout_ns();
 
+// Test hook set by spg_debug_inject_stall (one-CTA GEMM kernels only).
+bool debug_stall_enabled();
+
 // Streaming multiprocessors of the current device (queried once per device).
 int num_sms();
 

@@ -62,7 +62,7 @@ struct GemmCfg {
   static_assert(kTmemUsed <= 512, "TMEM budget exceeded");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned (128B swizzle)");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(2 * STAGES + 6 <= kBarBytes / 8 - 2, "barrier area too small");
   static_assert(!(KIND == kKindNvfp4 && (A_MN || B_MN)), "NVFP4 operands are K-major");
 
   // Instruction descriptor.
@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* stall = drain + 1;  // test hook: never arrived on
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&acc_empty[b], Cfg::kEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(stall, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -269,6 +271,11 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    // Test hook: wait on a barrier nothing arrives on, so the bounded wait
+    // runs out, the CTA aborts and every role drains and returns.
+    if (p.debug_stall && !mbar_wait(stall, 0, ctl, kErrInjectedStall)) {
+      // aborted: skip the tiles; the other roles see the abort flag
+    } else
     epilogue_loop<EPI, SCALE, BN>(
         p, &tmY, tmem_base, acc_full, [&](int b) { mbar_arrive(&acc_empty[b]); }, epi, blockIdx.x,
         p.total_tiles, gridDim.x,

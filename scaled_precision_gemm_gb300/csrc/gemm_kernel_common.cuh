@@ -18,6 +18,7 @@ enum : unsigned int {
   kErrWaitAccEmpty = 0x103,
   kErrWaitAccFull = 0x104,
   kErrDrain = 0x105,
+  kErrInjectedStall = 0x106,
 };
 
 struct GemmParams {
@@ -50,6 +51,7 @@ struct GemmParams {
   uint64_t timeout_ns;  // bound of every pipeline wait
   uint64_t drain_ns;    // bound of the exit waits for copies / MMAs in flight
   unsigned int* err;
+  int debug_stall;      // test hook: the epilogue first waits on a barrier nothing arrives on
 };
 
 // One unit of work of the persistent schedule: a tile, or a piece of one.

@@ -138,6 +138,7 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
   // Exit waits keep a generous bound even under a short pipeline bound, so a
   // CTA never leaves with a copy or an MMA still writing its memory.
   p.drain_ns = p.timeout_ns > 1000000000ull ? p.timeout_ns : 1000000000ull;
+  p.debug_stall = debug_stall_enabled() ? 1 : 0;
   p.err = device_error_word();
 }
 

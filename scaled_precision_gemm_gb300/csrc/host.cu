@@ -20,6 +20,7 @@ constexpr int kMaxDevices = 64;
 __device__ unsigned int g_error_word;
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_debug_stall{0};
 std::mutex g_mu;
 unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
@@ -48,6 +49,8 @@ spg_status cuda_status(cudaError_t e, const char* where) {
   if (std::getenv("SPG_DEBUG")) std::fprintf(stderr, "spg: %s: %s\n", where, cudaGetErrorString(e));
   return SPG_ERR_CUDA;
 }
+
+bool debug_stall_enabled() { return g_debug_stall.load(std::memory_order_relaxed) != 0; }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
@@ -251,6 +254,10 @@ extern "C" int spg_version(void) { return 100; }
 
 extern "C" void spg_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed);
+}
+
+extern "C" void spg_debug_inject_stall(int enable) {
+  g_debug_stall.store(enable ? 1 : 0, std::memory_order_relaxed);
 }
 
 extern "C" spg_status spg_last_device_error(spg_stream_t stream) {

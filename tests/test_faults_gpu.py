@@ -1,12 +1,12 @@
 """Failure detection without a GPU fault.
 
-Every in-kernel wait is bounded in time.  Shrinking the bound to 1 ns makes
-the waits of a normal GEMM run out (the epilogue's wait for the accumulator
-cannot be satisfied within a few polls); the kernel must then record the
-time-out in the device error word, drain the copies and MMAs it has in flight,
-free its tensor memory and return, so that the host reads SPG_ERR_TIMEOUT and
-the context stays usable.  The one-CTA kernel is pinned: its drain covers all
-of its own copies.
+Every in-kernel wait is bounded in time.  With the test hook
+spg_debug_inject_stall, the epilogue of the one-CTA kernel waits on a barrier
+that nothing arrives on (a flag nothing sets), under a 20 ms bound: the wait
+runs out, the kernel records the code in the device error word, the producer
+and MMA roles see the abort flag, drain the copies and MMAs in flight, free
+tensor memory and return.  The host must read SPG_ERR_TIMEOUT and the context
+must stay usable for a correct call right after.
 """
 import numpy as np
 import pytest
@@ -20,7 +20,7 @@ from tests.helpers import assert_within_tol
 
 pytestmark = pytest.mark.gpu
 
-WAIT_CODES = {0x101, 0x102, 0x103, 0x104}
+INJECTED = 0x106
 
 
 def _inputs(T, N, K):
@@ -36,13 +36,15 @@ def test_wait_timeout_is_reported_and_context_survives(monkeypatch):
     args = (cuda(A), cuda(sa), cuda(W), cuda(sw))
     torch.cuda.synchronize()
     assert spg.last_device_error() == 0
-    spg.set_wait_timeout_ns(1)
+    spg.set_wait_timeout_ns(20_000_000)
+    spg.debug_inject_stall(True)
     try:
         spg.fp8_rowscaled_gemm(*args)
         code = spg.last_device_error_code()
     finally:
+        spg.debug_inject_stall(False)
         spg.set_wait_timeout_ns(2_000_000_000)
-    assert code in WAIT_CODES, hex(code)
+    assert code == INJECTED, hex(code)
     assert spg.last_device_error() == 0          # reading the code cleared it
     # the context is intact: the same call now completes and is correct
     y = spg.fp8_rowscaled_gemm(*args)
