@@ -161,8 +161,16 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const bool force_one_cta =
       forced_name && (!std::strcmp(forced_name, "1sm256") || !std::strcmp(forced_name, "1sm128"));
   if (kind == SPG_KIND_NVFP4) {
-    // Two-SM 256x256 pair tile unless pinned to the one-CTA 128x128 tile.
-    const bool one_cta = force_one_cta;
+    // Two-SM 256x256 pair tile, or the one-CTA 128x128 tile when its waves
+    // are cheaper (narrow T: more, smaller tiles spread the weight stream
+    // over more SMs).  The one-CTA tile runs at about 0.6 of the pair tile's
+    // per-SM rate on GB300.
+    const int64_t t2 = ((T + 255) / 256) * ((N + 255) / 256) * nb;
+    const int64_t t1 = ((T + 127) / 128) * ((N + 127) / 128) * nb;
+    const double w2 = static_cast<double>((t2 + sms / 2 - 1) / (sms / 2)) * 2.0;
+    const double w1 = static_cast<double>((t1 + sms - 1) / sms) * 1.0 / 0.6;
+    bool one_cta = w1 < w2;
+    if (forced_name) one_cta = force_one_cta;
     r.block_m = one_cta ? 128 : 256;
     r.block_n = one_cta ? 128 : 256;
     r.block_k = 256;

@@ -73,9 +73,12 @@ def test_route_selector(lib):
     small = spg.select_route("fp8_rowscaled", 64, 128, 256, "linear")
     # one tile; a lone two-SM tile is split along N over up to 4 CTA pairs
     assert small["tiles"] == 1 and small["grid"] in (1, 2, 4, 8)
+    nv = spg.select_route("nvfp4", 4096, 5120, 17408, "add")
+    assert (nv["block_m"], nv["block_n"]) == (256, 256) and nv["tiles"] == 320
+    assert nv["grid"] == 152 and nv["acc_buffers"] == 1
+    # narrow T: the one-CTA 128x128 tile spreads the weight stream wider
     nv = spg.select_route("nvfp4", 256, 5120, 17408, "add")
-    assert (nv["block_m"], nv["block_n"]) == (256, 256) and nv["tiles"] == 20
-    assert nv["grid"] == 40 and nv["acc_buffers"] == 1
+    assert (nv["block_m"], nv["block_n"], nv["tiles"], nv["grid"]) == (128, 128, 80, 80)
     b = spg.select_route("fp8_tensor", 512, 512, 512, "linear", batch=64)
     assert b["tiles"] % 64 == 0
     with pytest.raises(spg.SpgError):
