@@ -24,6 +24,9 @@ Functions and the passages they follow:
 * ``fp8_tensor_gemm`` -- per-tensor FP8 GEMM, layouts NT / NN / TN, batch
   strides with stride 0 broadcasting (AstrAI fp8 gemm.cuh commit log, first
   bullet).
+* ``bias=`` / ``bias_scale=`` on the three GEMMs -- fused bias per output column
+  after the scales, bf16 or E4M3 x bias_scale (AstrAI fp8 gemm.cuh commit log,
+  bias bullets).
 
 Every pin of these functions is in ``tests/test_oracle.py``.
 """
@@ -83,6 +86,14 @@ def _load():
                                                   c.c_int, vp, i64, vp, vp]
             lib.spg_oracle_fp8_tensor_gemm.argtypes = [c.c_char, c.c_char, i64, vp, i64, f32, vp,
                                                        i64, f32, i64, i64, i64, vp, i64, vp]
+            lib.spg_oracle_fp8_rowscaled_gemm_bias.argtypes = [vp, vp, vp, vp, vp, c.c_int, f32, vp,
+                                                               i64, i64, i64, c.c_int, vp, i64, vp,
+                                                               vp]
+            lib.spg_oracle_nvfp4_gemm_bias.argtypes = [vp, vp, f32, vp, vp, f32, vp, c.c_int, f32,
+                                                       vp, i64, i64, i64, c.c_int, vp, i64, vp, vp]
+            lib.spg_oracle_fp8_tensor_gemm_bias.argtypes = [c.c_char, c.c_char, i64, vp, i64, f32,
+                                                            vp, i64, f32, vp, c.c_int, f32, i64,
+                                                            i64, i64, vp, i64, vp]
             _lib = lib
     return _lib
 
@@ -177,9 +188,25 @@ def _rows_arg(rows, T):
     return r, r.size
 
 
+def _bias_args(bias, bias_scale, N):
+    """(pointer array, kind, scale): bias bf16 bits uint16 [N] (kind 1), or
+    E4M3 codes uint8 [N] with an fp32 bias_scale (kind 2)."""
+    if bias is None:
+        return None, 0, 0.0
+    b = np.ascontiguousarray(bias)
+    assert b.shape == (N,)
+    if bias_scale is None:
+        if b.dtype != np.uint16:
+            raise TypeError("a bf16 bias is passed as uint16 bit patterns")
+        return b, 1, 0.0
+    if b.dtype != np.uint8:
+        raise TypeError("an fp8 bias is passed as uint8 E4M3 codes")
+    return b, 2, float(np.float32(bias_scale))
+
+
 def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", rows=None,
-                       return_acc=False):
-    """Y [len(rows) or T, N_out] fp64 = epilogue(dequant(A) dequant(W)^T)."""
+                       return_acc=False, bias=None, bias_scale=None):
+    """Y [len(rows) or T, N_out] fp64 = epilogue(dequant(A) dequant(W)^T [+ bias])."""
     A = _c(A, np.uint8); W = _c(W, np.uint8)
     sa = _c(sa, np.float32); sw = _c(sw, np.float32)
     T, K = A.shape
@@ -193,13 +220,15 @@ def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", rows=None
     n_out = N // 2 if epi == 2 else N
     out = np.empty((nr, n_out), np.float64)
     acc = np.empty((nr, N), np.float64) if return_acc else None
-    _load().spg_oracle_fp8_rowscaled_gemm(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), _ptr(res), T, N, K,
-                                          epi, _ptr(r), nr, _ptr(out), _ptr(acc))
+    bb, bk, bs = _bias_args(bias, bias_scale, N)
+    _load().spg_oracle_fp8_rowscaled_gemm_bias(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), _ptr(bb), bk, bs,
+                                               _ptr(res), T, N, K, epi, _ptr(r), nr, _ptr(out),
+                                               _ptr(acc))
     return (out, acc) if return_acc else out
 
 
 def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", rows=None,
-               return_acc=False):
+               return_acc=False, bias=None, bias_scale=None):
     """A codes [T, K/2], sfA row-major [T, K/16]; same for W [N, ...]."""
     A = _c(A, np.uint8); W = _c(W, np.uint8)
     sfA = _c(sfA, np.uint8); sfW = _c(sfW, np.uint8)
@@ -215,14 +244,15 @@ def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", rows=No
     n_out = N // 2 if epi == 2 else N
     out = np.empty((nr, n_out), np.float64)
     acc = np.empty((nr, N), np.float64) if return_acc else None
-    _load().spg_oracle_nvfp4_gemm(_ptr(A), _ptr(sfA), float(np.float32(gA)), _ptr(W), _ptr(sfW),
-                                  float(np.float32(gW)), _ptr(res), T, N, K, epi, _ptr(r), nr,
-                                  _ptr(out), _ptr(acc))
+    bb, bk, bs = _bias_args(bias, bias_scale, N)
+    _load().spg_oracle_nvfp4_gemm_bias(_ptr(A), _ptr(sfA), float(np.float32(gA)), _ptr(W),
+                                       _ptr(sfW), float(np.float32(gW)), _ptr(bb), bk, bs,
+                                       _ptr(res), T, N, K, epi, _ptr(r), nr, _ptr(out), _ptr(acc))
     return (out, acc) if return_acc else out
 
 
 def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, strideB=None,
-                    rows=None):
+                    rows=None, bias=None, bias_scale=None):
     """C [batch, M (or len(rows)), N] fp64 for layout 'NT', 'NN' or 'TN'.
 
     A / B are flat u8 buffers; matrix b starts at b*strideA / b*strideB
@@ -235,8 +265,10 @@ def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, s
     assert A.size >= (batch - 1) * strideA + M * K and B.size >= (batch - 1) * strideB + N * K
     r, nr = _rows_arg(rows, M)
     out = np.empty((batch, nr, N), np.float64)
-    _load().spg_oracle_fp8_tensor_gemm(layout[0].encode(), layout[1].encode(), batch, _ptr(A),
-                                       strideA, float(np.float32(sA)), _ptr(B), strideB,
-                                       float(np.float32(sB)), M, N, K, _ptr(r), nr, _ptr(out))
+    bb, bk, bs = _bias_args(bias, bias_scale, N)
+    _load().spg_oracle_fp8_tensor_gemm_bias(layout[0].encode(), layout[1].encode(), batch,
+                                            _ptr(A), strideA, float(np.float32(sA)), _ptr(B),
+                                            strideB, float(np.float32(sB)), _ptr(bb), bk, bs, M, N,
+                                            K, _ptr(r), nr, _ptr(out))
     return out
 

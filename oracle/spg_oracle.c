@@ -34,6 +34,8 @@
  *  - Per-tensor FP8 GEMM in NT / NN / TN layouts with batch strides (AstrAI
  *    fp8 gemm.cuh commit log, first bullet: 3D operands, batch strides,
  *    size-1 batches broadcast with stride 0, .t() views as layout tags).
+ *  - Optional fused bias per output column, added after the scales and
+ *    before the epilogue (AstrAI fp8 gemm.cuh commit log, bias bullets).
  *
  * fp32 steps are written as C float operations; the file must be compiled
  * without fast-math and with -ffp-contract=off so every fp32 operation is a
@@ -254,6 +256,19 @@ static int64_t e2m1_units(uint32_t code) {
 
 enum { EPI_LINEAR = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
 
+/* Bias of output column n (fused bias, AstrAI fp8 gemm.cuh commit log: bf16
+ * bias, or E4M3 bias storage dequantized with bias_scale after the operand
+ * scaling): bias_kind 0 none, 1 bf16 values, 2 E4M3 codes times bias_scale
+ * (the product rounded to fp32). */
+static double bias_value(const void* bias, int bias_kind, float bias_scale, int64_t n) {
+  if (bias_kind == 1) return (double)bf16_to_float(((const uint16_t*)bias)[n]);
+  if (bias_kind == 2) {
+    float d = (float)spg_oracle_e4m3_value(((const uint8_t*)bias)[n]) * bias_scale;
+    return (double)d;
+  }
+  return 0.0;
+}
+
 /* Apply the epilogue to one output row.  y [N] holds the scaled fp64
  * linear output of that row; out gets N values (linear / add) or N/2
  * (SwiGLU: gate = column 2j, up = column 2j+1). */
@@ -280,8 +295,9 @@ static void epilogue_row(const double* y, int64_t N, int epi,
  * [T,N] bf16 (linear_add only).  out is [nrows, N_out] fp64 with N_out = N
  * or N/2 for SwiGLU.  acc_out, when not NULL, receives the exact unscaled
  * dot products [nrows, N]. */
-SPG_EXPORT void spg_oracle_fp8_rowscaled_gemm(
+SPG_EXPORT void spg_oracle_fp8_rowscaled_gemm_bias(
     const uint8_t* A, const float* sa, const uint8_t* W, const float* sw,
+    const void* bias, int bias_kind, float bias_scale,
     const uint16_t* residual, int64_t T, int64_t N, int64_t K, int epi,
     const int64_t* rows, int64_t nrows, double* out, double* acc_out) {
   ensure_tables();
@@ -304,11 +320,19 @@ SPG_EXPORT void spg_oracle_fp8_rowscaled_gemm(
       }
       double dot = nan ? NAN : ldexp((double)acc, -18);
       if (acc_out) acc_out[i * N + n] = dot;
-      y[n] = dot * (double)sa[t] * (double)sw[n];
+      y[n] = dot * (double)sa[t] * (double)sw[n] + bias_value(bias, bias_kind, bias_scale, n);
     }
     epilogue_row(y, N, epi, residual ? residual + t * N : NULL, out + i * n_out);
     free(y);
   }
+}
+
+SPG_EXPORT void spg_oracle_fp8_rowscaled_gemm(
+    const uint8_t* A, const float* sa, const uint8_t* W, const float* sw,
+    const uint16_t* residual, int64_t T, int64_t N, int64_t K, int epi,
+    const int64_t* rows, int64_t nrows, double* out, double* acc_out) {
+  spg_oracle_fp8_rowscaled_gemm_bias(A, sa, W, sw, NULL, 0, 0.0f, residual, T, N, K, epi, rows,
+                                     nrows, out, acc_out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -319,9 +343,10 @@ SPG_EXPORT void spg_oracle_fp8_rowscaled_gemm(
  * W codes [N, K/2], sfW [N, K/16], gW.  Y = (sum_k dec(A)dec(sfA)dec(W)
  * dec(sfW)) * gA * gW, then the epilogue.  The sum is exact in units of
  * 2^-20.  Same row selection and outputs as the FP8 function. */
-SPG_EXPORT void spg_oracle_nvfp4_gemm(
+SPG_EXPORT void spg_oracle_nvfp4_gemm_bias(
     const uint8_t* A, const uint8_t* sfA, float gA, const uint8_t* W,
-    const uint8_t* sfW, float gW, const uint16_t* residual, int64_t T,
+    const uint8_t* sfW, float gW, const void* bias, int bias_kind, float bias_scale,
+    const uint16_t* residual, int64_t T,
     int64_t N, int64_t K, int epi, const int64_t* rows, int64_t nrows,
     double* out, double* acc_out) {
   ensure_tables();
@@ -349,11 +374,20 @@ SPG_EXPORT void spg_oracle_nvfp4_gemm(
       }
       double dot = nan ? NAN : ldexp((double)acc, -20);
       if (acc_out) acc_out[i * N + n] = dot;
-      y[n] = dot * (double)gA * (double)gW;
+      y[n] = dot * (double)gA * (double)gW + bias_value(bias, bias_kind, bias_scale, n);
     }
     epilogue_row(y, N, epi, residual ? residual + t * N : NULL, out + i * n_out);
     free(y);
   }
+}
+
+SPG_EXPORT void spg_oracle_nvfp4_gemm(
+    const uint8_t* A, const uint8_t* sfA, float gA, const uint8_t* W,
+    const uint8_t* sfW, float gW, const uint16_t* residual, int64_t T,
+    int64_t N, int64_t K, int epi, const int64_t* rows, int64_t nrows,
+    double* out, double* acc_out) {
+  spg_oracle_nvfp4_gemm_bias(A, sfA, gA, W, sfW, gW, NULL, 0, 0.0f, residual, T, N, K, epi, rows,
+                             nrows, out, acc_out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -368,9 +402,10 @@ SPG_EXPORT void spg_oracle_nvfp4_gemm(
  * b * strideA / b * strideB elements (stride 0 broadcasts one matrix).
  * out is [batch, M, N] fp64 (only rows in rows[] when rows != NULL, then
  * out is [batch, nrows, N]). */
-SPG_EXPORT void spg_oracle_fp8_tensor_gemm(
+SPG_EXPORT void spg_oracle_fp8_tensor_gemm_bias(
     char la, char lb, int64_t batch, const uint8_t* A, int64_t strideA,
-    float sA, const uint8_t* B, int64_t strideB, float sB, int64_t M,
+    float sA, const uint8_t* B, int64_t strideB, float sB, const void* bias,
+    int bias_kind, float bias_scale, int64_t M,
     int64_t N, int64_t K, const int64_t* rows, int64_t nrows, double* out) {
   ensure_tables();
   int64_t lut[256];
@@ -392,8 +427,18 @@ SPG_EXPORT void spg_oracle_fp8_tensor_gemm(
           nan |= is_e4m3_nan(a) | is_e4m3_nan(w);
         }
         out[(b * nr + i) * N + n] =
-            nan ? NAN : ldexp((double)acc, -18) * (double)sA * (double)sB;
+            nan ? NAN
+                : ldexp((double)acc, -18) * (double)sA * (double)sB +
+                      bias_value(bias, bias_kind, bias_scale, n);
       }
     }
   }
+}
+
+SPG_EXPORT void spg_oracle_fp8_tensor_gemm(
+    char la, char lb, int64_t batch, const uint8_t* A, int64_t strideA,
+    float sA, const uint8_t* B, int64_t strideB, float sB, int64_t M,
+    int64_t N, int64_t K, const int64_t* rows, int64_t nrows, double* out) {
+  spg_oracle_fp8_tensor_gemm_bias(la, lb, batch, A, strideA, sA, B, strideB, sB, NULL, 0, 0.0f,
+                                  M, N, K, rows, nrows, out);
 }

@@ -415,3 +415,53 @@ def test_tensor_gemm_layouts_vs_fractions(layout):
     o0 = oracle.fp8_tensor_gemm(layout, A, sA, B[0], sB, M, N, K, batch=batch, strideB=0)
     o1 = oracle.fp8_tensor_gemm(layout, A[1], sA, B[0], sB, M, N, K, batch=1)
     assert np.array_equal(o0[1], o1[0])
+
+
+# ------------------------------------------------------------ fused bias
+def test_bias_alone_bf16_and_fp8():
+    """A = 0 leaves exactly the bias: bf16 values, or E4M3 x bias_scale rounded to fp32."""
+    T, N, K = 3, 24, 32
+    A = np.zeros((T, K), np.uint8)
+    W = random_codes((N, K), seed=51, exclude=(0x7F, 0xFF))
+    sa = np.ones(T, np.float32)
+    sw = np.float32(np.linspace(0.5, 2, N))
+    b16 = normal_bf16((N,), seed=52, std=3.0)
+    y = oracle.fp8_rowscaled_gemm(A, sa, W, sw, bias=b16)
+    assert np.array_equal(y, np.broadcast_to(bf16_bits_to_f32(b16).astype(np.float64), (T, N)))
+    b8 = random_codes((N,), seed=53, exclude=(0x7F, 0xFF))
+    scale = np.float32(0.37)
+    y = oracle.fp8_rowscaled_gemm(A, sa, W, sw, bias=b8, bias_scale=scale)
+    ref = (torch_e4m3_values(b8).astype(np.float32) * scale).astype(np.float64)
+    assert np.array_equal(y, np.broadcast_to(ref, (T, N)))
+
+
+def test_bias_is_added_after_scales_and_before_epilogue():
+    from scipy.special import expit
+    T, N, K = 4, 16, 64
+    x = normal_bf16((T, K), seed=61)
+    w = normal_bf16((N, K), seed=62)
+    A, sa = oracle.quantize_fp8_rows(x)
+    W, sw = oracle.quantize_fp8_rows(w)
+    b = normal_bf16((N,), seed=63)
+    bf = bf16_bits_to_f32(b).astype(np.float64)
+    y = oracle.fp8_rowscaled_gemm(A, sa, W, sw)
+    yb = oracle.fp8_rowscaled_gemm(A, sa, W, sw, bias=b)
+    np.testing.assert_allclose(yb - y, np.broadcast_to(bf, (T, N)), rtol=0, atol=1e-12)
+    r = normal_bf16((T, N), seed=64)
+    ya = oracle.fp8_rowscaled_gemm(A, sa, W, sw, r, "add", bias=b)
+    np.testing.assert_allclose(ya, yb + bf16_bits_to_f32(r), rtol=1e-15)
+    ys = oracle.fp8_rowscaled_gemm(A, sa, W, sw, epilogue="swiglu", bias=b)
+    g, u = yb[:, 0::2], yb[:, 1::2]
+    np.testing.assert_allclose(ys, g * expit(g) * u, rtol=1e-13)
+    # the same bias on the NVFP4 and per-tensor GEMMs
+    gA = oracle.nvfp4_global_scale(x)
+    gW = oracle.nvfp4_global_scale(w)
+    An, sfA = oracle.quantize_nvfp4(x, gA)
+    Wn, sfW = oracle.quantize_nvfp4(w, gW)
+    d = oracle.nvfp4_gemm(An, sfA, gA, Wn, sfW, gW, bias=b) - oracle.nvfp4_gemm(An, sfA, gA, Wn, sfW, gW)
+    np.testing.assert_allclose(d, np.broadcast_to(bf, (T, N)), rtol=0, atol=1e-12)
+    At, sAt = oracle.quantize_fp8_tensor(x)
+    Bt, sBt = oracle.quantize_fp8_tensor(w)
+    d = (oracle.fp8_tensor_gemm("NT", At, sAt, Bt, sBt, T, N, K, bias=b)
+         - oracle.fp8_tensor_gemm("NT", At, sAt, Bt, sBt, T, N, K))
+    np.testing.assert_allclose(d[0], np.broadcast_to(bf, (T, N)), rtol=0, atol=1e-12)
