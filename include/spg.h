@@ -243,6 +243,33 @@ SPG_API spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batch, 
                            const float* sB, void* C, int64_t strideC, int64_t M, int64_t N,
                            int64_t K, spg_stream_t stream);
 
+/* The three GEMMs with a fused bias per output column, added after the
+ * scales and before the epilogue:
+ *   y[t,n] = acc[t,n] * scale + bias[n],  then LINEAR / ADD / SWIGLU as above
+ *   (for SWIGLU the gate and up columns each get their own bias).
+ * bias: bf16 [N] when bias_scale is NULL; otherwise E4M3 codes [N] (uint8)
+ * dequantized as fp32(dec(code) * bias_scale[0]) with bias_scale an fp32 [1]
+ * device scalar.  bias NULL means no bias (then bias_scale must be NULL).
+ * AstrAI commit log of csrc/kernels/fp8/gemm.cuh, bias bullets (bias fused
+ * into the epilogue for both dtypes; fp8 storage dequantized after the
+ * operand scaling).  Other arguments and rules as for the plain entry points. */
+SPG_API spg_status fp8_rowscaled_gemm_bias(const uint8_t* A, const float* sa, const uint8_t* W,
+                                           const float* sw, const void* bias,
+                                           const float* bias_scale, const void* residual, void* Y,
+                                           int64_t T, int64_t N, int64_t K, int epilogue,
+                                           spg_stream_t stream);
+SPG_API spg_status nvfp4_gemm_bias(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                   const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                   const void* bias, const float* bias_scale, const void* residual,
+                                   void* Y, int64_t T, int64_t N, int64_t K, int epilogue,
+                                   spg_stream_t stream);
+SPG_API spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t batch,
+                                        const uint8_t* A, int64_t strideA, const float* sA,
+                                        const uint8_t* B, int64_t strideB, const float* sB,
+                                        const void* bias, const float* bias_scale, void* C,
+                                        int64_t strideC, int64_t M, int64_t N, int64_t K,
+                                        spg_stream_t stream);
+
 /* Per-shape tile / route selector (host only, no device query after the
  * first call).  kind: spg_kind; T: rows of the output (M for the tensor
  * GEMM).  Fills *out with the configuration the GEMM entry points would

@@ -84,6 +84,12 @@ def load_library():
             "fp8_tensor_gemm": (st, [ctypes.c_char, ctypes.c_char, i64, vp, i64, vp, vp, i64, vp,
                                      vp, i64, i64, i64, i64, vp]),
             "spg_select_route": (st, [i32, i64, i64, i64, i32, i64, ctypes.POINTER(Route)]),
+            "fp8_rowscaled_gemm_bias": (st, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                             vp]),
+            "nvfp4_gemm_bias": (st, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                     vp]),
+            "fp8_tensor_gemm_bias": (st, [ctypes.c_char, ctypes.c_char, i64, vp, i64, vp, vp, i64,
+                                          vp, vp, vp, vp, i64, i64, i64, i64, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -234,8 +240,24 @@ def _epi(epilogue) -> int:
     return EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
 
 
-def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None):
-    """Y = epilogue((A . W^T) * sa[:, None] * sw[None, :]) in bf16."""
+def _check_bias(bias, bias_scale, N):
+    """bias: bf16 [N], or uint8 E4M3 codes [N] with an fp32 [1] bias_scale."""
+    if bias is None:
+        if bias_scale is not None:
+            raise ValueError("bias_scale without bias")
+        return
+    if bias_scale is None:
+        _need(bias, "bias", torch.bfloat16, 1)
+    else:
+        _need(bias, "bias", torch.uint8, 1)
+        _need(bias_scale, "bias_scale", torch.float32)
+    if bias.shape[0] != N:
+        raise ValueError("bias must have N elements")
+
+
+def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None, bias=None,
+                       bias_scale=None):
+    """Y = epilogue((A . W^T) * sa[:, None] * sw[None, :] [+ bias]) in bf16."""
     _need(A, "A", torch.uint8, 2)
     _need(W, "W", torch.uint8, 2)
     _need(sa, "sa", torch.float32, 1)
@@ -252,14 +274,22 @@ def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None)
     n_out = N // 2 if e == 2 else N
     out = torch.empty((T, n_out), dtype=torch.bfloat16, device=A.device) if out is None else out
     _need(out, "out", torch.bfloat16, 2)
-    _check(load_library().fp8_rowscaled_gemm(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
-                                             _ptr(residual if e == 1 else None), _ptr(out),
-                                             T, N, K, e, _stream(A)), "fp8_rowscaled_gemm")
+    _check_bias(bias, bias_scale, N)
+    res = _ptr(residual if e == 1 else None)
+    if bias is None:
+        st = load_library().fp8_rowscaled_gemm(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), res,
+                                               _ptr(out), T, N, K, e, _stream(A))
+    else:
+        st = load_library().fp8_rowscaled_gemm_bias(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
+                                                    _ptr(bias), _ptr(bias_scale), res, _ptr(out),
+                                                    T, N, K, e, _stream(A))
+    _check(st, "fp8_rowscaled_gemm")
     return out
 
 
-def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=None):
-    """Y = epilogue(block-scaled NVFP4 product * gA * gW) in bf16; A/W are packed [rows, K/2]."""
+def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=None, bias=None,
+               bias_scale=None):
+    """Y = epilogue(block-scaled NVFP4 product * gA * gW [+ bias]) in bf16; A/W packed [rows, K/2]."""
     for t, n, d in ((A, "A", torch.uint8), (W, "W", torch.uint8), (sfA, "sfA", torch.uint8),
                     (sfW, "sfW", torch.uint8), (gA, "gA", torch.float32),
                     (gW, "gW", torch.float32)):
@@ -279,14 +309,21 @@ def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=Non
     n_out = N // 2 if e == 2 else N
     out = torch.empty((T, n_out), dtype=torch.bfloat16, device=A.device) if out is None else out
     _need(out, "out", torch.bfloat16, 2)
-    _check(load_library().nvfp4_gemm(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW),
-                                     _ptr(residual if e == 1 else None), _ptr(out), T, N, K, e,
-                                     _stream(A)), "nvfp4_gemm")
+    _check_bias(bias, bias_scale, N)
+    res = _ptr(residual if e == 1 else None)
+    if bias is None:
+        st = load_library().nvfp4_gemm(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW),
+                                       res, _ptr(out), T, N, K, e, _stream(A))
+    else:
+        st = load_library().nvfp4_gemm_bias(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW),
+                                            _ptr(gW), _ptr(bias), _ptr(bias_scale), res,
+                                            _ptr(out), T, N, K, e, _stream(A))
+    _check(st, "nvfp4_gemm")
     return out
 
 
 def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, strideB=None,
-                    out=None, strideC=None):
+                    out=None, strideC=None, bias=None, bias_scale=None):
     """C[b] = bf16(sA*sB*opA(A[b]) opB(B[b])), layout in {'NT','NN','TN','TT'}.
 
     A / B are flat (or any contiguous) uint8 buffers; matrix b starts at
@@ -307,8 +344,15 @@ def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, s
     _need(out, "out", torch.bfloat16)
     if out.numel() < (batch - 1) * strideC + M * N:
         raise ValueError("output buffer too small")
-    _check(load_library().fp8_tensor_gemm(layout[0].encode(), layout[1].encode(), batch,
-                                          _ptr(A), strideA, _ptr(sA), _ptr(B), strideB, _ptr(sB),
-                                          _ptr(out), strideC, M, N, K, _stream(A)),
-           "fp8_tensor_gemm")
+    _check_bias(bias, bias_scale, N)
+    lib = load_library()
+    if bias is None:
+        st = lib.fp8_tensor_gemm(layout[0].encode(), layout[1].encode(), batch, _ptr(A), strideA,
+                                 _ptr(sA), _ptr(B), strideB, _ptr(sB), _ptr(out), strideC, M, N,
+                                 K, _stream(A))
+    else:
+        st = lib.fp8_tensor_gemm_bias(layout[0].encode(), layout[1].encode(), batch, _ptr(A),
+                                      strideA, _ptr(sA), _ptr(B), strideB, _ptr(sB), _ptr(bias),
+                                      _ptr(bias_scale), _ptr(out), strideC, M, N, K, _stream(A))
+    _check(st, "fp8_tensor_gemm")
     return out

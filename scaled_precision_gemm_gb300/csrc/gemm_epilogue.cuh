@@ -77,6 +77,13 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         swr[j] = (32 * j < tc.width && n < p.N) ? __ldg(p.col_scale + n) : 0.f;
       }
     }
+    float biasr[E::kSwRegs];
+    const bool has_bias = p.bias_kind != 0;
+    if (has_bias) {
+#pragma unroll
+      for (int j = 0; j < E::kSwRegs; ++j)
+        biasr[j] = 32 * j < tc.width ? load_bias(p, n0 + 32 * j + lane) : 0.f;
+    }
     uint4 res_cur[4];
     if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n0, row_ok, res_cur);
 
@@ -117,6 +124,13 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
           s = row_s * __shfl_sync(0xffffffffu, swr[col >> 5], col & 31);
         }
         v[i] = __uint_as_float(raw[i]) * s;
+      }
+      if (has_bias) {
+#pragma unroll
+        for (int i = 0; i < E::kAccColsPerChunk; ++i) {
+          const int col = acc_c0 + i;
+          v[i] += __shfl_sync(0xffffffffu, biasr[col >> 5], col & 31);
+        }
       }
       float o[32];
       if constexpr (EPI == SPG_EPI_SWIGLU) {
@@ -182,7 +196,7 @@ namespace spg {
 // epilogue and stores -- so the next tile's main loop overlaps the math and
 // the stores although TMEM holds one accumulator (the rest of TMEM holds the
 // block scales of the NVFP4 pipeline).
-template <int EPI, int SCALE, typename TileFn, typename ArriveEmpty>
+template <int EPI, int SCALE, bool HAS_BIAS, typename TileFn, typename ArriveEmpty>
 __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, const CUtensorMap* tmY,
                                                        uint32_t tmem_base, uint64_t* acc_full,
                                                        ArriveEmpty arrive_empty, uint8_t* epi_smem,
@@ -219,6 +233,10 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
         swr[j] = n < p.N ? __ldg(p.col_scale + n) : 0.f;
       }
     }
+    // The bias is loaded per chunk (one or two registers) to leave room for
+    // the 128 accumulator registers; its code exists only in the HAS_BIAS
+    // instantiation.
+    constexpr bool has_bias = HAS_BIAS;
     uint4 res_cur[4];
     if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
 
@@ -243,6 +261,11 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
     for (int c = 0; c < kOutChunks; ++c, ++chunk_ctr) {
       float o[32];
       if constexpr (EPI == SPG_EPI_SWIGLU) {
+        float biasr[2] = {0.f, 0.f};
+        if (has_bias) {
+          biasr[0] = load_bias(p, n_acc0 + c * 64 + lane);
+          biasr[1] = load_bias(p, n_acc0 + c * 64 + 32 + lane);
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int cg = c * 64 + 2 * j;  // gate column inside this warp's 128
@@ -251,11 +274,16 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
             sg *= __shfl_sync(0xffffffffu, swr[cg >> 5], cg & 31);
             su *= __shfl_sync(0xffffffffu, swr[(cg + 1) >> 5], (cg + 1) & 31);
           }
-          const float gate = __uint_as_float(acc[cg]) * sg;
-          const float up = __uint_as_float(acc[cg + 1]) * su;
+          float gate = __uint_as_float(acc[cg]) * sg;
+          float up = __uint_as_float(acc[cg + 1]) * su;
+          if (has_bias) {
+            gate += __shfl_sync(0xffffffffu, biasr[(2 * j) >> 5], (2 * j) & 31);
+            up += __shfl_sync(0xffffffffu, biasr[(2 * j + 1) >> 5], (2 * j + 1) & 31);
+          }
           o[j] = __fdividef(gate, 1.f + __expf(-gate)) * up;
         }
       } else {
+        const float bias_c = has_bias ? load_bias(p, n_acc0 + 32 * c + lane) : 0.f;
         uint4 res_next[4];
         if constexpr (EPI == SPG_EPI_ADD) {
           if (c + 1 < kOutChunks) load_residual_chunk(p, m, n_acc0 + 32 * (c + 1), row_ok, res_next);
@@ -265,6 +293,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
           float s = row_s;
           if constexpr (SCALE == kScaleRow) s *= __shfl_sync(0xffffffffu, swr[c], j);
           o[j] = __uint_as_float(acc[c * 32 + j]) * s;
+          if (has_bias) o[j] += __shfl_sync(0xffffffffu, bias_c, j);
         }
         if constexpr (EPI == SPG_EPI_ADD) {
 #pragma unroll

@@ -26,10 +26,11 @@ spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, 
 
 }  // namespace
 
-extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, const uint8_t* W,
-                                         const float* sw, const void* residual, void* Y,
-                                         int64_t T, int64_t N, int64_t K, int epilogue,
-                                         spg_stream_t stream) {
+namespace {
+
+spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, const float* sw,
+                          const void* bias, const float* bias_scale, const void* residual, void* Y,
+                          int64_t T, int64_t N, int64_t K, int epilogue, spg_stream_t stream) {
   if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2) return SPG_ERR_INVALID_ARG;
   if (T == 0 || N == 0) return SPG_OK;
   if (!A || !sa || !W || !sw || !Y || (epilogue == SPG_EPI_ADD && !residual))
@@ -52,6 +53,7 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
   GemmParams p;
   fill_common_params(p, r, T, N, K, K, n_out, 1);
   if (!p.err) return SPG_ERR_CUDA;
+  if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
   spg_route rr = r;
   if (r.block_m == 256) {
     const int pairs = num_sms() / 2;
@@ -69,4 +71,21 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
     case SPG_EPI_ADD: return dispatch<SPG_EPI_ADD>(rr, maps, p, stream);
     default: return dispatch<SPG_EPI_SWIGLU>(rr, maps, p, stream);
   }
+}
+
+}  // namespace
+
+extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, const uint8_t* W,
+                                         const float* sw, const void* residual, void* Y,
+                                         int64_t T, int64_t N, int64_t K, int epilogue,
+                                         spg_stream_t stream) {
+  return rowscaled_impl(A, sa, W, sw, nullptr, nullptr, residual, Y, T, N, K, epilogue, stream);
+}
+
+extern "C" spg_status fp8_rowscaled_gemm_bias(const uint8_t* A, const float* sa, const uint8_t* W,
+                                              const float* sw, const void* bias,
+                                              const float* bias_scale, const void* residual,
+                                              void* Y, int64_t T, int64_t N, int64_t K,
+                                              int epilogue, spg_stream_t stream) {
+  return rowscaled_impl(A, sa, W, sw, bias, bias_scale, residual, Y, T, N, K, epilogue, stream);
 }

@@ -39,6 +39,9 @@ struct GemmParams {
   const float* scalar_a;   // kScaleScalar: device scalars
   const float* scalar_b;
   const __nv_bfloat16* residual;  // SPG_EPI_ADD: [M, N] row-major
+  const void* bias;               // fused bias per output column, or nullptr
+  const float* bias_scale;        // bias_kind 2: device scalar
+  int bias_kind;                  // 0 none, 1 bf16 [N], 2 E4M3 codes [N] x bias_scale
   const uint8_t* sfa;             // NVFP4 scales, blocked layout
   const uint8_t* sfb;
   int sf_tiles_per_row_block;  // K / 64
@@ -95,6 +98,15 @@ __device__ __forceinline__ WorkItem work_item(int item, const GemmParams& p, int
   w.width = bn / ways;
   w.n_off = piece * w.width;
   return w;
+}
+
+// Bias of accumulator column n (0 when there is none or n is out of range).
+__device__ __forceinline__ float load_bias(const GemmParams& p, int n) {
+  if (n >= p.N) return 0.f;
+  if (p.bias_kind == 1)
+    return __uint_as_float(uint32_t(__ldg(static_cast<const unsigned short*>(p.bias) + n)) << 16);
+  const uint16_t c = __ldg(static_cast<const uint8_t*>(p.bias) + n);
+  return __fmul_rn(e4m3x2_to_float2(uint16_t(c | (c << 8))).x, __ldg(p.bias_scale));
 }
 
 // Drain-mode wait: bounded, but not cut short by the abort flag.

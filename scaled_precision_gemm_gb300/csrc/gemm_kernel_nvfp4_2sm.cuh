@@ -21,7 +21,7 @@
 
 namespace spg {
 
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, bool HAS_BIAS = false>
 struct Nvfp4PairCfg {
   static constexpr int kBN = 256;
   static constexpr int kBKBytes = 128;  // 256 E2M1 elements
@@ -52,7 +52,7 @@ struct Nvfp4PairCfg {
   }
 };
 
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, bool HAS_BIAS>
 // 10 warps: the 4 SM sub-partitions hold 3, 3, 2, 2 of them, so a thread may
 // use at most 16384 / (3 * 32) -> 168 registers.
 __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    epilogue_loop_regdrain<EPI, kScaleScalar>(
+    epilogue_loop_regdrain<EPI, kScaleScalar, HAS_BIAS>(
         p, &tmY, tmem_base, acc_full,
         [&](int) { mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0)); }, epi, pair,
         num_pairs,

@@ -73,11 +73,11 @@ spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, in
 }
 
 // Two-SM NVFP4 variant (clusters of 2 CTAs).
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, bool HAS_BIAS>
 spg_status launch_nvfp4_2sm_variant(const GemmMaps& maps, const GemmParams& p, int grid,
                                     cudaStream_t stream) {
   using Cfg = Nvfp4PairCfg<EPI, STAGES>;
-  auto kern = gemm_kernel_nvfp4_2sm<EPI, STAGES>;
+  auto kern = gemm_kernel_nvfp4_2sm<EPI, STAGES, HAS_BIAS>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
@@ -129,6 +129,9 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
   p.b_batch_mul = 0;
   p.row_scale = p.col_scale = p.scalar_a = p.scalar_b = nullptr;
   p.residual = nullptr;
+  p.bias = nullptr;
+  p.bias_scale = nullptr;
+  p.bias_kind = 0;
   p.sfa = p.sfb = nullptr;
   p.sf_tiles_per_row_block = 0;
   p.split_full = p.total_tiles;
@@ -143,6 +146,20 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
 }
 
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+// Fused bias arguments: none, bf16 [N] (bias_scale == nullptr) or E4M3 codes
+// [N] times the device scalar bias_scale.
+inline spg_status set_bias(GemmParams& p, const void* bias, const float* bias_scale) {
+  if (!bias) {
+    if (bias_scale) return SPG_ERR_INVALID_ARG;
+    return SPG_OK;
+  }
+  if (!aligned16(bias) || (bias_scale && !aligned16(bias_scale))) return SPG_ERR_MISALIGNED;
+  p.bias = bias;
+  p.bias_scale = bias_scale;
+  p.bias_kind = bias_scale ? 2 : 1;
+  return SPG_OK;
+}
 
 // Split the last partial wave of a two-SM schedule along N: with U pairs and
 // P tiles, the P mod U tiles of the last wave become 2 or 4 narrower items

@@ -9,16 +9,21 @@ namespace {
 
 template <int EPI>
 spg_status launch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
-  if (r.block_m == 256) return launch_nvfp4_2sm_variant<EPI, 5>(m, p, r.grid, s);
+  if (r.block_m == 256) {
+    if (p.bias_kind) return launch_nvfp4_2sm_variant<EPI, 5, true>(m, p, r.grid, s);
+    return launch_nvfp4_2sm_variant<EPI, 5, false>(m, p, r.grid, s);
+  }
   return launch_gemm_variant<kKindNvfp4, EPI, 128, 5, false, false, kScaleScalar>(m, p, r.grid, s);
 }
 
 }  // namespace
 
-extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
-                                 const uint8_t* W, const uint8_t* sfW, const float* gW,
-                                 const void* residual, void* Y, int64_t T, int64_t N, int64_t K,
-                                 int epilogue, spg_stream_t stream) {
+namespace {
+
+spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, const uint8_t* W,
+                      const uint8_t* sfW, const float* gW, const void* bias,
+                      const float* bias_scale, const void* residual, void* Y, int64_t T,
+                      int64_t N, int64_t K, int epilogue, spg_stream_t stream) {
   if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2) return SPG_ERR_INVALID_ARG;
   if (T == 0 || N == 0) return SPG_OK;
   if (!A || !sfA || !gA || !W || !sfW || !gW || !Y || (epilogue == SPG_EPI_ADD && !residual))
@@ -50,6 +55,7 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
   GemmParams p;
   fill_common_params(p, r, T, N, kh, K, n_out, 1);
   if (!p.err) return SPG_ERR_CUDA;
+  if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
   p.scalar_a = gA;
   p.scalar_b = gW;
   p.residual = static_cast<const __nv_bfloat16*>(residual);
@@ -61,4 +67,23 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
     case SPG_EPI_ADD: return launch<SPG_EPI_ADD>(r, maps, p, stream);
     default: return launch<SPG_EPI_SWIGLU>(r, maps, p, stream);
   }
+}
+
+}  // namespace
+
+extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                 const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                 const void* residual, void* Y, int64_t T, int64_t N, int64_t K,
+                                 int epilogue, spg_stream_t stream) {
+  return nvfp4_impl(A, sfA, gA, W, sfW, gW, nullptr, nullptr, residual, Y, T, N, K, epilogue,
+                    stream);
+}
+
+extern "C" spg_status nvfp4_gemm_bias(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                      const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                      const void* bias, const float* bias_scale,
+                                      const void* residual, void* Y, int64_t T, int64_t N,
+                                      int64_t K, int epilogue, spg_stream_t stream) {
+  return nvfp4_impl(A, sfA, gA, W, sfW, gW, bias, bias_scale, residual, Y, T, N, K, epilogue,
+                    stream);
 }

@@ -29,11 +29,12 @@ spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, 
 
 }  // namespace
 
-extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batch,
-                                      const uint8_t* A, int64_t strideA, const float* sA,
-                                      const uint8_t* B, int64_t strideB, const float* sB, void* C,
-                                      int64_t strideC, int64_t M, int64_t N, int64_t K,
-                                      spg_stream_t stream) {
+namespace {
+
+spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_t* A,
+                       int64_t strideA, const float* sA, const uint8_t* B, int64_t strideB,
+                       const float* sB, const void* bias, const float* bias_scale, void* C,
+                       int64_t strideC, int64_t M, int64_t N, int64_t K, spg_stream_t stream) {
   if ((layout_a != 'N' && layout_a != 'T') || (layout_b != 'N' && layout_b != 'T'))
     return SPG_ERR_INVALID_ARG;
   if (batch < 0 || M < 0 || N < 0 || K < 0 || strideA < 0 || strideB < 0 || strideC < 0)
@@ -102,4 +103,25 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
   if (!a_mn && b_mn) return dispatch<false, true>(rr, maps, p, stream);
   if (a_mn && !b_mn) return dispatch<true, false>(rr, maps, p, stream);
   return dispatch<true, true>(rr, maps, p, stream);
+}
+
+}  // namespace
+
+extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batch,
+                                      const uint8_t* A, int64_t strideA, const float* sA,
+                                      const uint8_t* B, int64_t strideB, const float* sB, void* C,
+                                      int64_t strideC, int64_t M, int64_t N, int64_t K,
+                                      spg_stream_t stream) {
+  return tensor_impl(layout_a, layout_b, batch, A, strideA, sA, B, strideB, sB, nullptr, nullptr, C,
+                     strideC, M, N, K, stream);
+}
+
+extern "C" spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t batch,
+                                           const uint8_t* A, int64_t strideA, const float* sA,
+                                           const uint8_t* B, int64_t strideB, const float* sB,
+                                           const void* bias, const float* bias_scale, void* C,
+                                           int64_t strideC, int64_t M, int64_t N, int64_t K,
+                                           spg_stream_t stream) {
+  return tensor_impl(layout_a, layout_b, batch, A, strideA, sA, B, strideB, sB, bias, bias_scale,
+                     C, strideC, M, N, K, stream);
 }
