@@ -80,6 +80,7 @@ spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_
   GemmParams p;
   fill_common_params(p, r, M, N, K, K, N, batch);
   if (!p.err) return SPG_ERR_CUDA;
+  if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
   // An N-major B half is one 128-byte swizzle row: keep whole tiles there.
   spg_route rr = r;
   if (r.block_m == 256) {
