@@ -161,6 +161,28 @@ SPG_API spg_status spg_quantize_fp8_tensor(const void* x, int64_t numel, uint8_t
 SPG_API spg_status spg_quantize_fp8_tensor_noalloc(const void* x, int64_t numel, uint8_t* codes,
                                                    float* scale, spg_stream_t stream);
 
+/* Delayed per-tensor scaling with an amax history ring, in one kernel.
+ * Each call encodes x with the scale the previous call published,
+ *   scale_used = ring.scale;  codes = E4M3(x / scale_used)  (RNE, satfinite)
+ * then folds amax(x) into the ring and publishes the next scale:
+ *   hist[idx] = amax(x);  idx = (idx + 1) % history;
+ *   ring.scale = max(hist) / 448  (1 when the history is all zero).
+ * The last block of the kernel (elected by an atomic counter after a
+ * fence) does the fold, so no extra launch is needed.  AstrAI commit log of
+ * csrc/kernels/fp8/gemm.cuh, scale-ring bullets.
+ * ring: caller-owned device buffer of spg_fp8_scale_ring_bytes(history)
+ * bytes, set up once with spg_fp8_scale_ring_init; layout (fp32 words):
+ * [0, history) amax history, [history] scale, then three private words.
+ * scale_used: fp32 [1], receives the scale the codes were made with (pass it
+ * to the GEMM).  Calls on one ring must be ordered (one stream).
+ * Requires numel % 8 == 0 and 1 <= history <= 65536. */
+SPG_API size_t spg_fp8_scale_ring_bytes(int history);
+SPG_API spg_status spg_fp8_scale_ring_init(void* ring, int history, float initial_scale,
+                                           spg_stream_t stream);
+SPG_API spg_status spg_quantize_fp8_tensor_delayed(const void* x, int64_t numel, uint8_t* codes,
+                                                   float* scale_used, void* ring, int history,
+                                                   spg_stream_t stream);
+
 /* NVFP4 global scale g = amax(x) / (448 * 6) (g = 1 when amax = 0), written
  * to the device scalar g.  The largest 16-element block scale of the tensor
  * then encodes to the E4M3 maximum 448.  ninfer PR #160 body (an E4M3 scale

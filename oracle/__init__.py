@@ -16,6 +16,8 @@ Functions and the passages they follow:
   "What actually changes": row-scaled A8 activations and row-scaled weights).
 * ``quantize_fp8_tensor`` -- one scale per tensor (AstrAI fp8 gemm.cuh commit
   log, the quantize bullets).
+* ``DelayedScaleRing`` -- delayed scaling from an amax history ring (AstrAI fp8
+  gemm.cuh commit log, scale-ring bullets).
 * ``nvfp4_global_scale`` / ``quantize_nvfp4`` -- two-level NVFP4 scaling (ninfer
   PR #160 body).
 * ``fp8_rowscaled_gemm`` / ``nvfp4_gemm`` -- Y = dequant(A) dequant(W)^T with the
@@ -77,6 +79,7 @@ def _load():
             lib.spg_oracle_e2m1_encode.argtypes = [c.c_double]
             lib.spg_oracle_quantize_fp8_rows.argtypes = [vp, i64, i64, vp, vp]
             lib.spg_oracle_quantize_fp8_tensor.argtypes = [vp, i64, vp, vp]
+            lib.spg_oracle_fp8_delayed_step.argtypes = [vp, i64, vp, vp, c.c_int, vp, vp, vp]
             lib.spg_oracle_nvfp4_global_scale.restype = f32
             lib.spg_oracle_nvfp4_global_scale.argtypes = [vp, i64]
             lib.spg_oracle_quantize_nvfp4.argtypes = [vp, i64, i64, f32, vp, vp]
@@ -159,6 +162,26 @@ def quantize_fp8_tensor(x_bf16: np.ndarray):
     scale = np.empty((1,), np.float32)
     _load().spg_oracle_quantize_fp8_tensor(_ptr(x), x.size, _ptr(codes), _ptr(scale))
     return codes, np.float32(scale[0])
+
+
+class DelayedScaleRing:
+    """Amax-history ring for delayed per-tensor scaling (state kept on the host)."""
+
+    def __init__(self, history: int, initial_scale: float = 1.0):
+        self.hist = np.zeros(history, np.float32)
+        self.idx = np.zeros(1, np.int32)
+        self.scale = np.array([initial_scale], np.float32)
+
+    def step(self, x_bf16):
+        """Quantize x with the current scale, then fold amax(x) into the ring.
+        Returns (codes, scale_used)."""
+        x = _bf16_bits(x_bf16)
+        codes = np.empty(x.shape, np.uint8)
+        used = np.empty(1, np.float32)
+        _load().spg_oracle_fp8_delayed_step(_ptr(x), x.size, _ptr(codes), _ptr(self.hist),
+                                            self.hist.size, _ptr(self.idx), _ptr(self.scale),
+                                            _ptr(used))
+        return codes, np.float32(used[0])
 
 
 def nvfp4_global_scale(x_bf16: np.ndarray) -> np.float32:

@@ -195,6 +195,32 @@ SPG_EXPORT void spg_oracle_quantize_fp8_tensor(const uint16_t* x, int64_t numel,
   fp8_encode_with_scale(x, numel, amax_bf16(x, numel), codes, scale);
 }
 
+/* Delayed scaling with an amax history ring (AstrAI fp8 gemm.cuh commit log,
+ * scale-ring bullets: the quantizer folds this call's amax into hist[idx],
+ * reduces the window and publishes the next scale).  One call:
+ *   scale_used = *scale                      (the scale published last time)
+ *   codes      = E4M3(x / scale_used)         (IEEE fp32 division, RNE, satfinite)
+ *   hist[*idx] = amax(x);  *idx = (*idx + 1) % history
+ *   *scale     = max(hist) / 448, or 1 when max(hist) == 0   (next call's scale)
+ * hist starts all zero, *idx at 0 and *scale at the caller's initial scale. */
+SPG_EXPORT void spg_oracle_fp8_delayed_step(const uint16_t* x, int64_t numel, uint8_t* codes,
+                                            float* hist, int history, int32_t* idx,
+                                            float* scale, float* scale_used) {
+  ensure_tables();
+  const float s = *scale;
+  *scale_used = s;
+  for (int64_t i = 0; i < numel; ++i) {
+    float q = bf16_to_float(x[i]) / s;
+    codes[i] = (uint8_t)spg_oracle_e4m3_encode((double)q);
+  }
+  hist[*idx] = amax_bf16(x, numel);
+  *idx = (*idx + 1) % history;
+  float m = 0.0f;
+  for (int h = 0; h < history; ++h)
+    if (hist[h] > m) m = hist[h];
+  *scale = (m == 0.0f) ? 1.0f : m / 448.0f;
+}
+
 /* NVFP4 global scale g = amax(tensor) / (448 * 6); 1 for an all-zero tensor. */
 SPG_EXPORT float spg_oracle_nvfp4_global_scale(const uint16_t* x, int64_t numel) {
   float amax = amax_bf16(x, numel);

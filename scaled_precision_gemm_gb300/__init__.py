@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "SpgError", "EPILOGUES", "load_library", "library_path",
     "quantize_fp8_rows", "quantize_fp8_tensor", "quantize_fp8_tensor_noalloc",
+    "fp8_scale_ring", "quantize_fp8_tensor_delayed",
     "nvfp4_global_scale", "quantize_nvfp4",
     "nvfp4_sf_bytes", "nvfp4_sf_offset", "fp8_rowscaled_gemm", "nvfp4_gemm", "fp8_tensor_gemm",
     "select_route", "last_device_error", "set_wait_timeout_ns", "status_string",
@@ -76,6 +77,9 @@ def load_library():
             "spg_quantize_fp8_tensor": (st, [vp, i64, vp, vp, vp, vp]),
             "spg_quantize_fp8_tensor_noalloc": (st, [vp, i64, vp, vp, vp]),
             "spg_nvfp4_global_scale": (st, [vp, i64, vp, vp, vp]),
+            "spg_fp8_scale_ring_bytes": (ctypes.c_size_t, [i32]),
+            "spg_fp8_scale_ring_init": (st, [vp, i32, ctypes.c_float, vp]),
+            "spg_quantize_fp8_tensor_delayed": (st, [vp, i64, vp, vp, vp, i32, vp]),
             "spg_quantize_nvfp4": (st, [vp, i64, i64, vp, vp, vp, vp]),
             "spg_nvfp4_sf_bytes": (ctypes.c_size_t, [i64, i64]),
             "spg_nvfp4_sf_offset": (i64, [i64, i64, i64]),
@@ -200,6 +204,31 @@ def quantize_fp8_tensor_noalloc(x: torch.Tensor, codes: torch.Tensor, scale: tor
                                                           _ptr(scale), _stream(x)),
            "spg_quantize_fp8_tensor_noalloc")
     return codes, scale
+
+
+def fp8_scale_ring(history: int, initial_scale: float = 1.0, device="cuda") -> torch.Tensor:
+    """A device amax-history ring for delayed scaling, initialised on `device`."""
+    n = int(load_library().spg_fp8_scale_ring_bytes(int(history))) // 4
+    ring = torch.empty((max(n, 4) + 3) // 4 * 4, dtype=torch.float32, device=device)
+    _check(load_library().spg_fp8_scale_ring_init(_ptr(ring), int(history), float(initial_scale),
+                                                  _stream(ring)), "spg_fp8_scale_ring_init")
+    return ring
+
+
+def quantize_fp8_tensor_delayed(x: torch.Tensor, ring: torch.Tensor, history: int, codes=None,
+                                scale_used=None):
+    """Encode x with the ring's current scale, fold amax(x) into the ring.
+    Returns (codes, scale_used)."""
+    _need(x, "x", torch.bfloat16)
+    _need(ring, "ring", torch.float32)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if codes is None else codes
+    scale_used = (torch.empty((4,), dtype=torch.float32, device=x.device)
+                  if scale_used is None else scale_used)
+    _check(load_library().spg_quantize_fp8_tensor_delayed(_ptr(x), x.numel(), _ptr(codes),
+                                                          _ptr(scale_used), _ptr(ring),
+                                                          int(history), _stream(x)),
+           "spg_quantize_fp8_tensor_delayed")
+    return codes, scale_used
 
 
 def nvfp4_global_scale(x: torch.Tensor, g=None, amax_scratch=None):

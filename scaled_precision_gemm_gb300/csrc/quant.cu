@@ -212,6 +212,61 @@ __global__ void __launch_bounds__(1024) reduce_partials_kernel(float* __restrict
   if (threadIdx.x == 0) partials[kStaticPartials] = a;
 }
 
+// ----------------------------------------------------------------------
+// Delayed scaling: one kernel encodes with the scale published by the
+// previous call and folds this call's amax into the history ring; its last
+// block (elected by an atomic counter after a __threadfence) reduces the
+// window and publishes the next scale.  Ring layout (fp32 words):
+//   [0, H) history   [H] scale   [H+1] amax of the call in flight
+//   [H+2] block counter (u32)   [H+3] next history index (u32)
+__global__ void __launch_bounds__(256) quantize_fp8_delayed_kernel(const uint4* __restrict__ x,
+                                                                  int64_t nvec,
+                                                                  uint2* __restrict__ codes,
+                                                                  float* __restrict__ scale_used,
+                                                                  float* ring, int history) {
+  __shared__ float red[8];
+  __shared__ bool last;
+  const float s = *reinterpret_cast<volatile float*>(ring + history);
+  float a = 0.f;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(x + i);
+    a = fmaxf(a, vec_amax(v));
+    codes[i] = vec_encode_e4m3(v, s);
+  }
+  a = block_max<256>(a, red);
+  unsigned int* amax_bits = reinterpret_cast<unsigned int*>(ring + history + 1);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(ring + history + 2);
+  unsigned int* idx = reinterpret_cast<unsigned int*>(ring + history + 3);
+  if (threadIdx.x == 0) {
+    if (a > 0.f) atomicMax(amax_bits, __float_as_uint(a));
+    __threadfence();
+    last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (last && threadIdx.x == 0) {
+    __threadfence();
+    const float amax = __uint_as_float(atomicExch(amax_bits, 0u));
+    const unsigned int k = *reinterpret_cast<volatile unsigned int*>(idx);
+    ring[k] = amax;
+    float m = 0.f;
+    for (int h = 0; h < history; ++h) m = fmaxf(m, reinterpret_cast<volatile float*>(ring)[h]);
+    *scale_used = s;
+    ring[history] = (m == 0.f) ? 1.f : __fdiv_rn(m, 448.f);
+    *idx = (k + 1 == unsigned(history)) ? 0u : k + 1;
+    *counter = 0u;
+    __threadfence();
+  }
+}
+
+__global__ void scale_ring_init_kernel(float* ring, int history, float initial_scale) {
+  for (int i = threadIdx.x; i < history + 4; i += blockDim.x) {
+    float v = 0.f;
+    if (i == history) v = initial_scale;
+    ring[i] = v;
+  }
+}
+
 int grid_for(int64_t work, int threads) {
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   int64_t g = (work + threads - 1) / threads;
@@ -350,5 +405,38 @@ extern "C" spg_status spg_quantize_fp8_tensor_noalloc(const void* x, int64_t num
   spg::encode_fp8_tensor_kernel<<<spg::grid_for(nvec > 0 ? nvec : 1, 256), 256, 0, stream>>>(
       static_cast<const uint4*>(x), nvec, scratch + spg::kStaticPartials,
       reinterpret_cast<uint2*>(codes), scale);
+  return launch_status();
+}
+
+extern "C" size_t spg_fp8_scale_ring_bytes(int history) {
+  if (history <= 0) return 0;
+  return (static_cast<size_t>(history) + 4) * sizeof(float);
+}
+
+extern "C" spg_status spg_fp8_scale_ring_init(void* ring, int history, float initial_scale,
+                                              spg_stream_t stream) {
+  if (!ring || history <= 0 || history > 65536 || !(initial_scale > 0.f))
+    return SPG_ERR_INVALID_ARG;
+  if (!aligned16(ring)) return SPG_ERR_MISALIGNED;
+  spg::scale_ring_init_kernel<<<1, 256, 0, stream>>>(static_cast<float*>(ring), history,
+                                                     initial_scale);
+  return launch_status();
+}
+
+extern "C" spg_status spg_quantize_fp8_tensor_delayed(const void* x, int64_t numel,
+                                                      uint8_t* codes, float* scale_used,
+                                                      void* ring, int history,
+                                                      spg_stream_t stream) {
+  if (numel < 0 || !scale_used || !ring || history <= 0 || history > 65536)
+    return SPG_ERR_INVALID_ARG;
+  if (numel > 0 && (!x || !codes)) return SPG_ERR_INVALID_ARG;
+  if (numel % 8 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if ((numel > 0 && (!aligned16(x) || !aligned16(codes))) || !aligned16(scale_used) ||
+      !aligned16(ring))
+    return SPG_ERR_MISALIGNED;
+  const int64_t nvec = numel / 8;
+  spg::quantize_fp8_delayed_kernel<<<spg::grid_for(nvec > 0 ? nvec : 1, 256), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), nvec, reinterpret_cast<uint2*>(codes), scale_used,
+      static_cast<float*>(ring), history);
   return launch_status();
 }

@@ -465,3 +465,35 @@ def test_bias_is_added_after_scales_and_before_epilogue():
     d = (oracle.fp8_tensor_gemm("NT", At, sAt, Bt, sBt, T, N, K, bias=b)
          - oracle.fp8_tensor_gemm("NT", At, sAt, Bt, sBt, T, N, K))
     np.testing.assert_allclose(d[0], np.broadcast_to(bf, (T, N)), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------- delayed scaling
+def test_delayed_scaling_ring_sequence():
+    """Each call uses the scale published by the previous one; the next scale
+    is max(history)/448 over the last H amaxes (worked sequence)."""
+    ring = oracle.DelayedScaleRing(history=3, initial_scale=1.0)
+    mags = [2.0, 8.0, 0.5, 0.25, 0.25]
+    xs = [f32_to_bf16_bits(np.array([m, -m / 2, 0.0, m / 4], np.float32)) for m in mags]
+    used = []
+    for x in xs:
+        codes, s = ring.step(x)
+        used.append(float(s))
+        # codes are exactly E4M3(x / s) with the scale in force
+        xf = torch.tensor(bf16_bits_to_f32(x)) / torch.tensor(np.float32(s))
+        assert np.array_equal(codes, xf.to(torch.float8_e4m3fn).view(torch.uint8).numpy()) \
+            or np.abs(bf16_bits_to_f32(x)).max() / s > 448  # saturated values differ from torch
+    f = lambda a: float(np.float32(a) / np.float32(448))
+    # window of 3: after 2 -> 2/448; after 8 -> 8/448; after .5 -> 8/448; after .25 -> 8/448
+    # (8 still in window), after .25 -> .5/448 (8 left the window)
+    assert used == [1.0, f(2), f(8), f(8), f(8)]
+    assert float(ring.scale[0]) == f(0.5)
+    assert ring.hist.tolist() == [0.25, 0.25, 0.5] and int(ring.idx[0]) == 2
+
+
+def test_delayed_scaling_saturates_when_amax_grows():
+    ring = oracle.DelayedScaleRing(history=2, initial_scale=float(np.float32(1) / np.float32(448)))
+    x = f32_to_bf16_bits(np.array([1.0, 2.0, -4.0, 0.5], np.float32))
+    codes, s = ring.step(x)
+    # the scale in force maps 1.0 to 448: larger magnitudes saturate to +-448
+    assert codes.tolist() == [0x7E, 0x7E, 0xFE, 0x76]
+    assert float(ring.scale[0]) == float(np.float32(4) / np.float32(448))
