@@ -85,6 +85,9 @@ typedef struct {
   int64_t tiles;        /* output tiles of the whole problem (all batches)    */
   int32_t smem_bytes;   /* dynamic shared memory per CTA                      */
   int32_t variant;      /* kernel variant index inside the library            */
+  int32_t split_n;      /* last partial wave: tiles split along N this many ways */
+  int32_t split_k;      /* last partial wave: tiles split along K this many ways */
+  int64_t workspace_bytes; /* workspace the K split needs (0 without one)     */
 } spg_route;
 
 /* Human-readable name of a status code (static string). */
@@ -113,7 +116,9 @@ SPG_API spg_status spg_last_device_error(spg_stream_t stream);
 /* Same as spg_last_device_error, and stores the raw code of the first wait
  * that ran out (0 if none) in *code: 0x101 ring slot free, 0x102 ring slot
  * full, 0x103 accumulator free, 0x104 accumulator full, 0x105 drain,
- * 0x106 injected stall (spg_debug_inject_stall). */
+ * 0x106 injected stall (spg_debug_inject_stall), 0x107 a K-split arrival
+ * counter could not be updated (bounded compare-and-swap loop), 0x108 the
+ * epilogue warps of a K-split piece did not meet. */
 SPG_API spg_status spg_last_device_error_code(spg_stream_t stream, uint32_t* code);
 
 /* ---------------------------------------------------------------------
@@ -292,6 +297,47 @@ SPG_API spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t ba
                                         int64_t strideC, int64_t M, int64_t N, int64_t K,
                                         spg_stream_t stream);
 
+/* Workspace entry points: the GEMMs above, plus a caller-owned device
+ * workspace that lets the last partial wave of two-SM tiles (every tile,
+ * when the problem has fewer tiles than CTA pairs: narrow T such as decode
+ * and small prefill chunks) be split along K into up to 4 pieces.  Each
+ * piece writes its fp32 partial sums to the workspace; the CTA whose piece
+ * arrives last adds all pieces in split order (so the result does not
+ * depend on the arrival order and repeats bit for bit) and runs the fused
+ * epilogue.  The result is the same GEMM as the plain entry points define,
+ * with fp32 sums taken in a different order.  The pages keep a separate
+ * small-T route on sm_120 (ninfer PR #160, the paragraph on the quantizer's
+ * plane layout); here the tcgen05 pair kernel covers narrow T by this split.
+ *
+ * workspace: device memory, 16-byte aligned, at least
+ *   spg_gemm_workspace_bytes(kind, T, N, K, epilogue, batch) bytes for the
+ *   split to be used (for fp8_tensor_gemm_ws the size covers both B
+ *   layouts); with less (or nullptr) the call runs the plain route.
+ *   Needs no initialisation: its arrival counters are tagged with a per-call
+ *   number and every completed call leaves them at zero.  One workspace
+ *   serves one launch at a time (calls on one stream may share it).
+ * Other arguments, rules and errors as for the _bias entry points. */
+SPG_API int64_t spg_gemm_workspace_bytes(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
+                                         int64_t batch);
+SPG_API spg_status fp8_rowscaled_gemm_ws(const uint8_t* A, const float* sa, const uint8_t* W,
+                                         const float* sw, const void* bias,
+                                         const float* bias_scale, const void* residual, void* Y,
+                                         int64_t T, int64_t N, int64_t K, int epilogue,
+                                         void* workspace, int64_t workspace_bytes,
+                                         spg_stream_t stream);
+SPG_API spg_status nvfp4_gemm_ws(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                 const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                 const void* bias, const float* bias_scale, const void* residual,
+                                 void* Y, int64_t T, int64_t N, int64_t K, int epilogue,
+                                 void* workspace, int64_t workspace_bytes, spg_stream_t stream);
+SPG_API spg_status fp8_tensor_gemm_ws(char layout_a, char layout_b, int64_t batch,
+                                      const uint8_t* A, int64_t strideA, const float* sA,
+                                      const uint8_t* B, int64_t strideB, const float* sB,
+                                      const void* bias, const float* bias_scale, void* C,
+                                      int64_t strideC, int64_t M, int64_t N, int64_t K,
+                                      void* workspace, int64_t workspace_bytes,
+                                      spg_stream_t stream);
+
 /* Per-shape tile / route selector (host only, no device query after the
  * first call).  kind: spg_kind; T: rows of the output (M for the tensor
  * GEMM).  Fills *out with the configuration the GEMM entry points would
@@ -300,6 +346,10 @@ SPG_API spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t ba
  * 152 SMs. */
 SPG_API spg_status spg_select_route(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
                             int64_t batch, spg_route* out);
+/* The route of the workspace entry points given a large enough workspace
+ * (split_k > 1 and workspace_bytes > 0 when the K split is taken). */
+SPG_API spg_status spg_select_route_ws(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
+                                       int64_t batch, spg_route* out);
 
 #ifdef __cplusplus
 }

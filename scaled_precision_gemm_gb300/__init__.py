@@ -47,7 +47,8 @@ class Route(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("acc_buffers", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("smem_bytes", ctypes.c_int32),
-                ("variant", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("split_n", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
 
 
 def library_path() -> str:
@@ -94,6 +95,14 @@ def load_library():
                                      vp]),
             "fp8_tensor_gemm_bias": (st, [ctypes.c_char, ctypes.c_char, i64, vp, i64, vp, vp, i64,
                                           vp, vp, vp, vp, i64, i64, i64, i64, vp]),
+            "spg_select_route_ws": (st, [i32, i64, i64, i64, i32, i64, ctypes.POINTER(Route)]),
+            "spg_gemm_workspace_bytes": (i64, [i32, i64, i64, i64, i32, i64]),
+            "fp8_rowscaled_gemm_ws": (st, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                           vp, i64, vp]),
+            "nvfp4_gemm_ws": (st, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                   vp, i64, vp]),
+            "fp8_tensor_gemm_ws": (st, [ctypes.c_char, ctypes.c_char, i64, vp, i64, vp, vp, i64,
+                                        vp, vp, vp, vp, i64, i64, i64, i64, vp, i64, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -157,13 +166,29 @@ def last_device_error_code(device=None) -> int:
     return int(code.value)
 
 
-def select_route(kind, T, N, K, epilogue="linear", batch=1) -> dict:
+def select_route(kind, T, N, K, epilogue="linear", batch=1, workspace=False) -> dict:
+    """Route of the plain entry points, or (workspace=True) of the workspace
+    entry points given a large enough workspace."""
     r = Route()
     k = KINDS[kind] if isinstance(kind, str) else int(kind)
     e = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
-    _check(load_library().spg_select_route(k, T, N, K, e, batch, ctypes.byref(r)),
-           "spg_select_route")
+    fn = load_library().spg_select_route_ws if workspace else load_library().spg_select_route
+    _check(fn(k, T, N, K, e, batch, ctypes.byref(r)), "spg_select_route")
     return {f: getattr(r, f) for f, _ in Route._fields_}
+
+
+def gemm_workspace_bytes(kind, T, N, K, epilogue="linear", batch=1) -> int:
+    """Bytes of workspace that let the workspace entry points split K."""
+    k = KINDS[kind] if isinstance(kind, str) else int(kind)
+    e = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    return int(load_library().spg_gemm_workspace_bytes(k, T, N, K, e, batch))
+
+
+def gemm_workspace(kind, T, N, K, epilogue="linear", batch=1, device="cuda"):
+    """A workspace tensor (uint8) sized for this GEMM, or None when its route
+    does not split K."""
+    n = gemm_workspace_bytes(kind, T, N, K, epilogue, batch)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
 
 
 # ------------------------------------------------------------- quantizers
@@ -284,9 +309,19 @@ def _check_bias(bias, bias_scale, N):
         raise ValueError("bias must have N elements")
 
 
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    _need(workspace, "workspace", torch.uint8, 1)
+    return _ptr(workspace), workspace.numel()
+
+
 def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None, bias=None,
-                       bias_scale=None):
-    """Y = epilogue((A . W^T) * sa[:, None] * sw[None, :] [+ bias]) in bf16."""
+                       bias_scale=None, workspace=None):
+    """Y = epilogue((A . W^T) * sa[:, None] * sw[None, :] [+ bias]) in bf16.
+
+    workspace (uint8 device tensor, see gemm_workspace) selects the
+    workspace entry point, which may split K over the last partial wave."""
     _need(A, "A", torch.uint8, 2)
     _need(W, "W", torch.uint8, 2)
     _need(sa, "sa", torch.float32, 1)
@@ -305,7 +340,12 @@ def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None,
     _need(out, "out", torch.bfloat16, 2)
     _check_bias(bias, bias_scale, N)
     res = _ptr(residual if e == 1 else None)
-    if bias is None:
+    if workspace is not None:
+        wp, wn = _ws(workspace)
+        st = load_library().fp8_rowscaled_gemm_ws(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
+                                                  _ptr(bias), _ptr(bias_scale), res, _ptr(out),
+                                                  T, N, K, e, wp, wn, _stream(A))
+    elif bias is None:
         st = load_library().fp8_rowscaled_gemm(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), res,
                                                _ptr(out), T, N, K, e, _stream(A))
     else:
@@ -317,7 +357,7 @@ def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None,
 
 
 def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=None, bias=None,
-               bias_scale=None):
+               bias_scale=None, workspace=None):
     """Y = epilogue(block-scaled NVFP4 product * gA * gW [+ bias]) in bf16; A/W packed [rows, K/2]."""
     for t, n, d in ((A, "A", torch.uint8), (W, "W", torch.uint8), (sfA, "sfA", torch.uint8),
                     (sfW, "sfW", torch.uint8), (gA, "gA", torch.float32),
@@ -340,7 +380,12 @@ def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=Non
     _need(out, "out", torch.bfloat16, 2)
     _check_bias(bias, bias_scale, N)
     res = _ptr(residual if e == 1 else None)
-    if bias is None:
+    if workspace is not None:
+        wp, wn = _ws(workspace)
+        st = load_library().nvfp4_gemm_ws(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW),
+                                          _ptr(gW), _ptr(bias), _ptr(bias_scale), res, _ptr(out),
+                                          T, N, K, e, wp, wn, _stream(A))
+    elif bias is None:
         st = load_library().nvfp4_gemm(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW),
                                        res, _ptr(out), T, N, K, e, _stream(A))
     else:
@@ -352,7 +397,7 @@ def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=Non
 
 
 def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, strideB=None,
-                    out=None, strideC=None, bias=None, bias_scale=None):
+                    out=None, strideC=None, bias=None, bias_scale=None, workspace=None):
     """C[b] = bf16(sA*sB*opA(A[b]) opB(B[b])), layout in {'NT','NN','TN','TT'}.
 
     A / B are flat (or any contiguous) uint8 buffers; matrix b starts at
@@ -375,7 +420,13 @@ def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, s
         raise ValueError("output buffer too small")
     _check_bias(bias, bias_scale, N)
     lib = load_library()
-    if bias is None:
+    if workspace is not None:
+        wp, wn = _ws(workspace)
+        st = lib.fp8_tensor_gemm_ws(layout[0].encode(), layout[1].encode(), batch, _ptr(A),
+                                    strideA, _ptr(sA), _ptr(B), strideB, _ptr(sB), _ptr(bias),
+                                    _ptr(bias_scale), _ptr(out), strideC, M, N, K, wp, wn,
+                                    _stream(A))
+    elif bias is None:
         st = lib.fp8_tensor_gemm(layout[0].encode(), layout[1].encode(), batch, _ptr(A), strideA,
                                  _ptr(sA), _ptr(B), strideB, _ptr(sB), _ptr(out), strideC, M, N,
                                  K, _stream(A))

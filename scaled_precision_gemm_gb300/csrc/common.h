@@ -19,6 +19,9 @@ uint64_t wait_timeout_ns();
 // Test hook set by spg_debug_inject_stall (one-CTA GEMM kernels only).
 bool debug_stall_enabled();
 
+// Call number tagging the arrival counters of a K-split launch (never 0).
+uint32_t next_split_epoch();
+
 // Streaming multiprocessors of the current device (queried once per device).
 int num_sms();
 

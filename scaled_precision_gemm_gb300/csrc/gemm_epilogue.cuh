@@ -34,16 +34,164 @@ __device__ __forceinline__ void load_residual_chunk(const GemmParams& p, int m, 
   }
 }
 
+// Per-warp resources of the K-split reduction: a scratch area in the
+// shared-memory operand ring (idle by then: a K-split piece is always the
+// last item of its CTA pair, so every stage has been consumed once its
+// accumulator is full) and one mbarrier for the bulk copies into it.
+struct SplitScratch {
+  uint8_t* buf;        // 1024-byte aligned
+  int bytes;           // at least 4096
+  uint64_t* bar;       // this warp's copy barrier (arrival count 1)
+  uint32_t* phase;     // its parity, kept by the caller across items
+};
+
+// K-split piece of a tile (two-SM kernels).  The calling warp owns TMEM
+// lane quarter q = row / 32 (t_row addresses column 0 of the tile's
+// accumulator in that quarter) and accumulator columns [c0, c0 + ncols), a
+// multiple of 32.  rows_live: some row of the quarter is inside the output.
+//  1. The piece's partial sums go to its workspace slice.
+//  2. Every epilogue warp arrives on split_bars[0] once its writes are
+//     fenced; the first epilogue thread then counts the CTA's arrival on the
+//     tile's counter and posts the outcome through split_bars[1].
+//  3. In the CTA of the last piece to arrive, every warp bulk-copies the
+//     other pieces' 4 KB blocks of its rows into its scratch, adds all
+//     pieces in split order (its own from TMEM, so the total does not depend
+//     on the arrival order) and writes the total back to TMEM, where the
+//     ordinary epilogue picks it up.
+// Returns 1 if this CTA holds the total, 0 if not, -1 if a wait ran out.
+// Nothing waits for another CTA, so pieces never rely on running at the same
+// time; the waits inside the CTA are bounded like every other.  `phase`
+// counts the K-split pieces this CTA has processed (mod 2).  At most 4
+// pieces per tile.
+template <int BN>
+__device__ __forceinline__ int split_piece_reduce(const GemmParams& p, uint32_t t_row,
+                                                  const WorkItem& tc, int rank, int row, int c0,
+                                                  int ncols, bool rows_live, uint64_t* split_bars,
+                                                  int* flag, uint32_t phase,
+                                                  const SplitScratch& scr, const WaitCtl& ctl) {
+  const int lane = threadIdx.x & 31;
+  const int q = row >> 5;
+  const bool have_k = tc.kb_end > tc.kb_begin;
+  if (rows_live) {
+    float4* own = split_slice(p, tc.tail, tc.split, rank, BN);
+#pragma unroll 1
+    for (int c = c0; c < c0 + ncols; c += 32) {
+      uint32_t r[32];
+      if (have_k) {
+        tmem_ld_32x32b_x32(t_row + c, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      float4* blk = own + split_block_index(c >> 5, q) + lane;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        __stcg(blk + g * 32,
+               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+    }
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&split_bars[0]);
+  if (threadIdx.x == 64) {  // first epilogue thread
+    int outcome = -1;
+    if (mbar_wait(&split_bars[0], phase, ctl, kErrWaitSplit)) {
+      const int before = split_arrive(p, tc.tail, rank);
+      __threadfence();
+      outcome = before == p.split_k - 1 ? 1 : 0;
+    }
+    *reinterpret_cast<volatile int*>(flag) = outcome;
+    mbar_arrive(&split_bars[1]);
+  }
+  if (!mbar_wait(&split_bars[1], phase, ctl, kErrWaitSplit)) return -1;
+  const int outcome = *reinterpret_cast<volatile int*>(flag);
+  if (outcome <= 0 || !rows_live) return outcome;
+  __threadfence();
+
+  const int own_s = tc.split;
+  const int others = p.split_k - 1;
+  const int nbuf = scr.bytes >> 12;
+  int per_round = nbuf / others;  // chunks whose other blocks fit the scratch at once
+  if (per_round < 1) per_round = 1;
+  const int nchunks = ncols >> 5;
+#pragma unroll 1
+  for (int ch0 = 0; ch0 < nchunks; ch0 += per_round) {
+    const int nch = nchunks - ch0 < per_round ? nchunks - ch0 : per_round;
+    if (lane == 0) {
+      fence_proxy_async_global();
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(scr.bar, uint32_t(nch * others) * 4096u);
+      for (int i = 0; i < nch; ++i) {
+        const int chunk = (c0 >> 5) + ch0 + i;
+        for (int k = 0; k < others; ++k) {
+          const int s2 = k + (k >= own_s ? 1 : 0);
+          const float4* src =
+              split_slice(p, tc.tail, s2, rank, BN) + split_block_index(chunk, q);
+          bulk_load(scr.buf + (i * others + k) * 4096, src, 4096u, scr.bar);
+        }
+      }
+    }
+    __syncwarp();
+    if (!mbar_wait(scr.bar, *scr.phase, ctl, kErrWaitSplit)) return -1;
+    *scr.phase ^= 1u;
+#pragma unroll 1
+    for (int i = 0; i < nch; ++i) {
+      const int c = c0 + (ch0 + i) * 32;
+      uint32_t r[32];
+      if (have_k) {
+        tmem_ld_32x32b_x32(t_row + c, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0u;
+      }
+      const float4* blk = reinterpret_cast<const float4*>(scr.buf + i * others * 4096) + lane;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 mine = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                        __uint_as_float(r[4 * g + 2]),
+                                        __uint_as_float(r[4 * g + 3]));
+        for (int s2 = 0; s2 < p.split_k; ++s2) {
+          const float4 x =
+              s2 == own_s ? mine : blk[(s2 - (s2 > own_s ? 1 : 0)) * 256 + g * 32];
+          t.x += x.x;
+          t.y += x.y;
+          t.z += x.z;
+          t.w += x.w;
+        }
+        r[4 * g] = __float_as_uint(t.x);
+        r[4 * g + 1] = __float_as_uint(t.y);
+        r[4 * g + 2] = __float_as_uint(t.z);
+        r[4 * g + 3] = __float_as_uint(t.w);
+      }
+      tmem_st_32x32b_x32(t_row + c, r);
+    }
+    __syncwarp();
+  }
+  tmem_wait_st();
+  return 1;
+}
+
 // ItemFn(item) -> WorkItem with mb already offset for this CTA's rows (a
 // whole tile has n_off = 0, width = BN); the loop runs over items
 // [item_begin, item_end) with stride item_step.  ArriveEmpty(buf) releases
-// accumulator buffer `buf` to the MMA issuer.
+// accumulator buffer `buf` to the MMA issuer.  K-split pieces (two-SM
+// kernels only) go through split_piece_reduce first; cta_rank, split_bars
+// (two mbarriers: arrival count 4 and 1), split_flag (one shared int),
+// copy_bars (one mbarrier of count 1 per epilogue warp) and the operand ring
+// (ring, ring_bytes: the warps' scratch) serve them.
 template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtensorMap* tmY,
                                               uint32_t tmem_base, uint64_t* acc_full,
                                               ArriveEmpty arrive_empty, uint8_t* epi_smem,
                                               int item_begin, int item_end, int item_step,
-                                              ItemFn item_fn, const WaitCtl& ctl) {
+                                              ItemFn item_fn, const WaitCtl& ctl, int cta_rank,
+                                              uint64_t* split_bars, int* split_flag,
+                                              uint64_t* copy_bars, uint8_t* ring,
+                                              int ring_bytes) {
   using E = EpilogueCfg<EPI, SCALE, BN>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -52,14 +200,34 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
   uint8_t* stage0 = epi_smem + (e * 2) * E::kBufBytes;
   int it = 0;
   int chunk_ctr = 0;
+  uint32_t split_phase = 0, copy_phase = 0;
+  const int scr_bytes = (ring_bytes / 4) & ~4095;
+  const SplitScratch scr{ring + e * scr_bytes, scr_bytes, copy_bars + e, &copy_phase};
   float scalar = 1.f;
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
-  const bool have_k = p.num_k_blocks > 0;
 
   for (int item = item_begin; item < item_end; item += item_step, ++it) {
     const int buf = it & 1;
     const uint32_t acc_ph = (it >> 1) & 1;
     const WorkItem tc = item_fn(item);
+    const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+    if (tc.split >= 0) {
+      if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
+      tc_fence_after();
+      const int outcome = split_piece_reduce<BN>(
+          p, t_row, tc, cta_rank, q * 32 + lane, 0, tc.width, tc.mb * 128 + q * 32 < p.M,
+          split_bars, split_flag, split_phase, scr, ctl);
+      split_phase ^= 1u;
+      if (outcome < 0) break;
+      if (outcome == 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_empty(buf);
+        continue;
+      }
+    }
+    // After a K-split reduction TMEM holds the total of all pieces.
+    const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
     const int m0 = tc.mb * 128;
     const int n0 = tc.nb * BN + tc.n_off;  // first accumulator column of the item (global)
     const int nch = tc.width / E::kAccColsPerChunk;
@@ -87,9 +255,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
     uint4 res_cur[4];
     if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n0, row_ok, res_cur);
 
-    if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
-    tc_fence_after();
-    const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+    if (tc.split < 0) {
+      if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
+      tc_fence_after();
+    }
 
 #pragma unroll
     for (int c = 0; c < E::kChunks; ++c) {
@@ -196,12 +365,17 @@ namespace spg {
 // epilogue and stores -- so the next tile's main loop overlaps the math and
 // the stores although TMEM holds one accumulator (the rest of TMEM holds the
 // block scales of the NVFP4 pipeline).
-template <int EPI, int SCALE, bool HAS_BIAS, typename TileFn, typename ArriveEmpty>
+// ItemFn(item) -> WorkItem (mb offset for this CTA); K-split pieces are
+// reduced first as in epilogue_loop.
+template <int EPI, int SCALE, bool HAS_BIAS, typename ItemFn, typename ArriveEmpty>
 __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, const CUtensorMap* tmY,
                                                        uint32_t tmem_base, uint64_t* acc_full,
                                                        ArriveEmpty arrive_empty, uint8_t* epi_smem,
-                                                       int tile_begin, int tile_step, TileFn tile_fn,
-                                                       const WaitCtl& ctl) {
+                                                       int item_begin, int item_step, ItemFn item_fn,
+                                                       const WaitCtl& ctl, int cta_rank,
+                                                       uint64_t* split_bars, int* split_flag,
+                                                       uint64_t* copy_bars, uint8_t* ring,
+                                                       int ring_bytes) {
   constexpr int kCols = 128;                 // accumulator columns per warp
   constexpr int kBufBytes = 32 * 64;
   constexpr int kOutChunks = EPI == SPG_EPI_SWIGLU ? 2 : 4;  // 32-wide output chunks
@@ -213,12 +387,30 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
   uint8_t* stage0 = epi_smem + (e * 2) * kBufBytes;
   int it = 0;
   int chunk_ctr = 0;
+  uint32_t split_phase = 0, copy_phase = 0;
+  const int scr_bytes = (ring_bytes / 8) & ~4095;
+  const SplitScratch scr{ring + e * scr_bytes, scr_bytes, copy_bars + e, &copy_phase};
   float scalar = 1.f;
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
-  const bool have_k = p.num_k_blocks > 0;
 
-  for (int tile = tile_begin; tile < p.total_tiles; tile += tile_step, ++it) {
-    const TileCoord tc = tile_fn(tile);
+  for (int item = item_begin; item < p.total_items; item += item_step, ++it) {
+    const WorkItem tc = item_fn(item);
+    if (tc.split >= 0) {
+      if (!mbar_wait(&acc_full[0], it & 1, ctl, kErrWaitAccFull)) break;
+      tc_fence_after();
+      const int outcome = split_piece_reduce<256>(
+          p, tmem_base + (uint32_t(q * 32) << 16), tc, cta_rank, q * 32 + lane, half * kCols,
+          kCols, tc.mb * 128 + q * 32 < p.M, split_bars, split_flag, split_phase, scr, ctl);
+      split_phase ^= 1u;
+      if (outcome < 0) break;
+      if (outcome == 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_empty(0);
+        continue;
+      }
+    }
+    const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
     const int m0 = tc.mb * 128;
     const int n_acc0 = tc.nb * 256 + half * kCols;  // first accumulator column of this warp
     const int m = m0 + q * 32 + lane;
@@ -240,8 +432,10 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
     uint4 res_cur[4];
     if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
 
-    if (!mbar_wait(&acc_full[0], it & 1, ctl, kErrWaitAccFull)) break;
-    tc_fence_after();
+    if (tc.split < 0) {
+      if (!mbar_wait(&acc_full[0], it & 1, ctl, kErrWaitAccFull)) break;
+      tc_fence_after();
+    }
     uint32_t acc[kCols];
     const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(half * kCols);
     if (have_k) {

@@ -30,8 +30,10 @@ namespace {
 
 spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, const float* sw,
                           const void* bias, const float* bias_scale, const void* residual, void* Y,
-                          int64_t T, int64_t N, int64_t K, int epilogue, spg_stream_t stream) {
-  if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2) return SPG_ERR_INVALID_ARG;
+                          int64_t T, int64_t N, int64_t K, int epilogue, void* workspace,
+                          int64_t workspace_bytes, spg_stream_t stream) {
+  if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2 || workspace_bytes < 0)
+    return SPG_ERR_INVALID_ARG;
   if (T == 0 || N == 0) return SPG_OK;
   if (!A || !sa || !W || !sw || !Y || (epilogue == SPG_EPI_ADD && !residual))
     return SPG_ERR_INVALID_ARG;
@@ -39,10 +41,11 @@ spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, c
       T > kMaxDim || N > kMaxDim || K > kMaxDim)
     return SPG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(A) || !aligned16(sa) || !aligned16(W) || !aligned16(sw) || !aligned16(Y) ||
-      (epilogue == SPG_EPI_ADD && !aligned16(residual)))
+      (epilogue == SPG_EPI_ADD && !aligned16(residual)) || !aligned16(workspace))
     return SPG_ERR_MISALIGNED;
 
-  const spg_route r = select_route_internal(SPG_KIND_FP8_ROWSCALED, T, N, K, epilogue, 1, false);
+  const spg_route r = route_for(SPG_KIND_FP8_ROWSCALED, T, N, K, epilogue, 1, false, workspace,
+                                workspace_bytes);
   const int b_rows = r.block_m == 256 ? r.block_n / 2 : r.block_n;  // B rows staged per CTA
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;
@@ -57,7 +60,7 @@ spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, c
   spg_route rr = r;
   if (r.block_m == 256) {
     const int pairs = num_sms() / 2;
-    plan_tail_split(p, pairs, r.block_n, epilogue, true);
+    plan_items(p, r, pairs, workspace);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
     const uint32_t narrow_rows = static_cast<uint32_t>(r.block_n / p.split_ways / 2);
     if (!make_tmap_3d(&maps.b_narrow, W, false, K, N, 1, K, K * N, 128, narrow_rows, 128))
@@ -79,7 +82,8 @@ extern "C" spg_status fp8_rowscaled_gemm(const uint8_t* A, const float* sa, cons
                                          const float* sw, const void* residual, void* Y,
                                          int64_t T, int64_t N, int64_t K, int epilogue,
                                          spg_stream_t stream) {
-  return rowscaled_impl(A, sa, W, sw, nullptr, nullptr, residual, Y, T, N, K, epilogue, stream);
+  return rowscaled_impl(A, sa, W, sw, nullptr, nullptr, residual, Y, T, N, K, epilogue, nullptr, 0,
+                        stream);
 }
 
 extern "C" spg_status fp8_rowscaled_gemm_bias(const uint8_t* A, const float* sa, const uint8_t* W,
@@ -87,5 +91,16 @@ extern "C" spg_status fp8_rowscaled_gemm_bias(const uint8_t* A, const float* sa,
                                               const float* bias_scale, const void* residual,
                                               void* Y, int64_t T, int64_t N, int64_t K,
                                               int epilogue, spg_stream_t stream) {
-  return rowscaled_impl(A, sa, W, sw, bias, bias_scale, residual, Y, T, N, K, epilogue, stream);
+  return rowscaled_impl(A, sa, W, sw, bias, bias_scale, residual, Y, T, N, K, epilogue, nullptr, 0,
+                        stream);
+}
+
+extern "C" spg_status fp8_rowscaled_gemm_ws(const uint8_t* A, const float* sa, const uint8_t* W,
+                                            const float* sw, const void* bias,
+                                            const float* bias_scale, const void* residual, void* Y,
+                                            int64_t T, int64_t N, int64_t K, int epilogue,
+                                            void* workspace, int64_t workspace_bytes,
+                                            spg_stream_t stream) {
+  return rowscaled_impl(A, sa, W, sw, bias, bias_scale, residual, Y, T, N, K, epilogue, workspace,
+                        workspace_bytes, stream);
 }

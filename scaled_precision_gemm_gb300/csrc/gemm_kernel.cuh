@@ -281,9 +281,9 @@ __global__ void __launch_bounds__(192, 1)
         p.total_tiles, gridDim.x,
         [&](int tile) {
           const TileCoord tc = tile_coord(tile, p);
-          return WorkItem{tc.b, tc.mb, tc.nb, 0, BN};
+          return WorkItem{tc.b, tc.mb, tc.nb, 0, BN, 0, p.num_k_blocks, -1, 0};
         },
-        ctl);
+        ctl, 0, nullptr, nullptr, nullptr, nullptr, 0);
   }
 
   tc_fence_before();

@@ -17,8 +17,9 @@
 // Every wait is bounded in time, as in the one-CTA kernel.
 //
 // Schedule: pair p processes work items p, p + pairs, ...; the last partial
-// wave of tiles is split along N into narrower items (work_item), whose
-// MMAs carry the narrower N in the instruction descriptor.
+// wave of tiles is split along N into narrower items, whose MMAs carry the
+// narrower N in the instruction descriptor, or along K into pieces whose
+// partial sums meet in a workspace (work_item, split_piece_reduce).
 #pragma once
 
 #include "gemm_epilogue.cuh"
@@ -48,7 +49,8 @@ struct Gemm2smCfg {
   static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(2 * STAGES + 7 + kEpiWarps <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(STAGES * kStageBytes / kEpiWarps >= 3 * 4096, "K-split scratch too small");
 
   // kind::f8f6f4, E4M3 x E4M3 -> f32, M = 256 (pair), N = BN.
   __host__ __device__ static constexpr uint32_t idesc() {
@@ -74,8 +76,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* split_bars = drain + 1;  // K-split pieces: gather (4 warps), broadcast (1)
+  uint64_t* copy_bars = split_bars + 2;  // K-split reduction: one per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(copy_bars + Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* split_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -93,6 +98,9 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&acc_empty[b], 2 * Cfg::kEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(&split_bars[0], Cfg::kEpiWarps);
+    mbar_init(&split_bars[1], 1);
+    for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&copy_bars[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -126,7 +134,7 @@ __global__ void __launch_bounds__(192, 1)
         const int nb0 = tc.nb * BN + tc.n_off + int(rank) * (tc.width / 2);
         const int za = tc.b * p.a_batch_mul;
         const int zb = tc.b * p.b_batch_mul;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = tc.kb_begin; kb < tc.kb_end; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, ctl, kErrWaitEmpty)) {
             ok = false;
             break;
@@ -175,13 +183,14 @@ __global__ void __launch_bounds__(192, 1)
       for (int item = pair; ok && item < p.total_items; item += num_pairs, ++it) {
         const int buf = it & 1;
         const uint32_t acc_ph = (it >> 1) & 1;
-        const int width = work_item(item, p, BN).width;
+        const WorkItem w = work_item(item, p, BN);
+        const int width = w.width;
         // The instruction descriptor's N field carries the item's width.
         const uint32_t idesc = (kIdesc & ~(0x3Fu << 17)) | (uint32_t(width >> 3) << 17);
         if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull)) {
             ok = false;
             break;
@@ -200,7 +209,7 @@ __global__ void __launch_bounds__(192, 1)
               bdesc = smem_desc(sb + j * 32 * 128, 16384, 1024, kSwizzle128B);
             else
               bdesc = smem_desc(sb + j * 32, 16, 1024, kSwizzle128B);
-            mma_f8f6f4_pair(d_tmem, adesc, bdesc, idesc, (kb | j) != 0);
+            mma_f8f6f4_pair(d_tmem, adesc, bdesc, idesc, (kb != w.kb_begin) || j != 0);
           }
           tc_commit_pair_multicast(&empty[s], 0x3);
           if (++s == STAGES) {
@@ -225,7 +234,7 @@ __global__ void __launch_bounds__(192, 1)
           w.mb = w.mb * 2 + int(rank);
           return w;
         },
-        ctl);
+        ctl, int(rank), split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes);
   }
 
   tc_fence_before();

@@ -19,6 +19,8 @@ enum : unsigned int {
   kErrWaitAccFull = 0x104,
   kErrDrain = 0x105,
   kErrInjectedStall = 0x106,
+  kErrSplitCounter = 0x107,
+  kErrWaitSplit = 0x108,
 };
 
 struct GemmParams {
@@ -46,11 +48,21 @@ struct GemmParams {
   const uint8_t* sfb;
   int sf_tiles_per_row_block;  // K / 64
   // Tail split (two-SM kernels): work items [0, split_full) are whole tiles;
-  // the remaining tiles are each split along N into split_ways pieces so the
-  // last, partial wave is split_ways times shorter.  total_items counts both.
+  // the remaining tiles are each split along N into split_ways pieces, or
+  // along K into split_k pieces of kb_per_split K blocks, so the last,
+  // partial wave is shorter.  total_items counts both kinds of item.
   int split_full;
   int split_ways;
+  int split_k;
+  int kb_per_split;
   int total_items;
+  // K-split workspace: per (tail tile, split, CTA of the pair) one 128 x BN
+  // fp32 slice of partial sums, then one 64-bit arrival counter per (tail
+  // tile, CTA).  A counter holds (epoch << 32) | arrivals; a value tagged
+  // with another epoch counts as zero arrivals.
+  float* ws_partial;
+  unsigned long long* ws_counter;
+  uint32_t epoch;
   uint64_t timeout_ns;  // bound of every pipeline wait
   uint64_t drain_ns;    // bound of the exit waits for copies / MMAs in flight
   unsigned int* err;
@@ -59,9 +71,12 @@ struct GemmParams {
 
 // One unit of work of the persistent schedule: a tile, or a piece of one.
 struct WorkItem {
-  int b, mb, nb;  // batch, m-block, n-block of the tile
-  int n_off;      // first accumulator column of the piece inside the tile
-  int width;      // accumulator columns of the piece
+  int b, mb, nb;         // batch, m-block, n-block of the tile
+  int n_off;             // first accumulator column of the piece inside the tile
+  int width;             // accumulator columns of the piece
+  int kb_begin, kb_end;  // K blocks the piece reduces over
+  int split;             // K-split index of the piece, -1 for an unsplit K range
+  int tail;              // tile index relative to split_full (K-split pieces)
 };
 
 struct TileCoord {
@@ -86,10 +101,25 @@ __device__ __forceinline__ TileCoord tile_coord(int tile, const GemmParams& p) {
 __device__ __forceinline__ WorkItem work_item(int item, const GemmParams& p, int bn) {
   WorkItem w;
   int tile = item, piece = 0, ways = 1;
+  w.split = -1;
+  w.tail = 0;
+  w.kb_begin = 0;
+  w.kb_end = p.num_k_blocks;
   if (item >= p.split_full) {
-    ways = p.split_ways;
-    tile = p.split_full + (item - p.split_full) / ways;
-    piece = (item - p.split_full) % ways;
+    const int rel = item - p.split_full;
+    if (p.split_k > 1) {
+      w.tail = rel / p.split_k;
+      w.split = rel - w.tail * p.split_k;
+      tile = p.split_full + w.tail;
+      w.kb_begin = w.split * p.kb_per_split;
+      const int e = w.kb_begin + p.kb_per_split;
+      w.kb_end = e < p.num_k_blocks ? e : p.num_k_blocks;
+      if (w.kb_begin > w.kb_end) w.kb_begin = w.kb_end;
+    } else {
+      ways = p.split_ways;
+      tile = p.split_full + rel / ways;
+      piece = rel % ways;
+    }
   }
   const TileCoord tc = tile_coord(tile, p);
   w.b = tc.b;
@@ -98,6 +128,54 @@ __device__ __forceinline__ WorkItem work_item(int item, const GemmParams& p, int
   w.width = bn / ways;
   w.n_off = piece * w.width;
   return w;
+}
+
+// ---------------------------------------------------------------- K split
+// Slice of partial sums of (tail tile, split, CTA rank): 128 rows x bn fp32,
+// stored as float4 groups ordered (32-column chunk, 32-row quarter, 4-column
+// group, row in the quarter): the lanes of an epilogue warp (32 consecutive
+// rows) write 512 contiguous bytes per access, and the 32 x 32 block of one
+// warp and chunk is one contiguous 4 KB run that a bulk copy moves whole.
+__device__ __forceinline__ float4* split_slice(const GemmParams& p, int tail, int split, int rank,
+                                               int bn) {
+  const int64_t idx = (int64_t(tail) * p.split_k + split) * 2 + rank;
+  return reinterpret_cast<float4*>(p.ws_partial + idx * 128 * bn);
+}
+
+// float4 index of (column col, row) inside a slice.
+__device__ __forceinline__ int split_f4_index(int col, int row) {
+  return (((col >> 5) * 4 + (row >> 5)) * 8 + ((col >> 2) & 7)) * 32 + (row & 31);
+}
+
+// float4 index of the 4 KB block of (chunk, quarter) inside a slice.
+__device__ __forceinline__ int split_block_index(int chunk, int quarter) {
+  return (chunk * 4 + quarter) * 256;
+}
+
+// Record one arrival on the counter of (tail tile, CTA rank) and return how
+// many pieces arrived before (0 .. split_k - 1).  Called by one thread after
+// the CTA's partial sums are written and fenced.  The last arrival puts the
+// counter back to zero so the workspace stays clean for the next call.
+__device__ __forceinline__ int split_arrive(const GemmParams& p, int tail, int rank) {
+  unsigned long long* c = p.ws_counter + tail * 2 + rank;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c);
+  int before = -1;
+  for (int i = 0; i < (1 << 20); ++i) {
+    const bool mine = uint32_t(old >> 32) == p.epoch;
+    const unsigned long long nv = mine ? old + 1ull : ((unsigned long long)p.epoch << 32) | 1ull;
+    const unsigned long long prev = atomicCAS(c, old, nv);
+    if (prev == old) {
+      before = mine ? int(uint32_t(old)) : 0;
+      break;
+    }
+    old = prev;
+  }
+  if (before < 0) {
+    atomicCAS(p.err, 0u, kErrSplitCounter);
+    return 0;
+  }
+  if (before == p.split_k - 1) *reinterpret_cast<volatile unsigned long long*>(c) = 0ull;
+  return before;
 }
 
 // Bias of accumulator column n (0 when there is none or n is out of range).

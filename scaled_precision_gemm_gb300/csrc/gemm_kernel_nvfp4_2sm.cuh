@@ -45,6 +45,9 @@ struct Nvfp4PairCfg {
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
   static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(2 * STAGES + 5 + 2 + kEpiWarps <= kBarBytes / 8 - 2,
+                "no room for the K-split barriers");
+  static_assert(STAGES * kStageBytes / kEpiWarps >= 3 * 4096, "K-split scratch too small");
 
   // Block-scaled descriptor: A, B = E2M1 (1), UE4M3 scales, M = 256, N = 256, K = 64.
   __host__ __device__ static constexpr uint32_t idesc() {
@@ -73,8 +76,11 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* split_bars = drain + 1;  // K-split pieces: gather (8 warps), broadcast (1)
+  uint64_t* copy_bars = split_bars + 2;  // K-split reduction: one per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(copy_bars + Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* split_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -90,6 +96,9 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * Cfg::kEpiWarps);
     mbar_init(drain, 1);
+    mbar_init(&split_bars[0], Cfg::kEpiWarps);
+    mbar_init(&split_bars[1], 1);
+    for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&copy_bars[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -120,8 +129,8 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
       const int64_t tpr = p.sf_tiles_per_row_block;
       const int a_row_blocks = (p.M + 127) / 128;
       const int b_row_blocks = (p.N + 127) / 128;
-      for (int tile = pair; ok && tile < p.total_tiles; tile += num_pairs) {
-        const TileCoord tc = tile_coord(tile, p);
+      for (int item = pair; ok && item < p.total_items; item += num_pairs) {
+        const WorkItem tc = work_item(item, p, Cfg::kBN);
         const int a_rb = tc.mb * 2 + int(rank);
         const int m0 = a_rb * 128;
         const int n0 = tc.nb * 256 + int(rank) * 128;
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
         const int a_rb_sf = a_rb < a_row_blocks ? a_rb : a_row_blocks - 1;
         const int b_rb0 = tc.nb * 2 < b_row_blocks ? tc.nb * 2 : b_row_blocks - 1;
         const int b_rb1 = tc.nb * 2 + 1 < b_row_blocks ? tc.nb * 2 + 1 : b_row_blocks - 1;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = tc.kb_begin; kb < tc.kb_end; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, ctl, kErrWaitEmpty)) {
             ok = false;
             break;
@@ -174,10 +183,11 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.total_tiles; tile += num_pairs, ++it) {
+      for (int item = pair; ok && item < p.total_items; item += num_pairs, ++it) {
+        const WorkItem w = work_item(item, p, Cfg::kBN);
         if (!mbar_wait(acc_empty, (it & 1) ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull)) {
             ok = false;
             break;
@@ -201,7 +211,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
             const uint32_t col = sf_col0 + uint32_t(j * Cfg::kSfColsPerKStep);
             mma_nvf4_pair(tmem_base, smem_desc(sa + j * 32, 16, 1024, kSwizzle128B),
                           smem_desc(sb + j * 32, 16, 1024, kSwizzle128B), kIdesc, col, col + 4,
-                          (kb | j) != 0);
+                          (kb != w.kb_begin) || j != 0);
           }
           tc_commit_pair_multicast(&empty[s], 0x3);
           if (++s == STAGES) {
@@ -221,12 +231,12 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
         p, &tmY, tmem_base, acc_full,
         [&](int) { mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0)); }, epi, pair,
         num_pairs,
-        [&](int tile) {
-          TileCoord tc = tile_coord(tile, p);
-          tc.mb = tc.mb * 2 + int(rank);
-          return tc;
+        [&](int item) {
+          WorkItem w = work_item(item, p, Cfg::kBN);
+          w.mb = w.mb * 2 + int(rank);
+          return w;
         },
-        ctl);
+        ctl, int(rank), split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes);
   }
 
   tc_fence_before();

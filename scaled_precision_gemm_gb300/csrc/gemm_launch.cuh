@@ -136,7 +136,12 @@ inline void fill_common_params(GemmParams& p, const spg_route& r, int64_t M, int
   p.sf_tiles_per_row_block = 0;
   p.split_full = p.total_tiles;
   p.split_ways = 1;
+  p.split_k = 1;
+  p.kb_per_split = p.num_k_blocks;
   p.total_items = p.total_tiles;
+  p.ws_partial = nullptr;
+  p.ws_counter = nullptr;
+  p.epoch = 0;
   p.timeout_ns = wait_timeout_ns();
   // Exit waits keep a generous bound even under a short pipeline bound, so a
   // CTA never leaves with a copy or an MMA still writing its memory.
@@ -161,16 +166,37 @@ inline spg_status set_bias(GemmParams& p, const void* bias, const float* bias_sc
   return SPG_OK;
 }
 
-// Split the last partial wave of a two-SM schedule along N: with U pairs and
-// P tiles, the P mod U tiles of the last wave become 2 or 4 narrower items
-// each (the most that still fit in that wave), so the wave ends 2 or 4 times
-// sooner.  A problem of fewer than U tiles is one partial wave.
-inline void plan_tail_split(GemmParams& p, int units, int bn, int epilogue, bool allowed) {
+// Work items of a two-SM schedule (`units` CTA pairs) from the route's plan
+// for its last partial wave: whole tiles, then that wave's tiles split
+// r.split_n ways along N, or r.split_k ways along K with their partial sums
+// and arrival counters in `workspace` (at least r.workspace_bytes).
+inline void plan_items(GemmParams& p, const spg_route& r, int units, void* workspace) {
   const int tiles = p.total_tiles;
-  const int ways = allowed ? tail_split_ways(tiles, units, bn, epilogue) : 1;
-  p.split_ways = ways;
-  p.split_full = ways > 1 ? tiles - tiles % units : tiles;
-  p.total_items = p.split_full + (tiles - p.split_full) * p.split_ways;
+  if (r.split_k > 1) {
+    const KSplit k = ksplit_plan(tiles, units, p.num_k_blocks);  // the selector's plan
+    p.split_k = k.split_k;
+    p.kb_per_split = k.kb_per_split;
+    p.split_full = tiles - static_cast<int>(k.tail_tiles);
+    p.total_items = p.split_full + static_cast<int>(k.tail_tiles) * k.split_k;
+    p.ws_partial = static_cast<float*>(workspace);
+    p.ws_counter = reinterpret_cast<unsigned long long*>(
+        static_cast<char*>(workspace) + k.tail_tiles * k.split_k * 2 * 128 * int64_t(r.block_n) * 4);
+    p.epoch = next_split_epoch();
+  } else if (r.split_n > 1) {
+    p.split_ways = r.split_n;
+    p.split_full = tiles - tiles % units;
+    p.total_items = p.split_full + (tiles - p.split_full) * p.split_ways;
+  }
+}
+
+// Route of a GEMM entry point: with a workspace the last partial wave may be
+// split along K, if the workspace is large enough for the plan.
+inline spg_route route_for(int kind, int64_t T, int64_t N, int64_t K, int epilogue, int64_t batch,
+                           bool b_mn, const void* workspace, int64_t workspace_bytes) {
+  spg_route r = select_route_internal(kind, T, N, K, epilogue, batch, b_mn, workspace != nullptr);
+  if (r.workspace_bytes > workspace_bytes)
+    r = select_route_internal(kind, T, N, K, epilogue, batch, b_mn, false);
+  return r;
 }
 
 }  // namespace spg

@@ -23,8 +23,10 @@ namespace {
 spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, const uint8_t* W,
                       const uint8_t* sfW, const float* gW, const void* bias,
                       const float* bias_scale, const void* residual, void* Y, int64_t T,
-                      int64_t N, int64_t K, int epilogue, spg_stream_t stream) {
-  if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2) return SPG_ERR_INVALID_ARG;
+                      int64_t N, int64_t K, int epilogue, void* workspace,
+                      int64_t workspace_bytes, spg_stream_t stream) {
+  if (T < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2 || workspace_bytes < 0)
+    return SPG_ERR_INVALID_ARG;
   if (T == 0 || N == 0) return SPG_OK;
   if (!A || !sfA || !gA || !W || !sfW || !gW || !Y || (epilogue == SPG_EPI_ADD && !residual))
     return SPG_ERR_INVALID_ARG;
@@ -32,10 +34,12 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
       T > kMaxDim || N > kMaxDim || K > kMaxDim)
     return SPG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(A) || !aligned16(sfA) || !aligned16(gA) || !aligned16(W) || !aligned16(sfW) ||
-      !aligned16(gW) || !aligned16(Y) || (epilogue == SPG_EPI_ADD && !aligned16(residual)))
+      !aligned16(gW) || !aligned16(Y) || (epilogue == SPG_EPI_ADD && !aligned16(residual)) ||
+      !aligned16(workspace))
     return SPG_ERR_MISALIGNED;
 
-  const spg_route r = select_route_internal(SPG_KIND_NVFP4, T, N, K, epilogue, 1, false);
+  const spg_route r =
+      route_for(SPG_KIND_NVFP4, T, N, K, epilogue, 1, false, workspace, workspace_bytes);
   const int64_t kh = K / 2;
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;
@@ -62,10 +66,16 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
   p.sfa = sfA;
   p.sfb = sfW;
   p.sf_tiles_per_row_block = static_cast<int>(K / 64);
+  spg_route rr = r;
+  if (r.block_m == 256) {
+    const int pairs = num_sms() / 2;
+    plan_items(p, r, pairs, workspace);
+    rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+  }
   switch (epilogue) {
-    case SPG_EPI_LINEAR: return launch<SPG_EPI_LINEAR>(r, maps, p, stream);
-    case SPG_EPI_ADD: return launch<SPG_EPI_ADD>(r, maps, p, stream);
-    default: return launch<SPG_EPI_SWIGLU>(r, maps, p, stream);
+    case SPG_EPI_LINEAR: return launch<SPG_EPI_LINEAR>(rr, maps, p, stream);
+    case SPG_EPI_ADD: return launch<SPG_EPI_ADD>(rr, maps, p, stream);
+    default: return launch<SPG_EPI_SWIGLU>(rr, maps, p, stream);
   }
 }
 
@@ -76,7 +86,7 @@ extern "C" spg_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const flo
                                  const void* residual, void* Y, int64_t T, int64_t N, int64_t K,
                                  int epilogue, spg_stream_t stream) {
   return nvfp4_impl(A, sfA, gA, W, sfW, gW, nullptr, nullptr, residual, Y, T, N, K, epilogue,
-                    stream);
+                    nullptr, 0, stream);
 }
 
 extern "C" spg_status nvfp4_gemm_bias(const uint8_t* A, const uint8_t* sfA, const float* gA,
@@ -85,5 +95,15 @@ extern "C" spg_status nvfp4_gemm_bias(const uint8_t* A, const uint8_t* sfA, cons
                                       const void* residual, void* Y, int64_t T, int64_t N,
                                       int64_t K, int epilogue, spg_stream_t stream) {
   return nvfp4_impl(A, sfA, gA, W, sfW, gW, bias, bias_scale, residual, Y, T, N, K, epilogue,
-                    stream);
+                    nullptr, 0, stream);
+}
+
+extern "C" spg_status nvfp4_gemm_ws(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                    const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                    const void* bias, const float* bias_scale,
+                                    const void* residual, void* Y, int64_t T, int64_t N, int64_t K,
+                                    int epilogue, void* workspace, int64_t workspace_bytes,
+                                    spg_stream_t stream) {
+  return nvfp4_impl(A, sfA, gA, W, sfW, gW, bias, bias_scale, residual, Y, T, N, K, epilogue,
+                    workspace, workspace_bytes, stream);
 }

@@ -34,10 +34,12 @@ namespace {
 spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_t* A,
                        int64_t strideA, const float* sA, const uint8_t* B, int64_t strideB,
                        const float* sB, const void* bias, const float* bias_scale, void* C,
-                       int64_t strideC, int64_t M, int64_t N, int64_t K, spg_stream_t stream) {
+                       int64_t strideC, int64_t M, int64_t N, int64_t K, void* workspace,
+                       int64_t workspace_bytes, spg_stream_t stream) {
   if ((layout_a != 'N' && layout_a != 'T') || (layout_b != 'N' && layout_b != 'T'))
     return SPG_ERR_INVALID_ARG;
-  if (batch < 0 || M < 0 || N < 0 || K < 0 || strideA < 0 || strideB < 0 || strideC < 0)
+  if (batch < 0 || M < 0 || N < 0 || K < 0 || strideA < 0 || strideB < 0 || strideC < 0 ||
+      workspace_bytes < 0)
     return SPG_ERR_INVALID_ARG;
   if (batch == 0 || M == 0 || N == 0) return SPG_OK;
   if (!A || !B || !C || !sA || !sB) return SPG_ERR_INVALID_ARG;
@@ -51,11 +53,12 @@ spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_
         (strideA != 0 && strideA < M * K) || (strideB != 0 && strideB < N * K))
       return SPG_ERR_UNSUPPORTED_SHAPE;
   }
-  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA) || !aligned16(sB))
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA) || !aligned16(sB) ||
+      !aligned16(workspace))
     return SPG_ERR_MISALIGNED;
 
-  const spg_route r =
-      select_route_internal(SPG_KIND_FP8_TENSOR, M, N, K, SPG_EPI_LINEAR, batch, b_mn);
+  const spg_route r = route_for(SPG_KIND_FP8_TENSOR, M, N, K, SPG_EPI_LINEAR, batch, b_mn,
+                                workspace, workspace_bytes);
   const int b_rows = r.block_m == 256 ? r.block_n / 2 : r.block_n;  // B rows staged per CTA
   const bool a_batched = batch > 1 && strideA != 0;
   const bool b_batched = batch > 1 && strideB != 0;
@@ -85,7 +88,7 @@ spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_
   spg_route rr = r;
   if (r.block_m == 256) {
     const int pairs = num_sms() / 2;
-    plan_tail_split(p, pairs, r.block_n, SPG_EPI_LINEAR, !b_mn);
+    plan_items(p, r, pairs, workspace);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
     if (!b_mn) {
       const uint32_t narrow_rows = static_cast<uint32_t>(r.block_n / p.split_ways / 2);
@@ -114,7 +117,7 @@ extern "C" spg_status fp8_tensor_gemm(char layout_a, char layout_b, int64_t batc
                                       int64_t strideC, int64_t M, int64_t N, int64_t K,
                                       spg_stream_t stream) {
   return tensor_impl(layout_a, layout_b, batch, A, strideA, sA, B, strideB, sB, nullptr, nullptr, C,
-                     strideC, M, N, K, stream);
+                     strideC, M, N, K, nullptr, 0, stream);
 }
 
 extern "C" spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t batch,
@@ -124,5 +127,16 @@ extern "C" spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t
                                            int64_t strideC, int64_t M, int64_t N, int64_t K,
                                            spg_stream_t stream) {
   return tensor_impl(layout_a, layout_b, batch, A, strideA, sA, B, strideB, sB, bias, bias_scale,
-                     C, strideC, M, N, K, stream);
+                     C, strideC, M, N, K, nullptr, 0, stream);
+}
+
+extern "C" spg_status fp8_tensor_gemm_ws(char layout_a, char layout_b, int64_t batch,
+                                         const uint8_t* A, int64_t strideA, const float* sA,
+                                         const uint8_t* B, int64_t strideB, const float* sB,
+                                         const void* bias, const float* bias_scale, void* C,
+                                         int64_t strideC, int64_t M, int64_t N, int64_t K,
+                                         void* workspace, int64_t workspace_bytes,
+                                         spg_stream_t stream) {
+  return tensor_impl(layout_a, layout_b, batch, A, strideA, sA, B, strideB, sB, bias, bias_scale,
+                     C, strideC, M, N, K, workspace, workspace_bytes, stream);
 }

@@ -50,6 +50,13 @@ spg_status cuda_status(cudaError_t e, const char* where) {
   return SPG_ERR_CUDA;
 }
 
+uint32_t next_split_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
+
 bool debug_stall_enabled() { return g_debug_stall.load(std::memory_order_relaxed) != 0; }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -146,31 +153,55 @@ struct Candidate {
 }  // namespace
 
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
-                                int64_t batch, bool b_mn_major) {
+                                int64_t batch, bool b_mn_major, bool allow_ksplit) {
   spg_route r;
   std::memset(&r, 0, sizeof r);
   r.kind = kind;
   r.acc_buffers = 2;
   r.group_m = 16;
   const int sms = num_sms();
+  const int pairs = sms / 2;
   const int64_t nb = batch > 0 ? batch : 1;
   // SPG_FORCE_VARIANT pins the tile shape for A/B runs and tests:
   // 2sm | 2sm192 | 2sm160 | 2sm128 (pair tiles), 1sm256 | 1sm128 (one CTA).
+  // SPG_FORCE_TAIL = none | n | k pins how the last partial wave is split.
   const char* forced_name = std::getenv("SPG_FORCE_VARIANT");
   if (forced_name && !*forced_name) forced_name = nullptr;
   const bool force_one_cta =
       forced_name && (!std::strcmp(forced_name, "1sm256") || !std::strcmp(forced_name, "1sm128"));
+  const char* forced_tail = std::getenv("SPG_FORCE_TAIL");
+  if (forced_tail && !*forced_tail) forced_tail = nullptr;
+  const bool tail_n_ok = !forced_tail || !std::strcmp(forced_tail, "n");
+  const bool tail_k_ok = allow_ksplit && (!forced_tail || !std::strcmp(forced_tail, "k"));
+  const bool tail_none_ok = !forced_tail || !std::strcmp(forced_tail, "none");
+  const int64_t nkb = kind == SPG_KIND_NVFP4 ? (K / 2 + 127) / 128 : (K + 127) / 128;
+  const double kb = static_cast<double>(nkb);
+  const double fixed = 6.0;  // per-tile fixed cost in 128-byte-deep K blocks
+  KSplit best_ks;
+  int best_ways = 1;
   if (kind == SPG_KIND_NVFP4) {
-    // Two-SM 256x256 pair tile, or the one-CTA 128x128 tile when its waves
-    // are cheaper (narrow T: more, smaller tiles spread the weight stream
-    // over more SMs).  The one-CTA tile runs at about 0.6 of the pair tile's
-    // per-SM rate on GB300.
+    // Two-SM 256x256 pair tile (optionally with a K split of its last
+    // partial wave), or the one-CTA 128x128 tile when its waves are cheaper
+    // (narrow T: more, smaller tiles spread the weight stream over more
+    // SMs).  The one-CTA tile runs at about 0.6 of the pair tile's per-SM
+    // rate on GB300.
     const int64_t t2 = ((T + 255) / 256) * ((N + 255) / 256) * nb;
     const int64_t t1 = ((T + 127) / 128) * ((N + 127) / 128) * nb;
-    const double w2 = static_cast<double>((t2 + sms / 2 - 1) / (sms / 2)) * 2.0;
+    const double full2 = static_cast<double>(t2 / pairs);
+    double w2 = (t2 % pairs) ? full2 + 1.0 : full2;
+    KSplit ks = ksplit_plan(t2, pairs, nkb);
+    if (ks.split_k > 1 && tail_k_ok) {
+      const double wk = full2 + (ksplit_piece_time(ks, 256) + fixed) / (kb + fixed);
+      if (wk < w2 || !tail_none_ok) {
+        w2 = wk;
+        best_ks = ks;
+      }
+    }
+    w2 *= 2.0;
     const double w1 = static_cast<double>((t1 + sms - 1) / sms) * 1.0 / 0.6;
     bool one_cta = w1 < w2;
     if (forced_name) one_cta = force_one_cta;
+    if (one_cta) best_ks = KSplit();
     r.block_m = one_cta ? 128 : 256;
     r.block_n = one_cta ? 128 : 256;
     r.block_k = 256;
@@ -188,8 +219,6 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     constexpr int kCands = sizeof(cands) / sizeof(cands[0]);
     static const char* const kNames[kCands] = {"2sm", "2sm192", "2sm160", "2sm128", "1sm256",
                                                "1sm128"};
-    const double kb = static_cast<double>((K + 127) / 128);
-    const double fixed = 6.0;  // per-tile fixed cost in 128-deep K blocks
     double best = 1e300;
     int best_i = 0;
     for (int i = 0; i < kCands; ++i) {
@@ -197,18 +226,42 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
       if (forced_name && std::strcmp(forced_name, kNames[i]) != 0) continue;
       if (b_mn_major && !c.mn_b_ok) continue;
       if (epilogue == SPG_EPI_SWIGLU && c.block_n % 64 != 0) continue;
-      const int units = c.block_m == 256 ? sms / 2 : sms;
+      const int units = c.block_m == 256 ? pairs : sms;
       const int64_t tiles = ((T + c.block_m - 1) / c.block_m) * ((N + c.block_n - 1) / c.block_n) * nb;
-      // Whole waves, plus the last partial wave shortened by the tail split
-      // of the two-SM kernel (when B is K-major).
-      const int ways =
-          (c.block_m == 256 && !b_mn_major) ? tail_split_ways(tiles, units, c.block_n, epilogue) : 1;
-      const double waves =
-          static_cast<double>(tiles / units) + ((tiles % units) ? tail_item_time(ways) : 0.0);
-      const double cost = waves * (c.block_n / 128.0) * (kb + fixed) / c.eff;
+      const double full = static_cast<double>(tiles / units);
+      const bool partial = (tiles % units) != 0;
+      // The last partial wave: whole tiles, or (two-SM tiles) split along N
+      // (K-major B only) or along K (with a workspace).
+      double tail = 1e300;
+      int ways = 1;
+      KSplit ks;
+      if (!partial) {
+        tail = 0.0;
+      } else {
+        if (tail_none_ok || c.block_m != 256) tail = kb + fixed;
+        if (c.block_m == 256 && !b_mn_major && tail_n_ok) {
+          const int w = tail_split_ways(tiles, units, c.block_n, epilogue);
+          if (w > 1 && tail_item_time(w) * (kb + fixed) < tail) {
+            tail = tail_item_time(w) * (kb + fixed);
+            ways = w;
+          }
+        }
+        if (c.block_m == 256 && tail_k_ok) {
+          const KSplit k = ksplit_plan(tiles, units, nkb);
+          if (k.split_k > 1 && ksplit_piece_time(k, c.block_n) + fixed < tail) {
+            tail = ksplit_piece_time(k, c.block_n) + fixed;
+            ks = k;
+            ways = 1;
+          }
+        }
+        if (tail >= 1e299) continue;  // the forced tail split does not apply
+      }
+      const double cost = (full * (kb + fixed) + tail) * (c.block_n / 128.0) / c.eff;
       if (cost < best * (1.0 - 1e-9)) {
         best = cost;
         best_i = i;
+        best_ways = ways;
+        best_ks = ks;
       }
     }
     r.block_m = cands[best_i].block_m;
@@ -219,11 +272,18 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   }
   const int64_t tiles = ((T + r.block_m - 1) / r.block_m) * ((N + r.block_n - 1) / r.block_n) * nb;
   r.tiles = tiles;
-  const int units = r.block_m == 256 ? sms / 2 : sms;
+  const int units = r.block_m == 256 ? pairs : sms;
   int64_t items = tiles;
-  if (r.block_m == 256 && kind != SPG_KIND_NVFP4 && !b_mn_major) {
-    const int ways = tail_split_ways(tiles, units, r.block_n, epilogue);
-    items = tiles - tiles % units + (tiles % units) * ways;
+  r.split_n = 1;
+  r.split_k = 1;
+  r.workspace_bytes = 0;
+  if (r.block_m == 256 && best_ks.split_k > 1) {
+    r.split_k = best_ks.split_k;
+    r.workspace_bytes = ksplit_workspace_bytes(best_ks, r.block_n);
+    items = tiles - best_ks.tail_tiles + best_ks.tail_tiles * best_ks.split_k;
+  } else if (r.block_m == 256 && best_ways > 1) {
+    r.split_n = best_ways;
+    items = tiles - tiles % units + (tiles % units) * best_ways;
   }
   const int64_t g = items < units ? items : units;
   r.grid = static_cast<int>((g < 1 ? 1 : g) * (r.block_m == 256 ? 2 : 1));
@@ -238,7 +298,6 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     if (r.block_m == 256) epi_warps = 4;
   }
   r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + 256;
-  (void)epilogue;
   return r;
 }
 
@@ -258,7 +317,7 @@ extern "C" const char* spg_status_string(int s) {
   }
 }
 
-extern "C" int spg_version(void) { return 100; }
+extern "C" int spg_version(void) { return 101; }
 
 extern "C" void spg_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed);
@@ -306,6 +365,27 @@ extern "C" spg_status spg_select_route(int kind, int64_t T, int64_t N, int64_t K
   if (!out || kind < 0 || kind > 2 || T < 0 || N < 0 || K < 0 || batch < 0 || epilogue < 0 ||
       epilogue > 2)
     return SPG_ERR_INVALID_ARG;
-  *out = select_route_internal(kind, T, N, K, epilogue, batch, false);
+  *out = select_route_internal(kind, T, N, K, epilogue, batch, false, false);
   return SPG_OK;
+}
+
+extern "C" spg_status spg_select_route_ws(int kind, int64_t T, int64_t N, int64_t K,
+                                          int epilogue, int64_t batch, spg_route* out) {
+  if (!out || kind < 0 || kind > 2 || T < 0 || N < 0 || K < 0 || batch < 0 || epilogue < 0 ||
+      epilogue > 2)
+    return SPG_ERR_INVALID_ARG;
+  *out = select_route_internal(kind, T, N, K, epilogue, batch, false, true);
+  return SPG_OK;
+}
+
+extern "C" int64_t spg_gemm_workspace_bytes(int kind, int64_t T, int64_t N, int64_t K,
+                                            int epilogue, int64_t batch) {
+  if (kind < 0 || kind > 2 || T <= 0 || N <= 0 || K <= 0 || batch < 0 || epilogue < 0 ||
+      epilogue > 2)
+    return 0;
+  const int64_t b = select_route_internal(kind, T, N, K, epilogue, batch, false, true).workspace_bytes;
+  if (kind != SPG_KIND_FP8_TENSOR) return b;
+  // Per-tensor GEMM: enough for either B layout (an N-major B takes other tiles).
+  const int64_t n = select_route_internal(kind, T, N, K, epilogue, batch, true, true).workspace_bytes;
+  return b > n ? b : n;
 }

@@ -21,7 +21,7 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
 bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
 
-// Tail split of a two-SM schedule (see plan_tail_split): with `units` CTA
+// Tail split of a two-SM schedule along N (see plan_items): with `units` CTA
 // pairs and `tiles` tiles of width bn, the tiles of the last partial wave
 // are split into `ways` (1, 2 or 4) narrower items, each a whole number of
 // epilogue chunks wide (32 columns, 64 for SwiGLU).
@@ -39,9 +39,55 @@ inline int tail_split_ways(int64_t tiles, int64_t units, int bn, int epilogue) {
 // the width but the A operand it stages does not (measured on GB300).
 inline double tail_item_time(int ways) { return ways <= 1 ? 1.0 : 0.45 + 0.55 / ways; }
 
+// K split of a two-SM schedule's last partial wave: the tiles of that wave
+// (tiles mod units; all tiles when there are fewer than units) are each
+// reduced by split_k pieces of kb_per_split K blocks, as many pieces as still
+// fit the wave, at most kMaxSplitK, each at least 4 K blocks deep.
+constexpr int kMaxSplitK = 4;
+struct KSplit {
+  int split_k = 1;
+  int kb_per_split = 0;
+  int64_t tail_tiles = 0;
+};
+
+inline KSplit ksplit_plan(int64_t tiles, int64_t units, int64_t nkb) {
+  KSplit k;
+  if (units <= 0 || nkb <= 0) return k;
+  const int64_t rem = tiles % units;
+  if (rem == 0) return k;
+  int64_t s = units / rem;
+  if (s > kMaxSplitK) s = kMaxSplitK;
+  while (s > 1 && (nkb + s - 1) / s < 4) --s;
+  if (s < 2) return k;
+  const int64_t kbps = (nkb + s - 1) / s;
+  s = (nkb + kbps - 1) / kbps;  // no empty piece
+  if (s < 2) return k;
+  k.split_k = static_cast<int>(s);
+  k.kb_per_split = static_cast<int>(kbps);
+  k.tail_tiles = rem;
+  return k;
+}
+
+// Workspace of a K split with tiles bn columns wide: one 128 x bn fp32 slice
+// per (tail tile, piece, CTA of the pair), then one 64-bit arrival counter
+// per (tail tile, CTA).
+inline int64_t ksplit_workspace_bytes(const KSplit& k, int bn) {
+  if (k.split_k < 2) return 0;
+  return k.tail_tiles * k.split_k * 2 * 128 * int64_t(bn) * 4 + k.tail_tiles * 2 * 8;
+}
+
+// Duration of a K-split tail piece in K blocks of the tile: its own K
+// blocks plus the partial sums written by every piece and read back by the
+// last one (about 2.5 K blocks per 128 x 256 fp32 slice, measured).
+inline double ksplit_piece_time(const KSplit& k, int bn) {
+  return k.kb_per_split + 2.5 * k.split_k * (bn / 256.0);
+}
+
 // The selector behind spg_select_route (no validation).
 // b_mn_major: the B operand is N-major (per-tensor GEMM with layout_b 'N').
+// allow_ksplit: the caller provides a workspace, so the last partial wave may
+// be split along K.
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
-                                int64_t batch, bool b_mn_major);
+                                int64_t batch, bool b_mn_major, bool allow_ksplit);
 
 }  // namespace spg

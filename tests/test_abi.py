@@ -102,6 +102,41 @@ def test_route_selector_forced_variants(lib, monkeypatch):
     assert r["tiles"] == 4 * ((5120 + r["block_n"] - 1) // r["block_n"])
 
 
+def test_route_selector_k_split(lib, monkeypatch):
+    """Workspace routes split the last partial wave along K; the plain routes never do."""
+    monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+    monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
+    for kind, T, N, K, epi in [("fp8_rowscaled", 256, 5120, 17408, "add"),
+                               ("fp8_rowscaled", 64, 6144, 5120, "linear"),
+                               ("nvfp4", 256, 5120, 17408, "add"),
+                               ("fp8_tensor", 128, 4096, 4096, "linear")]:
+        plain = spg.select_route(kind, T, N, K, epi)
+        assert plain["split_k"] == 1 and plain["workspace_bytes"] == 0
+        r = spg.select_route(kind, T, N, K, epi, workspace=True)
+        assert r["block_m"] == 256 and 2 <= r["split_k"] <= 4, (kind, T, r)
+        tail = r["tiles"] % 76 if r["tiles"] % 76 else 76
+        assert r["tiles"] < 76 and tail == r["tiles"]
+        per_tile = r["split_k"] * 2 * 128 * r["block_n"] * 4 + 16
+        assert r["workspace_bytes"] == tail * per_tile
+        ws = spg.gemm_workspace_bytes(kind, T, N, K, epi)
+        # the per-tensor size covers both B layouts
+        assert ws == r["workspace_bytes"] if kind != "fp8_tensor" else ws >= r["workspace_bytes"]
+        items = r["tiles"] * r["split_k"]
+        assert r["grid"] == 2 * min(items, 76)
+        nkb = (K // 2 if kind == "nvfp4" else K + 127) // 128
+        kbps = -(-nkb // r["split_k"])
+        assert kbps >= 4 and (r["split_k"] - 1) * kbps < nkb  # no empty piece
+    # whole waves (19 x 4 pair tiles on 76 pairs): nothing to split
+    assert spg.gemm_workspace_bytes("fp8_rowscaled", 19 * 256, 1024, 17408, "add") == 0
+    # the tail pin
+    monkeypatch.setenv("SPG_FORCE_TAIL", "none")
+    assert spg.select_route("fp8_rowscaled", 256, 5120, 17408, "add", workspace=True)[
+        "split_k"] == 1
+    monkeypatch.setenv("SPG_FORCE_TAIL", "k")
+    r = spg.select_route("fp8_rowscaled", 1024, 5120, 17408, "add", workspace=True)
+    assert r["split_k"] > 1 and r["split_n"] == 1
+
+
 def _vp(x):
     return ctypes.c_void_p(x)
 
