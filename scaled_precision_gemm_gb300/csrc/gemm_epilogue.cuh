@@ -358,6 +358,47 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
 
 namespace spg {
 
+// Side duty of the register-drain epilogue warps: a functor called while
+// they wait for the accumulator and between output chunks, which must not
+// block.  NoService: none.
+struct NoService {
+  static constexpr bool kActive = false;
+  __device__ __forceinline__ void operator()() {}
+};
+
+// Bounded wait for phase `parity` of `bar` that keeps calling svc() while it
+// waits.  The warp polls through lane 0, so every decision is warp-uniform.
+template <typename Svc>
+__device__ __forceinline__ bool wait_serving(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                             unsigned int code, Svc& svc) {
+  if constexpr (!Svc::kActive) {
+    return mbar_wait(bar, parity, ctl, code);
+  } else {
+    const int lane = threadIdx.x & 31;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+      int st = 0;
+      if (lane == 0) {
+        if (mbar_test_wait(smem_u32(bar), parity)) {
+          st = 1;
+        } else if ((i & 15u) == 0) {
+          if (*ctl.abort_flag) {
+            st = 2;
+          } else if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+            *ctl.abort_flag = 1;
+            atomicCAS(ctl.err, 0u, code);
+            st = 2;
+          }
+        }
+      }
+      st = __shfl_sync(0xffffffffu, st, 0);
+      if (st == 1) return true;
+      if (st == 2) return false;
+      svc();
+    }
+  }
+}
+
 // Register-drain epilogue for a single TMEM accumulator of 256 columns:
 // eight epilogue warps, two per TMEM lane quarter, each owning 128 columns.
 // A warp copies its 128 fp32 columns into registers, hands the accumulator
@@ -367,7 +408,8 @@ namespace spg {
 // block scales of the NVFP4 pipeline).
 // ItemFn(item) -> WorkItem (mb offset for this CTA); K-split pieces are
 // reduced first as in epilogue_loop.
-template <int EPI, int SCALE, bool HAS_BIAS, typename ItemFn, typename ArriveEmpty>
+template <int EPI, int SCALE, bool HAS_BIAS, typename ItemFn, typename ArriveEmpty,
+          typename Svc = NoService>
 __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, const CUtensorMap* tmY,
                                                        uint32_t tmem_base, uint64_t* acc_full,
                                                        ArriveEmpty arrive_empty, uint8_t* epi_smem,
@@ -375,7 +417,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
                                                        const WaitCtl& ctl, int cta_rank,
                                                        uint64_t* split_bars, int* split_flag,
                                                        uint64_t* copy_bars, uint8_t* ring,
-                                                       int ring_bytes) {
+                                                       int ring_bytes, Svc svc = Svc()) {
   constexpr int kCols = 128;                 // accumulator columns per warp
   constexpr int kBufBytes = 32 * 64;
   constexpr int kOutChunks = EPI == SPG_EPI_SWIGLU ? 2 : 4;  // 32-wide output chunks
@@ -396,7 +438,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
   for (int item = item_begin; item < p.total_items; item += item_step, ++it) {
     const WorkItem tc = item_fn(item);
     if (tc.split >= 0) {
-      if (!mbar_wait(&acc_full[0], it & 1, ctl, kErrWaitAccFull)) break;
+      if (!wait_serving(&acc_full[0], it & 1, ctl, kErrWaitAccFull, svc)) break;
       tc_fence_after();
       const int outcome = split_piece_reduce<256>(
           p, tmem_base + (uint32_t(q * 32) << 16), tc, cta_rank, q * 32 + lane, half * kCols,
@@ -433,7 +475,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
     if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
 
     if (tc.split < 0) {
-      if (!mbar_wait(&acc_full[0], it & 1, ctl, kErrWaitAccFull)) break;
+      if (!wait_serving(&acc_full[0], it & 1, ctl, kErrWaitAccFull, svc)) break;
       tc_fence_after();
     }
     uint32_t acc[kCols];
@@ -453,6 +495,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
 
 #pragma unroll
     for (int c = 0; c < kOutChunks; ++c, ++chunk_ctr) {
+      svc();
       float o[32];
       if constexpr (EPI == SPG_EPI_SWIGLU) {
         float biasr[2] = {0.f, 0.f};

@@ -1,0 +1,322 @@
+// Two-SM block-scaled NVFP4 GEMM with the scale factors written into TMEM by
+// warps (tcgen05.st) instead of copied by the tensor core (tcgen05.cp),
+// sm_103a.
+//
+// The tile, the operand ring, the producer, the MMAs and the register-drain
+// epilogue are those of gemm_kernel_nvfp4_2sm.  What changes is how each
+// stage's scales reach TMEM.  A block-scaled MMA computing the rows of one
+// TMEM lane quarter reads its scales from that quarter's 32 lanes: lane i of
+// every quarter must hold, in the 4 columns of a scale group, the words (four
+// E4M3 scales each) of rows i, 32 + i, 64 + i and 96 + i of the 128-row
+// block -- the layout a tcgen05.cp 32x128b.warpx4 produces by broadcasting a
+// 512-byte scale tile to the four quarters (measured on GB300: with the B
+// scales of one quarter only, the other quarters' rows come out wrong).  That
+// copy runs in the tensor pipe, where the 12 copies of a stage cost about as
+// much time as its 4 MMAs.  Here the eight epilogue warps store the same 12
+// groups with tcgen05.st, each into its own lane quarter, outside the tensor
+// pipe: the warps with (warp - 2) / 4 == h serve the stages k with
+// k % 2 == h, one warp per quarter, whenever they wait for the accumulator
+// and between their output chunks.  The scale tiles land on a barrier of
+// their own CTA (sf_full), so they can be written up to STAGES stages ahead
+// of the MMAs.
+//
+// Barriers (per stage s): full[s] (leader; both CTAs' A/B codes), sf_full[s]
+// (each CTA; its scale tiles), sf_ready[s] (leader; 8 arrivals: the 4 scale
+// writers of each CTA), empty[s] (both CTAs; multicast commit after the
+// stage's MMAs).  Every wait is bounded.
+#pragma once
+
+#include "gemm_epilogue.cuh"
+#include "gemm_kernel_common.cuh"
+#include "gemm_kernel_nvfp4_2sm.cuh"
+
+namespace spg {
+
+template <int EPI, int STAGES>
+struct Nvfp4StCfg {
+  using Base = Nvfp4PairCfg<EPI, STAGES>;
+  static constexpr int kBN = Base::kBN;
+  static constexpr int kBKBytes = Base::kBKBytes;
+  static constexpr int kKSteps = Base::kKSteps;
+  static constexpr int kABytes = Base::kABytes;
+  static constexpr int kBBytes = Base::kBBytes;
+  static constexpr int kSfaBytes = Base::kSfaBytes;
+  static constexpr int kSfbBytes = Base::kSfbBytes;
+  static constexpr int kStageBytes = Base::kStageBytes;
+  static constexpr int kSfColsPerKStep = Base::kSfColsPerKStep;
+  static constexpr int kSfColsPerStage = Base::kSfColsPerStage;
+  static constexpr int kTmemCols = Base::kTmemCols;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * 32 * 64;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+  static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+  static_assert((4 * STAGES + 5 + 2 + kEpiWarps) * 8 + 32 <= kBarBytes, "barrier area too small");
+  static_assert(STAGES * kStageBytes / kEpiWarps >= 3 * 4096, "K-split scratch too small");
+  __host__ __device__ static constexpr uint32_t idesc() { return Base::idesc(); }
+};
+
+// Issue the stores of one stage's scales into lane quarter q: its 12 scale
+// groups (4 k-steps x {A, B rows 0-127, B rows 128-255}) at sf_col0, 4
+// columns each.  Scale tile layout in shared memory: 512 bytes per (128-row
+// block, k-step), row r's four scales at (r % 32) * 16 + (r / 32) * 4, so
+// lane i's 16 bytes are exactly the 4 columns it holds.  The caller waits
+// for the stores (tcgen05.wait::st) before it signals them.
+__device__ __forceinline__ void store_stage_scales(uint32_t tmem_base, uint32_t sf_col0,
+                                                   const uint8_t* ssfa, const uint8_t* ssfb,
+                                                   int q, int lane) {
+  const uint32_t col0 = tmem_base + (uint32_t(q * 32) << 16) + sf_col0;
+  const int off = lane * 16;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 a = *reinterpret_cast<const uint4*>(ssfa + j * 512 + off);
+    const uint4 b0 = *reinterpret_cast<const uint4*>(ssfb + j * 512 + off);
+    const uint4 b1 = *reinterpret_cast<const uint4*>(ssfb + 2048 + j * 512 + off);
+    const uint32_t col = col0 + uint32_t(j * 12);
+    tmem_st_32x32b_x4(col, a);
+    tmem_st_32x32b_x4(col + 4, b0);
+    tmem_st_32x32b_x4(col + 8, b1);
+  }
+}
+
+// The epilogue warps' side duty: store the scales of every stage of this
+// warp's parity whose scale tiles have landed, for its lane quarter, and
+// signal each one as soon as its stores are done (non-blocking).
+template <int STAGES>
+struct ScaleService {
+  static constexpr bool kActive = true;
+  int next;           // next stage to serve (this warp's parity)
+  int end;            // stages of this CTA pair
+  uint64_t* sf_full;  // this CTA's scale-tile barriers
+  uint32_t sf_ready_leader;
+  uint8_t* ring;
+  int stage_bytes, sf_offset;  // ring stride; scale tiles' offset in a stage
+  uint32_t tmem_base, sf_col_base, sf_cols_per_stage;
+  int q, lane;
+
+  __device__ __forceinline__ void operator()() {
+    while (next < end) {
+      const int s = next % STAGES;
+      const uint32_t par = uint32_t(next / STAGES) & 1u;
+      const int ready = __shfl_sync(
+          0xffffffffu, lane == 0 ? (mbar_test_wait(smem_u32(&sf_full[s]), par) ? 1 : 0) : 0, 0);
+      if (!ready) return;
+      const uint8_t* ssfa = ring + s * stage_bytes + sf_offset;
+      store_stage_scales(tmem_base, sf_col_base + uint32_t(s) * sf_cols_per_stage, ssfa,
+                         ssfa + 2048, q, lane);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(sf_ready_leader + uint32_t(s * 8));
+      next += 2;
+    }
+  }
+};
+
+template <int EPI, int STAGES, bool HAS_BIAS>
+__global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
+    gemm_kernel_nvfp4_2sm_st(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmY,
+                             const __grid_constant__ CUtensorMap tmSFA,
+                             const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+  using Cfg = Nvfp4StCfg<EPI, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* epi = smem + STAGES * Cfg::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + Cfg::kEpiBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* sf_full = bars + 2 * STAGES;
+  uint64_t* sf_ready = bars + 3 * STAGES;
+  uint64_t* acc_full = bars + 4 * STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint64_t* split_bars = drain + 1;
+  uint64_t* copy_bars = split_bars + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(copy_bars + Cfg::kEpiWarps);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* split_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_ready[s], 8);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * Cfg::kEpiWarps);
+    mbar_init(drain, 1);
+    mbar_init(&split_bars[0], Cfg::kEpiWarps);
+    mbar_init(&split_bars[1], 1);
+    for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&copy_bars[w], 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmY);
+    prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl ctl{p.timeout_ns, p.err, abort_flag};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      const int64_t tpr = p.sf_tiles_per_row_block;
+      const int a_row_blocks = (p.M + 127) / 128;
+      const int b_row_blocks = (p.N + 127) / 128;
+      for (int item = pair; ok && item < p.total_items; item += num_pairs) {
+        const WorkItem tc = work_item(item, p, Cfg::kBN);
+        const int a_rb = tc.mb * 2 + int(rank);
+        const int m0 = a_rb * 128;
+        const int n0 = tc.nb * 256 + int(rank) * 128;
+        // Scale tiles of row blocks past the operand are never multiplied by
+        // a non-zero code (TMA zero-fills those rows): read the last real
+        // block instead of running past the buffer.
+        const int a_rb_sf = a_rb < a_row_blocks ? a_rb : a_row_blocks - 1;
+        const int b_rb0 = tc.nb * 2 < b_row_blocks ? tc.nb * 2 : b_row_blocks - 1;
+        const int b_rb1 = tc.nb * 2 + 1 < b_row_blocks ? tc.nb * 2 + 1 : b_row_blocks - 1;
+        for (int kb = tc.kb_begin; kb < tc.kb_end; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, ctl, kErrWaitEmpty)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = ring + s * Cfg::kStageBytes;
+          uint8_t* sb = sa + Cfg::kABytes;
+          uint8_t* ssfa = sb + Cfg::kBBytes;
+          uint8_t* ssfb = ssfa + Cfg::kSfaBytes;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (Cfg::kABytes + Cfg::kBBytes));
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          const int kx = kb * Cfg::kBKBytes;
+          tma_load_3d_pair(sa, &tmA, bar, kx, m0, 0);
+          tma_load_3d_pair(sb, &tmB, bar, kx, n0, 0);
+          // Scale tiles: 4 consecutive 512-byte tiles per 128-row block, on
+          // this CTA's own barrier.
+          mbar_arrive_expect_tx(&sf_full[s], Cfg::kSfaBytes + Cfg::kSfbBytes);
+          const int k_tile = kb * 4;
+          tma_load_3d(ssfa, &tmSFA, &sf_full[s], 0, a_rb_sf * int(tpr) + k_tile, 0);
+          tma_load_3d(ssfb, &tmSFB, &sf_full[s], 0, b_rb0 * int(tpr) + k_tile, 0);
+          tma_load_3d(ssfb + 2048, &tmSFB, &sf_full[s], 0, b_rb1 * int(tpr) + k_tile, 0);
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // No copy may still be writing this CTA's memory (or signalling the
+      // leader's barriers) at exit.
+      const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
+      for (uint32_t i = 0; i < outstanding; ++i) {
+        const uint32_t idx = issued - 1 - i;
+        mbar_wait_drain(&sf_full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
+        if (rank == 0)
+          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t kIdesc = Cfg::idesc();
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int item = pair; ok && item < p.total_items; item += num_pairs, ++it) {
+        const WorkItem w = work_item(item, p, Cfg::kBN);
+        if (!mbar_wait(acc_empty, (it & 1) ^ 1u, ctl, kErrWaitAccEmpty)) break;
+        tc_fence_after();
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull) ||
+              !mbar_wait(&sf_ready[s], ph, ctl, kErrWaitFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(ring + s * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+          const uint32_t sf_col0 = tmem_base + uint32_t(Cfg::kBN + s * Cfg::kSfColsPerStage);
+#pragma unroll
+          for (int j = 0; j < Cfg::kKSteps; ++j) {
+            const uint32_t col = sf_col0 + uint32_t(j * Cfg::kSfColsPerKStep);
+            mma_nvf4_pair(tmem_base, smem_desc(sa + j * 32, 16, 1024, kSwizzle128B),
+                          smem_desc(sb + j * 32, 16, 1024, kSwizzle128B), kIdesc, col, col + 4,
+                          (kb != w.kb_begin) || j != 0);
+          }
+          tc_commit_pair_multicast(&empty[s], 0x3);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(acc_full, 0x3);
+      }
+      tc_commit_pair(drain);
+      mbar_wait_drain(drain, 0, p.drain_ns, p.err);
+    }
+  } else {
+    // ------------------------------------- epilogue + scale-factor stores
+    int my_stages = 0;
+    for (int item = pair; item < p.total_items; item += num_pairs) {
+      const WorkItem w = work_item(item, p, Cfg::kBN);
+      my_stages += w.kb_end - w.kb_begin;
+    }
+    ScaleService<STAGES> svc;
+    svc.next = (warp - 2) >> 2;
+    svc.end = my_stages;
+    svc.sf_full = sf_full;
+    svc.sf_ready_leader = mapa_shared(smem_u32(sf_ready), 0);
+    svc.ring = ring;
+    svc.stage_bytes = Cfg::kStageBytes;
+    svc.sf_offset = Cfg::kABytes + Cfg::kBBytes;
+    svc.tmem_base = tmem_base;
+    svc.sf_col_base = uint32_t(Cfg::kBN);
+    svc.sf_cols_per_stage = uint32_t(Cfg::kSfColsPerStage);
+    svc.q = warp & 3;
+    svc.lane = lane;
+    epilogue_loop_regdrain<EPI, kScaleScalar, HAS_BIAS>(
+        p, &tmY, tmem_base, acc_full,
+        [&](int) { mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0)); }, epi, pair,
+        num_pairs,
+        [&](int item) {
+          WorkItem w = work_item(item, p, Cfg::kBN);
+          w.mb = w.mb * 2 + int(rank);
+          return w;
+        },
+        ctl, int(rank), split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes, svc);
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+}
+
+}  // namespace spg

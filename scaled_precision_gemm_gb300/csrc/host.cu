@@ -207,7 +207,14 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     r.block_k = 256;
     r.stages = 5;
     r.acc_buffers = one_cta ? 2 : 1;
-    r.variant = one_cta ? 2 : 0;
+    // Pair tile: scales copied into TMEM by the tensor core (variant 0,
+    // SPG_FORCE_VARIANT=2sm_cp) or stored by the epilogue warps (variant 3,
+    // 2sm_st).  Measured on GB300: the warp stores free the tensor pipe
+    // (+10% for linear and SwiGLU), but the linear_add epilogue, whose
+    // residual loads keep the warps busy longer, then delays the scales.
+    const bool st_scales = forced_name ? !std::strcmp(forced_name, "2sm_st")
+                                       : epilogue != SPG_EPI_ADD;
+    r.variant = one_cta ? 2 : (st_scales ? 3 : 0);
   } else {
     // Pair tiles first (widths 256/192/160/128), then one-CTA tiles.  The
     // efficiencies are steady-state tensor-pipe fractions measured on GB300
@@ -297,7 +304,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     stage_bytes = 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
     if (r.block_m == 256) epi_warps = 4;
   }
-  r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + 256;
+  r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + (r.variant == 3 ? 512 : 256);
   return r;
 }
 

@@ -152,9 +152,11 @@ def test_fp8_k5120_full_size_sampled(T, N, epi):
 
 
 # ----------------------------------------------------------------- NVFP4
-@pytest.fixture(params=["auto", "1sm128"])
+@pytest.fixture(params=["auto", "1sm128", "2sm_cp", "2sm_st"])
 def nv_variant(request, monkeypatch):
-    """Pin the NVFP4 tile shape (two-SM 256x256 or one-CTA 128x128)."""
+    """Pin the NVFP4 kernel: two-SM 256x256 with its scales copied into TMEM
+    by the tensor core (2sm_cp) or written by warps (2sm_st), or the one-CTA
+    128x128 tile."""
     if request.param == "auto":
         monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
     else:

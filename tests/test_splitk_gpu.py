@@ -247,9 +247,10 @@ def run_nvfp4_ws(A, sfA, gA, W, sfW, gW, res, epi, ws, bias=None, bias_scale=Non
 @pytest.mark.parametrize("T,N,K", [(1, 16, 2048), (64, 512, 4096), (200, 272, 2304),
                                    (333, 400, 3072)])
 @pytest.mark.parametrize("bias", [False, True])
-def test_nvfp4_splitk_ragged(T, N, K, epi, bias, monkeypatch):
+@pytest.mark.parametrize("kernel", ["2sm_cp", "2sm_st"])
+def test_nvfp4_splitk_ragged(T, N, K, epi, bias, kernel, monkeypatch):
     monkeypatch.setenv("SPG_FORCE_TAIL", "k")
-    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm")
+    monkeypatch.setenv("SPG_FORCE_VARIANT", kernel)
     A, sfA, gA, W, sfW, gW = nvfp4_inputs(T, N, K, seed=T + N)
     res = normal_bf16((T, N), seed=71) if epi == "add" else None
     b = normal_bf16((N,), seed=72, std=2.0) if bias else None
