@@ -408,8 +408,13 @@ __device__ __forceinline__ bool wait_serving(uint64_t* bar, uint32_t parity, con
 // block scales of the NVFP4 pipeline).
 // ItemFn(item) -> WorkItem (mb offset for this CTA); K-split pieces are
 // reduced first as in epilogue_loop.
+// Residual by TMA (RES_TMA, linear_add): each 32 x 32 bf16 residual block
+// is loaded by a TMA copy into the warp's staging buffer one chunk ahead
+// (res_bars: two mbarriers per epilogue warp, one per buffer), the output is
+// computed in place and TMA-stored from the same buffer, and the wait for a
+// block is one the warp can serve svc() in.
 template <int EPI, int SCALE, bool HAS_BIAS, typename ItemFn, typename ArriveEmpty,
-          typename Svc = NoService>
+          typename Svc = NoService, bool RES_TMA = false>
 __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, const CUtensorMap* tmY,
                                                        uint32_t tmem_base, uint64_t* acc_full,
                                                        ArriveEmpty arrive_empty, uint8_t* epi_smem,
@@ -417,8 +422,11 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
                                                        const WaitCtl& ctl, int cta_rank,
                                                        uint64_t* split_bars, int* split_flag,
                                                        uint64_t* copy_bars, uint8_t* ring,
-                                                       int ring_bytes, Svc svc = Svc()) {
+                                                       int ring_bytes, Svc svc = Svc(),
+                                                       const CUtensorMap* tmR = nullptr,
+                                                       uint64_t* res_bars = nullptr) {
   constexpr int kCols = 128;                 // accumulator columns per warp
+  constexpr bool kResTma = RES_TMA && EPI == SPG_EPI_ADD;
   constexpr int kBufBytes = 32 * 64;
   constexpr int kOutChunks = EPI == SPG_EPI_SWIGLU ? 2 : 4;  // 32-wide output chunks
   const int warp = threadIdx.x >> 5;
@@ -434,9 +442,28 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
   const SplitScratch scr{ring + e * scr_bytes, scr_bytes, copy_bars + e, &copy_phase};
   float scalar = 1.f;
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
+  bool aborted = false;
+  int res_inflight = -1;  // chunk index of a residual copy not yet waited for
 
-  for (int item = item_begin; item < p.total_items; item += item_step, ++it) {
+  for (int item = item_begin; item < p.total_items && !aborted; item += item_step, ++it) {
     const WorkItem tc = item_fn(item);
+    // First residual block of the item, into the buffer of its first chunk
+    // (whose previous store, two chunks back, must have been read).  For a
+    // K-split piece only once it is known to hold the tile's total.
+    auto first_residual = [&]() {
+      if constexpr (kResTma) {
+        if (lane == 0) {
+          bulk_wait_read<1>();
+          uint64_t* bar = &res_bars[e * 2 + (chunk_ctr & 1)];
+          mbar_arrive_expect_tx(bar, kBufBytes);
+          tma_load_3d(stage0 + (chunk_ctr & 1) * kBufBytes, tmR, bar, tc.nb * 256 + half * kCols,
+                      tc.mb * 128 + q * 32, tc.b);
+        }
+        res_inflight = chunk_ctr;
+        __syncwarp();
+      }
+    };
+    if (tc.split < 0) first_residual();
     if (tc.split >= 0) {
       if (!wait_serving(&acc_full[0], it & 1, ctl, kErrWaitAccFull, svc)) break;
       tc_fence_after();
@@ -451,6 +478,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
         if (lane == 0) arrive_empty(0);
         continue;
       }
+      first_residual();
     }
     const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
     const int m0 = tc.mb * 128;
@@ -472,7 +500,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
     // instantiation.
     constexpr bool has_bias = HAS_BIAS;
     uint4 res_cur[4];
-    if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
+    if constexpr (EPI == SPG_EPI_ADD && !kResTma) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
 
     if (tc.split < 0) {
       if (!wait_serving(&acc_full[0], it & 1, ctl, kErrWaitAccFull, svc)) break;
@@ -522,7 +550,32 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
       } else {
         const float bias_c = has_bias ? load_bias(p, n_acc0 + 32 * c + lane) : 0.f;
         uint4 res_next[4];
-        if constexpr (EPI == SPG_EPI_ADD) {
+        if constexpr (kResTma) {
+          // This chunk's residual block (serving svc() while it lands), then
+          // the next one into the other buffer once that buffer's store has
+          // been read.
+          if (!wait_serving(&res_bars[e * 2 + (chunk_ctr & 1)], uint32_t(chunk_ctr >> 1) & 1u,
+                            ctl, kErrWaitFull, svc)) {
+            aborted = true;
+            break;
+          }
+          res_inflight = -1;
+          if (c + 1 < kOutChunks) {
+            if (lane == 0) {
+              bulk_wait_read<0>();
+              uint64_t* bar = &res_bars[e * 2 + ((chunk_ctr + 1) & 1)];
+              mbar_arrive_expect_tx(bar, kBufBytes);
+              tma_load_3d(stage0 + ((chunk_ctr + 1) & 1) * kBufBytes, tmR, bar,
+                          n_acc0 + 32 * (c + 1), m0 + q * 32, tc.b);
+            }
+            res_inflight = chunk_ctr + 1;
+            __syncwarp();
+          }
+          const uint8_t* rbuf = stage0 + (chunk_ctr & 1) * kBufBytes + lane * 64;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            res_cur[g] = *reinterpret_cast<const uint4*>(rbuf + ((g ^ ((lane >> 1) & 3)) * 16));
+        } else if constexpr (EPI == SPG_EPI_ADD) {
           if (c + 1 < kOutChunks) load_residual_chunk(p, m, n_acc0 + 32 * (c + 1), row_ok, res_next);
         }
 #pragma unroll
@@ -542,12 +595,16 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
               o[g * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xFFFF0000u);
             }
           }
+          if constexpr (!kResTma) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) res_cur[g] = res_next[g];
+            for (int g = 0; g < 4; ++g) res_cur[g] = res_next[g];
+          }
         }
       }
       uint8_t* sbuf = stage0 + (chunk_ctr & 1) * kBufBytes;
-      if (lane == 0) bulk_wait_read<1>();
+      if constexpr (!kResTma) {
+        if (lane == 0) bulk_wait_read<1>();
+      }
       __syncwarp();
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
@@ -568,6 +625,18 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
         bulk_commit();
       }
     }
+  }
+  if constexpr (kResTma) {
+    // No residual copy may still be writing the staging buffers at exit.
+    if (res_inflight >= 0 && lane == 0)
+      mbar_wait_drain(&res_bars[e * 2 + (res_inflight & 1)], uint32_t(res_inflight >> 1) & 1u,
+                      p.drain_ns, p.err);
+  }
+  if constexpr (kResTma) {
+    // No residual copy may still be writing the staging buffers at exit.
+    if (res_inflight >= 0 && lane == 0)
+      mbar_wait_drain(&res_bars[e * 2 + (res_inflight & 1)], uint32_t(res_inflight >> 1) & 1u,
+                      p.drain_ns, p.err);
   }
   if (lane == 0) bulk_wait<0>();
   __syncwarp();

@@ -53,7 +53,7 @@ struct Nvfp4StCfg {
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
 
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert((4 * STAGES + 5 + 2 + kEpiWarps) * 8 + 32 <= kBarBytes, "barrier area too small");
+  static_assert((4 * STAGES + 5 + 2 + 3 * kEpiWarps) * 8 + 16 <= kBarBytes, "barrier area too small");
   static_assert(STAGES * kStageBytes / kEpiWarps >= 3 * 4096, "K-split scratch too small");
   __host__ __device__ static constexpr uint32_t idesc() { return Base::idesc(); }
 };
@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmY,
                              const __grid_constant__ CUtensorMap tmSFA,
-                             const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+                             const __grid_constant__ CUtensorMap tmSFB,
+                             const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
   using Cfg = Nvfp4StCfg<EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -138,7 +139,8 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* drain = acc_empty + 1;
   uint64_t* split_bars = drain + 1;
   uint64_t* copy_bars = split_bars + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(copy_bars + Cfg::kEpiWarps);
+  uint64_t* res_bars = copy_bars + Cfg::kEpiWarps;  // linear_add residual: 2 per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(res_bars + 2 * Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* split_flag = abort_flag + 1;
 
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     mbar_init(&split_bars[0], Cfg::kEpiWarps);
     mbar_init(&split_bars[1], 1);
     for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&copy_bars[w], 1);
+    for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     prefetch_tmap(&tmY);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
+    if (EPI == SPG_EPI_ADD) prefetch_tmap(&tmR);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
@@ -301,16 +305,16 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     svc.sf_cols_per_stage = uint32_t(Cfg::kSfColsPerStage);
     svc.q = warp & 3;
     svc.lane = lane;
-    epilogue_loop_regdrain<EPI, kScaleScalar, HAS_BIAS>(
-        p, &tmY, tmem_base, acc_full,
-        [&](int) { mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0)); }, epi, pair,
-        num_pairs,
-        [&](int item) {
-          WorkItem w = work_item(item, p, Cfg::kBN);
-          w.mb = w.mb * 2 + int(rank);
-          return w;
-        },
-        ctl, int(rank), split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes, svc);
+    auto arrive_fn = [&](int) { mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0)); };
+    auto item_fn = [&](int item) {
+      WorkItem w = work_item(item, p, Cfg::kBN);
+      w.mb = w.mb * 2 + int(rank);
+      return w;
+    };
+    epilogue_loop_regdrain<EPI, kScaleScalar, HAS_BIAS, decltype(item_fn), decltype(arrive_fn),
+                           ScaleService<STAGES>, true>(
+        p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, num_pairs, item_fn, ctl, int(rank),
+        split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes, svc, &tmR, res_bars);
   }
 
   tc_fence_before();

@@ -59,6 +59,12 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
     if (!make_tmap_2d_u32(&maps.sfa, sfA, 128, tiles_a, 512, 128, 4) ||
         !make_tmap_2d_u32(&maps.sfb, sfW, 128, tiles_b, 512, 128, 4))
       return SPG_ERR_CUDA;
+    if (epilogue == SPG_EPI_ADD) {
+      if (!make_tmap_3d(&maps.r, residual, true, N, T, 1, N * 2, N * 2 * T, 32, 32, 64))
+        return SPG_ERR_CUDA;
+    } else {
+      maps.r = maps.y;
+    }
   }
   GemmParams p;
   fill_common_params(p, r, T, N, kh, K, n_out, 1);

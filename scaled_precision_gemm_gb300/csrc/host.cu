@@ -207,13 +207,11 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     r.block_k = 256;
     r.stages = 5;
     r.acc_buffers = one_cta ? 2 : 1;
-    // Pair tile: scales copied into TMEM by the tensor core (variant 0,
-    // SPG_FORCE_VARIANT=2sm_cp) or stored by the epilogue warps (variant 3,
-    // 2sm_st).  Measured on GB300: the warp stores free the tensor pipe
-    // (+10% for linear and SwiGLU), but the linear_add epilogue, whose
-    // residual loads keep the warps busy longer, then delays the scales.
-    const bool st_scales = forced_name ? !std::strcmp(forced_name, "2sm_st")
-                                       : epilogue != SPG_EPI_ADD;
+    // Pair tile: scales stored into TMEM by the epilogue warps (variant 3,
+    // SPG_FORCE_VARIANT=2sm_st, the default: measured on GB300 it frees the
+    // tensor pipe for +5-12% over the copies) or copied by the tensor core
+    // (variant 0, 2sm_cp).
+    const bool st_scales = forced_name ? std::strcmp(forced_name, "2sm_cp") != 0 : true;
     r.variant = one_cta ? 2 : (st_scales ? 3 : 0);
   } else {
     // Pair tiles first (widths 256/192/160/128), then one-CTA tiles.  The
