@@ -367,7 +367,8 @@ struct NoService {
 };
 
 // Bounded wait for phase `parity` of `bar` that keeps calling svc() while it
-// waits.  The warp polls through lane 0, so every decision is warp-uniform.
+// waits.  The warp polls through lane 0, so every decision is warp-uniform;
+// once the phase is complete every lane acquires it.
 template <typename Svc>
 __device__ __forceinline__ bool wait_serving(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
                                              unsigned int code, Svc& svc) {
@@ -392,7 +393,14 @@ __device__ __forceinline__ bool wait_serving(uint64_t* bar, uint32_t parity, con
         }
       }
       st = __shfl_sync(0xffffffffu, st, 0);
-      if (st == 1) return true;
+      if (st == 1) {
+        // Lane 0's test was the acquire; the shuffle orders nothing, so every
+        // lane acquires the completed phase itself before it reads what the
+        // phase guards.
+        (void)mbar_test_wait(smem_u32(bar), parity);
+        __syncwarp();
+        return true;
+      }
       if (st == 2) return false;
       svc();
     }

@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(192, 1)
         const int width = w.width;
         // The instruction descriptor's N field carries the item's width.
         const uint32_t idesc = (kIdesc & ~(0x3Fu << 17)) | (uint32_t(width >> 3) << 17);
-        if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
+        // The peer CTA's epilogue warps release this barrier across the pair.
+        if (!mbar_wait_cluster(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {

@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
       bool ok = true;
       for (int item = pair; ok && item < p.total_items; item += num_pairs, ++it) {
         const WorkItem w = work_item(item, p, Cfg::kBN);
-        if (!mbar_wait(acc_empty, (it & 1) ^ 1u, ctl, kErrWaitAccEmpty)) break;
+        // The peer CTA's epilogue warps release this barrier across the pair.
+        if (!mbar_wait_cluster(acc_empty, (it & 1) ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull)) {

@@ -22,8 +22,9 @@
 //
 // Barriers (per stage s): full[s] (leader; both CTAs' A/B codes), sf_full[s]
 // (each CTA; its scale tiles), sf_ready[s] (leader; 8 arrivals: the 4 scale
-// writers of each CTA), empty[s] (both CTAs; multicast commit after the
-// stage's MMAs).  Every wait is bounded.
+// writers of each CTA; the MMA issuer waits with a cluster-scope acquire),
+// empty[s] (both CTAs; multicast commit after the stage's MMAs).  Every wait
+// is bounded.
 #pragma once
 
 #include "gemm_epilogue.cuh"
@@ -89,8 +90,10 @@ struct ScaleService {
   static constexpr bool kActive = true;
   int next;           // next stage to serve (this warp's parity)
   int end;            // stages of this CTA pair
-  uint64_t* sf_full;  // this CTA's scale-tile barriers
-  uint32_t sf_ready_leader;
+  uint64_t* sf_full;         // this CTA's scale-tile barriers
+  uint64_t* sf_ready;        // the leader's stage barriers (local in the leader)
+  uint32_t sf_ready_leader;  // the same, as cluster addresses (peer CTA)
+  bool leader;
   uint8_t* ring;
   int stage_bytes, sf_offset;  // ring stride; scale tiles' offset in a stage
   uint32_t tmem_base, sf_col_base, sf_cols_per_stage;
@@ -103,13 +106,26 @@ struct ScaleService {
       const int ready = __shfl_sync(
           0xffffffffu, lane == 0 ? (mbar_test_wait(smem_u32(&sf_full[s]), par) ? 1 : 0) : 0, 0);
       if (!ready) return;
+      // Every lane acquires the completed phase before it reads the tiles.
+      (void)mbar_test_wait(smem_u32(&sf_full[s]), par);
+      __syncwarp();
       const uint8_t* ssfa = ring + s * stage_bytes + sf_offset;
       store_stage_scales(tmem_base, sf_col_base + uint32_t(s) * sf_cols_per_stage, ssfa,
                          ssfa + 2048, q, lane);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(sf_ready_leader + uint32_t(s * 8));
+      // Signalled by lane 31: a release waits for the arriving thread's own
+      // outstanding memory operations, and lane 0 issues the warp's TMA
+      // stores and residual loads (a release from it measured ~1 us per
+      // stage).  The other lanes' TMEM stores are ordered before it by
+      // their tcgen05.fence::before_thread_sync and the __syncwarp.
+      if (lane == 31) {
+        if (leader)
+          mbar_arrive(&sf_ready[s]);
+        else
+          mbar_arrive_cluster(sf_ready_leader + uint32_t(s * 8));
+      }
       next += 2;
     }
   }
@@ -215,18 +231,20 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
           uint8_t* sb = sa + Cfg::kABytes;
           uint8_t* ssfa = sb + Cfg::kBBytes;
           uint8_t* ssfb = ssfa + Cfg::kSfaBytes;
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (Cfg::kABytes + Cfg::kBBytes));
-          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-          const int kx = kb * Cfg::kBKBytes;
-          tma_load_3d_pair(sa, &tmA, bar, kx, m0, 0);
-          tma_load_3d_pair(sb, &tmB, bar, kx, n0, 0);
-          // Scale tiles: 4 consecutive 512-byte tiles per 128-row block, on
-          // this CTA's own barrier.
+          // Scale tiles first (4 consecutive 512-byte tiles per 128-row block,
+          // on this CTA's own barrier): they are 6 KB against 64 KB of codes,
+          // so their stores into TMEM overlap the codes' arrival instead of
+          // following it.
           mbar_arrive_expect_tx(&sf_full[s], Cfg::kSfaBytes + Cfg::kSfbBytes);
           const int k_tile = kb * 4;
           tma_load_3d(ssfa, &tmSFA, &sf_full[s], 0, a_rb_sf * int(tpr) + k_tile, 0);
           tma_load_3d(ssfb, &tmSFB, &sf_full[s], 0, b_rb0 * int(tpr) + k_tile, 0);
           tma_load_3d(ssfb + 2048, &tmSFB, &sf_full[s], 0, b_rb1 * int(tpr) + k_tile, 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (Cfg::kABytes + Cfg::kBBytes));
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          const int kx = kb * Cfg::kBKBytes;
+          tma_load_3d_pair(sa, &tmA, bar, kx, m0, 0);
+          tma_load_3d_pair(sb, &tmB, bar, kx, n0, 0);
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -254,11 +272,12 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
       bool ok = true;
       for (int item = pair; ok && item < p.total_items; item += num_pairs, ++it) {
         const WorkItem w = work_item(item, p, Cfg::kBN);
-        if (!mbar_wait(acc_empty, (it & 1) ^ 1u, ctl, kErrWaitAccEmpty)) break;
+        // The peer CTA's epilogue warps release this barrier across the pair.
+        if (!mbar_wait_cluster(acc_empty, (it & 1) ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull) ||
-              !mbar_wait(&sf_ready[s], ph, ctl, kErrWaitFull)) {
+              !mbar_wait_cluster(&sf_ready[s], ph, ctl, kErrWaitFull)) {
             ok = false;
             break;
           }
@@ -296,7 +315,9 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     svc.next = (warp - 2) >> 2;
     svc.end = my_stages;
     svc.sf_full = sf_full;
+    svc.sf_ready = sf_ready;
     svc.sf_ready_leader = mapa_shared(smem_u32(sf_ready), 0);
+    svc.leader = rank == 0;
     svc.ring = ring;
     svc.stage_bytes = Cfg::kStageBytes;
     svc.sf_offset = Cfg::kABytes + Cfg::kBBytes;

@@ -53,6 +53,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return done != 0;
 }
 
+// try_wait with acquire at cluster scope: for barriers that receive
+// arrivals released by the other CTA of the pair.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Non-blocking test of phase `parity` (mbarrier.try_wait may suspend the
 // thread for a while when the phase is incomplete; test_wait never does).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
@@ -101,6 +115,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   return mbar_wait_slow(a, parity, ctl.timeout_ns, ctl.err, ctl.abort_flag, code);
+}
+
+// Bounded wait like mbar_wait whose successful test is an acquire at cluster
+// scope (the phase's last arrival may be a release by the other CTA of the
+// pair).
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar_addr, uint32_t parity,
+                                                          uint64_t timeout_ns, unsigned int* err,
+                                                          volatile int* abort_flag,
+                                                          unsigned int code) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar_addr, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns || i > (1u << 30)) {
+        *abort_flag = 1;
+        atomicCAS(err, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const WaitCtl& ctl, unsigned int code) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  return mbar_wait_cluster_slow(a, parity, ctl.timeout_ns, ctl.err, ctl.abort_flag, code);
 }
 
 // ----------------------------------------------------------------------- TMA

@@ -288,3 +288,31 @@ def test_tensor_workload_shapes_sampled(layout, M, N, K, batch):
     rows = _sample_rows(M, n=4)
     ref = oracle.fp8_tensor_gemm(layout, A, sA, B, sB, M, N, K, batch=batch, rows=rows)
     assert_within_tol(y[:, rows, :], ref, f"tensor {layout} {M}x{N}x{K}x{batch}")
+
+
+@pytest.mark.parametrize("epi", ["add", "swiglu"])
+def test_nvfp4_pair_kernels_agree_and_repeat(epi, monkeypatch):
+    """The two NVFP4 pair kernels differ only in how the scale factors reach
+    TMEM, so their outputs must agree bit for bit -- on every one of many
+    repeated launches (a missed ordering between the scale stores, the
+    residual copies or the accumulator hand-over shows up as a run that
+    differs).  Shapes with short K give frequent tile changes."""
+    T, N, K = 4096, 5120, 5120
+    A, sfA, gA, W, sfW, gW = nvfp4_inputs(T, N, K, seed=91)
+    res = normal_bf16((T, N), seed=92) if epi == "add" else None
+    dA, dW = cuda(A), cuda(W)
+    dsA, dsW = cuda(sf_rowmajor_to_blocked(sfA, T, K)), cuda(sf_rowmajor_to_blocked(sfW, N, K))
+    tgA = torch.tensor([gA], dtype=torch.float32, device=DEV)
+    tgW = torch.tensor([gW], dtype=torch.float32, device=DEV)
+    dr = None if res is None else cuda_bf16(res)
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_cp")
+    base = spg.nvfp4_gemm(dA, dsA, tgA, dW, dsW, tgW, residual=dr, epilogue=epi).clone()
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
+    for _ in range(12):
+        y = spg.nvfp4_gemm(dA, dsA, tgA, dW, dsW, tgW, residual=dr, epilogue=epi)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), base.view(torch.int16))
+    assert spg.last_device_error() == 0
+    rows = _sample_rows(T, n=4)
+    ref = oracle.nvfp4_gemm(A, sfA, gA, W, sfW, gW, res, epi, rows=rows)
+    assert_within_tol(to_f64(base[torch.from_numpy(rows).to(DEV)]), ref, f"nvfp4 {epi} repeat")
