@@ -115,12 +115,13 @@ struct ScaleService {
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      // Signalled by lane 31: a release waits for the arriving thread's own
-      // outstanding memory operations, and lane 0 issues the warp's TMA
-      // stores and residual loads (a release from it measured ~1 us per
-      // stage).  The other lanes' TMEM stores are ordered before it by
-      // their tcgen05.fence::before_thread_sync and the __syncwarp.
-      if (lane == 31) {
+      // Release (CTA scope in the leader, cluster scope from the peer), so
+      // the leader's cluster-scope acquire orders these TMEM stores before
+      // its MMAs.  Measured on GB300: a relaxed arrival instead runs the
+      // kernel at ~5.4 PFLOP/s but lets MMAs read stale scales (outputs
+      // differed in up to half of repeated launches), while each
+      // cluster-scope release holds its warp ~1 us.
+      if (lane == 0) {
         if (leader)
           mbar_arrive(&sf_ready[s]);
         else
