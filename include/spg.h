@@ -117,8 +117,7 @@ SPG_API spg_status spg_last_device_error(spg_stream_t stream);
  * that ran out (0 if none) in *code: 0x101 ring slot free, 0x102 ring slot
  * full, 0x103 accumulator free, 0x104 accumulator full, 0x105 drain,
  * 0x106 injected stall (spg_debug_inject_stall), 0x107 a K-split arrival
- * counter could not be updated (bounded compare-and-swap loop), 0x108 the
- * epilogue warps of a K-split piece did not meet. */
+ * counter could not be updated (bounded compare-and-swap loop). */
 SPG_API spg_status spg_last_device_error_code(spg_stream_t stream, uint32_t* code);
 
 /* ---------------------------------------------------------------------

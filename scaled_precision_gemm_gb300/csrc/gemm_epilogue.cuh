@@ -34,111 +34,74 @@ __device__ __forceinline__ void load_residual_chunk(const GemmParams& p, int m, 
   }
 }
 
-// Per-warp resources of the K-split reduction: a scratch area in the
-// shared-memory operand ring (idle by then: a K-split piece is always the
-// last item of its CTA pair, so every stage has been consumed once its
-// accumulator is full) and one mbarrier for the bulk copies into it.
-struct SplitScratch {
-  uint8_t* buf;        // 1024-byte aligned
-  int bytes;           // at least 4096
-  uint64_t* bar;       // this warp's copy barrier (arrival count 1)
-  uint32_t* phase;     // its parity, kept by the caller across items
-};
-
-// K-split piece of a tile (two-SM kernels).  The calling warp owns TMEM
-// lane quarter q = row / 32 (t_row addresses column 0 of the tile's
-// accumulator in that quarter) and accumulator columns [c0, c0 + ncols), a
-// multiple of 32.  rows_live: some row of the quarter is inside the output.
-//  1. The piece's partial sums go to its workspace slice.
-//  2. Every epilogue warp arrives on split_bars[0] once its writes are
-//     fenced; the first epilogue thread then counts the CTA's arrival on the
-//     tile's counter and posts the outcome through split_bars[1].
-//  3. In the CTA of the last piece to arrive, every warp bulk-copies the
-//     other pieces' 4 KB blocks of its rows into its scratch, adds all
-//     pieces in split order (its own from TMEM, so the total does not depend
-//     on the arrival order) and writes the total back to TMEM, where the
-//     ordinary epilogue picks it up.
-// Returns 1 if this CTA holds the total, 0 if not, -1 if a wait ran out.
-// Nothing waits for another CTA, so pieces never rely on running at the same
-// time; the waits inside the CTA are bounded like every other.  `phase`
-// counts the K-split pieces this CTA has processed (mod 2).  At most 4
-// pieces per tile.
-template <int BN>
-__device__ __forceinline__ int split_piece_reduce(const GemmParams& p, uint32_t t_row,
-                                                  const WorkItem& tc, int rank, int row, int c0,
-                                                  int ncols, bool rows_live, uint64_t* split_bars,
-                                                  int* flag, uint32_t phase,
-                                                  const SplitScratch& scr, const WaitCtl& ctl) {
+// K-split piece of a tile (two-SM kernels), one epilogue warp's share.  The
+// warp owns TMEM lane quarter q (rows q*32 .. q*32+31 of the CTA's 128; t_row
+// addresses column 0 of the tile's accumulator in that quarter) and
+// accumulator columns [c0, c0 + ncols), which its epilogue processes in
+// chunks of CW columns.
+//  1. It writes its partial sums of those columns to the piece's slice.
+//  2. After one fence, lane i counts the piece's arrival on the counter of
+//     chunk i (all chunks at once, one round trip).
+//  3. For every chunk where this piece arrived last, it adds all pieces in
+//     split order (its own from TMEM, so the total does not depend on the
+//     arrival order) and writes the total back to TMEM.
+// Returns the mask of chunks whose total this warp now holds (bit i: chunk
+// i); the caller runs the epilogue on exactly those.  The chunks of a tile
+// finish in whichever pieces arrive last for them, so the reduction and the
+// epilogue spread over the pieces; nothing waits for another CTA or warp.
+// rows_live == false (every row of the quarter past the output): only the
+// arrivals, so the counters still return to zero.  G: float4 groups of a
+// 32-column block loaded at once per other piece (8 or 4, trading registers
+// against round trips).  At most 4 pieces per tile.
+template <int BN, int CW, int G>
+__device__ __forceinline__ uint32_t split_piece_finish(const GemmParams& p, uint32_t t_row,
+                                                       const WorkItem& tc, int rank, int q,
+                                                       int c0, int ncols, bool rows_live) {
+  static_assert(CW == 32 || CW == 64, "epilogue chunks are 32 or 64 columns");
+  static_assert(G == 4 || G == 8, "a 32-column block is 8 float4 groups");
   const int lane = threadIdx.x & 31;
-  const int q = row >> 5;
   const bool have_k = tc.kb_end > tc.kb_begin;
-  if (rows_live) {
-    float4* own = split_slice(p, tc.tail, tc.split, rank, BN);
+  float4* own = split_slice(p, tc.tail, tc.split, rank, BN);
 #pragma unroll 1
-    for (int c = c0; c < c0 + ncols; c += 32) {
-      uint32_t r[32];
-      if (have_k) {
-        tmem_ld_32x32b_x32(t_row + c, r);
-        tmem_wait_ld();
-      } else {
+  for (int c = c0; rows_live && c < c0 + ncols; c += 32) {
+    uint32_t r[32];
+    if (have_k) {
+      tmem_ld_32x32b_x32(t_row + c, r);
+      tmem_wait_ld();
+    } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      }
-      float4* blk = own + split_block_index(c >> 5, q) + lane;
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        __stcg(blk + g * 32,
-               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
     }
+    float4* blk = own + split_block_index(c >> 5, q) + lane;
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      __stcg(blk + g * 32,
+             make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                         __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
   }
   __threadfence();
   __syncwarp();
-  if (lane == 0) mbar_arrive(&split_bars[0]);
-  if (threadIdx.x == 64) {  // first epilogue thread
-    int outcome = -1;
-    if (mbar_wait(&split_bars[0], phase, ctl, kErrWaitSplit)) {
-      const int before = split_arrive(p, tc.tail, rank);
-      __threadfence();
-      outcome = before == p.split_k - 1 ? 1 : 0;
-    }
-    *reinterpret_cast<volatile int*>(flag) = outcome;
-    mbar_arrive(&split_bars[1]);
+  const int nch = ncols / CW;
+  int last = 0;
+  if (lane < nch) {
+    const int before =
+        split_arrive(p, split_counter_index(tc.tail, rank, q, (c0 + lane * CW) / CW, BN, CW));
+    last = before == p.split_k - 1 ? 1 : 0;
+    __threadfence();
   }
-  if (!mbar_wait(&split_bars[1], phase, ctl, kErrWaitSplit)) return -1;
-  const int outcome = *reinterpret_cast<volatile int*>(flag);
-  if (outcome <= 0 || !rows_live) return outcome;
+  // Warps with no live row still count their arrivals (so every counter
+  // returns to zero) but finish nothing.
+  const uint32_t mask = rows_live ? __ballot_sync(0xffffffffu, last) : 0u;
+  if (mask == 0u) return 0u;
+  __syncwarp();
   __threadfence();
-
   const int own_s = tc.split;
-  const int others = p.split_k - 1;
-  const int nbuf = scr.bytes >> 12;
-  int per_round = nbuf / others;  // chunks whose other blocks fit the scratch at once
-  if (per_round < 1) per_round = 1;
-  const int nchunks = ncols >> 5;
 #pragma unroll 1
-  for (int ch0 = 0; ch0 < nchunks; ch0 += per_round) {
-    const int nch = nchunks - ch0 < per_round ? nchunks - ch0 : per_round;
-    if (lane == 0) {
-      fence_proxy_async_global();
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(scr.bar, uint32_t(nch * others) * 4096u);
-      for (int i = 0; i < nch; ++i) {
-        const int chunk = (c0 >> 5) + ch0 + i;
-        for (int k = 0; k < others; ++k) {
-          const int s2 = k + (k >= own_s ? 1 : 0);
-          const float4* src =
-              split_slice(p, tc.tail, s2, rank, BN) + split_block_index(chunk, q);
-          bulk_load(scr.buf + (i * others + k) * 4096, src, 4096u, scr.bar);
-        }
-      }
-    }
-    __syncwarp();
-    if (!mbar_wait(scr.bar, *scr.phase, ctl, kErrWaitSplit)) return -1;
-    *scr.phase ^= 1u;
+  for (int i = 0; i < nch; ++i) {
+    if (!((mask >> i) & 1u)) continue;
 #pragma unroll 1
-    for (int i = 0; i < nch; ++i) {
-      const int c = c0 + (ch0 + i) * 32;
+    for (int sb = 0; sb < CW; sb += 32) {
+      const int c = c0 + i * CW + sb;
       uint32_t r[32];
       if (have_k) {
         tmem_ld_32x32b_x32(t_row + c, r);
@@ -147,51 +110,67 @@ __device__ __forceinline__ int split_piece_reduce(const GemmParams& p, uint32_t 
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = 0u;
       }
-      const float4* blk = reinterpret_cast<const float4*>(scr.buf + i * others * 4096) + lane;
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 mine = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                        __uint_as_float(r[4 * g + 2]),
-                                        __uint_as_float(r[4 * g + 3]));
-        for (int s2 = 0; s2 < p.split_k; ++s2) {
-          const float4 x =
-              s2 == own_s ? mine : blk[(s2 - (s2 > own_s ? 1 : 0)) * 256 + g * 32];
-          t.x += x.x;
-          t.y += x.y;
-          t.z += x.z;
-          t.w += x.w;
+      for (int g0 = 0; g0 < 8; g0 += G) {
+        // The other pieces: slot k holds piece k, or k + 1 past this one.
+        float4 part[3][G];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int s2 = k + (k >= own_s ? 1 : 0);
+          if (s2 < p.split_k) {
+            const float4* src =
+                split_slice(p, tc.tail, s2, rank, BN) + split_block_index(c >> 5, q) + lane;
+#pragma unroll
+            for (int g = 0; g < G; ++g) part[k][g] = __ldcg(src + (g0 + g) * 32);
+          } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) part[k][g] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-        r[4 * g] = __float_as_uint(t.x);
-        r[4 * g + 1] = __float_as_uint(t.y);
-        r[4 * g + 2] = __float_as_uint(t.z);
-        r[4 * g + 3] = __float_as_uint(t.w);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int j = 4 * (g0 + g);
+          const float4 mine = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            if (k == own_s) {
+              t.x += mine.x; t.y += mine.y; t.z += mine.z; t.w += mine.w;
+            }
+            if (k + (k >= own_s ? 1 : 0) < p.split_k) {
+              t.x += part[k][g].x; t.y += part[k][g].y; t.z += part[k][g].z; t.w += part[k][g].w;
+            }
+          }
+          if (own_s == 3) {
+            t.x += mine.x; t.y += mine.y; t.z += mine.z; t.w += mine.w;
+          }
+          r[j] = __float_as_uint(t.x);
+          r[j + 1] = __float_as_uint(t.y);
+          r[j + 2] = __float_as_uint(t.z);
+          r[j + 3] = __float_as_uint(t.w);
+        }
       }
       tmem_st_32x32b_x32(t_row + c, r);
     }
-    __syncwarp();
   }
   tmem_wait_st();
-  return 1;
+  return mask;
 }
 
 // ItemFn(item) -> WorkItem with mb already offset for this CTA's rows (a
 // whole tile has n_off = 0, width = BN); the loop runs over items
 // [item_begin, item_end) with stride item_step.  ArriveEmpty(buf) releases
 // accumulator buffer `buf` to the MMA issuer.  K-split pieces (two-SM
-// kernels only) go through split_piece_reduce first; cta_rank, split_bars
-// (two mbarriers: arrival count 4 and 1), split_flag (one shared int),
-// copy_bars (one mbarrier of count 1 per epilogue warp) and the operand ring
-// (ring, ring_bytes: the warps' scratch) serve them.
+// kernels only, cta_rank: this CTA's rank in the pair) go through
+// split_piece_finish first and then run the epilogue on the chunks whose
+// total they hold.
 template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtensorMap* tmY,
                                               uint32_t tmem_base, uint64_t* acc_full,
                                               ArriveEmpty arrive_empty, uint8_t* epi_smem,
                                               int item_begin, int item_end, int item_step,
-                                              ItemFn item_fn, const WaitCtl& ctl, int cta_rank,
-                                              uint64_t* split_bars, int* split_flag,
-                                              uint64_t* copy_bars, uint8_t* ring,
-                                              int ring_bytes) {
+                                              ItemFn item_fn, const WaitCtl& ctl, int cta_rank) {
   using E = EpilogueCfg<EPI, SCALE, BN>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -200,9 +179,6 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
   uint8_t* stage0 = epi_smem + (e * 2) * E::kBufBytes;
   int it = 0;
   int chunk_ctr = 0;
-  uint32_t split_phase = 0, copy_phase = 0;
-  const int scr_bytes = (ring_bytes / 4) & ~4095;
-  const SplitScratch scr{ring + e * scr_bytes, scr_bytes, copy_bars + e, &copy_phase};
   float scalar = 1.f;
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
 
@@ -211,21 +187,22 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
     const uint32_t acc_ph = (it >> 1) & 1;
     const WorkItem tc = item_fn(item);
     const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+    // Chunks this warp finishes: all of them, or those whose K-split total
+    // it holds.
+    uint32_t own_mask = 0xffffffffu;
     if (tc.split >= 0) {
       if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
       tc_fence_after();
-      const int outcome = split_piece_reduce<BN>(
-          p, t_row, tc, cta_rank, q * 32 + lane, 0, tc.width, tc.mb * 128 + q * 32 < p.M,
-          split_bars, split_flag, split_phase, scr, ctl);
-      split_phase ^= 1u;
-      if (outcome < 0) break;
-      if (outcome == 0) {
+      own_mask = split_piece_finish<BN, E::kAccColsPerChunk, 8>(
+          p, t_row, tc, cta_rank, q, 0, tc.width, tc.mb * 128 + q * 32 < p.M);
+      if (own_mask == 0u) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_empty(buf);
         continue;
       }
     }
+    const bool split_item = tc.split >= 0;
     // After a K-split reduction TMEM holds the total of all pieces.
     const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
     const int m0 = tc.mb * 128;
@@ -233,6 +210,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
     const int nch = tc.width / E::kAccColsPerChunk;
     const int m = m0 + q * 32 + lane;
     const bool row_ok = m < p.M;
+    own_mask &= nch >= 32 ? 0xffffffffu : ((1u << nch) - 1u);
+    const int last_c = 31 - __clz(own_mask);  // the accumulator goes back after this chunk
 
     // Epilogue operands, requested before the accumulator is ready.
     float row_s = scalar;
@@ -253,7 +232,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         biasr[j] = 32 * j < tc.width ? load_bias(p, n0 + 32 * j + lane) : 0.f;
     }
     uint4 res_cur[4];
-    if constexpr (EPI == SPG_EPI_ADD) load_residual_chunk(p, m, n0, row_ok, res_cur);
+    if constexpr (EPI == SPG_EPI_ADD) {
+      if (!split_item) load_residual_chunk(p, m, n0, row_ok, res_cur);
+    }
 
     if (tc.split < 0) {
       if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
@@ -263,7 +244,12 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
 #pragma unroll
     for (int c = 0; c < E::kChunks; ++c) {
       if (c >= nch) break;
+      if (!((own_mask >> c) & 1u)) continue;
       const int acc_c0 = c * E::kAccColsPerChunk;
+      if constexpr (EPI == SPG_EPI_ADD) {
+        // A K-split piece finishes scattered chunks: load each one's residual.
+        if (split_item) load_residual_chunk(p, m, n0 + acc_c0, row_ok, res_cur);
+      }
       uint32_t raw[E::kAccColsPerChunk];
       if (have_k) {
         tmem_ld_32x32b_x32(t_row + acc_c0, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
@@ -275,10 +261,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       }
       uint4 res_next[4];
       if constexpr (EPI == SPG_EPI_ADD) {
-        if (c + 1 < nch) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
+        if (!split_item && c + 1 < nch) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
       }
       if (have_k) tmem_wait_ld();
-      if (c == nch - 1) {
+      if (c == last_c) {
         // Every column of this accumulator buffer has been read: hand it back.
         tc_fence_before();
         __syncwarp();
@@ -428,9 +414,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
                                                        ArriveEmpty arrive_empty, uint8_t* epi_smem,
                                                        int item_begin, int item_step, ItemFn item_fn,
                                                        const WaitCtl& ctl, int cta_rank,
-                                                       uint64_t* split_bars, int* split_flag,
-                                                       uint64_t* copy_bars, uint8_t* ring,
-                                                       int ring_bytes, Svc svc = Svc(),
+                                                       Svc svc = Svc(),
                                                        const CUtensorMap* tmR = nullptr,
                                                        uint64_t* res_bars = nullptr) {
   constexpr int kCols = 128;                 // accumulator columns per warp
@@ -445,9 +429,6 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
   uint8_t* stage0 = epi_smem + (e * 2) * kBufBytes;
   int it = 0;
   int chunk_ctr = 0;
-  uint32_t split_phase = 0, copy_phase = 0;
-  const int scr_bytes = (ring_bytes / 8) & ~4095;
-  const SplitScratch scr{ring + e * scr_bytes, scr_bytes, copy_bars + e, &copy_phase};
   float scalar = 1.f;
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
   bool aborted = false;
@@ -456,8 +437,10 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
   for (int item = item_begin; item < p.total_items && !aborted; item += item_step, ++it) {
     const WorkItem tc = item_fn(item);
     // First residual block of the item, into the buffer of its first chunk
-    // (whose previous store, two chunks back, must have been read).  For a
-    // K-split piece only once it is known to hold the tile's total.
+    // (whose previous store, two chunks back, must have been read).  A
+    // K-split piece finishes scattered chunks and loads their residual
+    // directly instead.
+    const bool split_item = tc.split >= 0;
     auto first_residual = [&]() {
       if constexpr (kResTma) {
         if (lane == 0) {
@@ -471,22 +454,20 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
         __syncwarp();
       }
     };
-    if (tc.split < 0) first_residual();
-    if (tc.split >= 0) {
+    uint32_t own_mask = 0xffffffffu;  // chunks this warp finishes
+    if (!split_item) first_residual();
+    if (split_item) {
       if (!wait_serving(&acc_full[0], it & 1, ctl, kErrWaitAccFull, svc)) break;
       tc_fence_after();
-      const int outcome = split_piece_reduce<256>(
-          p, tmem_base + (uint32_t(q * 32) << 16), tc, cta_rank, q * 32 + lane, half * kCols,
-          kCols, tc.mb * 128 + q * 32 < p.M, split_bars, split_flag, split_phase, scr, ctl);
-      split_phase ^= 1u;
-      if (outcome < 0) break;
-      if (outcome == 0) {
+      own_mask = split_piece_finish<256, EPI == SPG_EPI_SWIGLU ? 64 : 32, 4>(
+          p, tmem_base + (uint32_t(q * 32) << 16), tc, cta_rank, q, half * kCols, kCols,
+          tc.mb * 128 + q * 32 < p.M);
+      if (own_mask == 0u) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_empty(0);
         continue;
       }
-      first_residual();
     }
     const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
     const int m0 = tc.mb * 128;
@@ -508,7 +489,9 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
     // instantiation.
     constexpr bool has_bias = HAS_BIAS;
     uint4 res_cur[4];
-    if constexpr (EPI == SPG_EPI_ADD && !kResTma) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
+    if constexpr (EPI == SPG_EPI_ADD && !kResTma) {
+      if (!split_item) load_residual_chunk(p, m, n_acc0, row_ok, res_cur);
+    }
 
     if (tc.split < 0) {
       if (!wait_serving(&acc_full[0], it & 1, ctl, kErrWaitAccFull, svc)) break;
@@ -530,7 +513,8 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
     if (lane == 0) arrive_empty(0);
 
 #pragma unroll
-    for (int c = 0; c < kOutChunks; ++c, ++chunk_ctr) {
+    for (int c = 0; c < kOutChunks; ++c) {
+      if (!((own_mask >> c) & 1u)) continue;
       svc();
       float o[32];
       if constexpr (EPI == SPG_EPI_SWIGLU) {
@@ -558,7 +542,9 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
       } else {
         const float bias_c = has_bias ? load_bias(p, n_acc0 + 32 * c + lane) : 0.f;
         uint4 res_next[4];
-        if constexpr (kResTma) {
+        if (EPI == SPG_EPI_ADD && split_item) {
+          load_residual_chunk(p, m, n_acc0 + 32 * c, row_ok, res_cur);
+        } else if constexpr (kResTma) {
           // This chunk's residual block (serving svc() while it lands), then
           // the next one into the other buffer once that buffer's store has
           // been read.
@@ -610,7 +596,9 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
         }
       }
       uint8_t* sbuf = stage0 + (chunk_ctr & 1) * kBufBytes;
-      if constexpr (!kResTma) {
+      // The buffer's store of two chunks back must have been read (the TMA
+      // residual path has waited for it before loading the residual here).
+      if (!kResTma || split_item) {
         if (lane == 0) bulk_wait_read<1>();
       }
       __syncwarp();
@@ -632,6 +620,7 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
         if (out_y < p.M && out_x < p.n_out) tma_store_3d(tmY, sbuf, out_x, out_y, tc.b);
         bulk_commit();
       }
+      ++chunk_ctr;
     }
   }
   if constexpr (kResTma) {

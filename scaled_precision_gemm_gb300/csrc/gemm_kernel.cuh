@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(192, 1)
           const TileCoord tc = tile_coord(tile, p);
           return WorkItem{tc.b, tc.mb, tc.nb, 0, BN, 0, p.num_k_blocks, -1, 0};
         },
-        ctl, 0, nullptr, nullptr, nullptr, nullptr, 0);
+        ctl, 0);
   }
 
   tc_fence_before();

@@ -20,7 +20,6 @@ enum : unsigned int {
   kErrDrain = 0x105,
   kErrInjectedStall = 0x106,
   kErrSplitCounter = 0x107,
-  kErrWaitSplit = 0x108,
 };
 
 struct GemmParams {
@@ -58,8 +57,9 @@ struct GemmParams {
   int total_items;
   // K-split workspace: per (tail tile, split, CTA of the pair) one 128 x BN
   // fp32 slice of partial sums, then one 64-bit arrival counter per (tail
-  // tile, CTA).  A counter holds (epoch << 32) | arrivals; a value tagged
-  // with another epoch counts as zero arrivals.
+  // tile, CTA, lane quarter, epilogue chunk).  A counter holds
+  // (epoch << 32) | arrivals; a value tagged with another epoch counts as
+  // zero arrivals.
   float* ws_partial;
   unsigned long long* ws_counter;
   uint32_t epoch;
@@ -152,12 +152,19 @@ __device__ __forceinline__ int split_block_index(int chunk, int quarter) {
   return (chunk * 4 + quarter) * 256;
 }
 
-// Record one arrival on the counter of (tail tile, CTA rank) and return how
-// many pieces arrived before (0 .. split_k - 1).  Called by one thread after
-// the CTA's partial sums are written and fenced.  The last arrival puts the
-// counter back to zero so the workspace stays clean for the next call.
-__device__ __forceinline__ int split_arrive(const GemmParams& p, int tail, int rank) {
-  unsigned long long* c = p.ws_counter + tail * 2 + rank;
+// Arrival counter of (tail tile, CTA rank, lane quarter, epilogue chunk of
+// cw columns).
+__device__ __forceinline__ int split_counter_index(int tail, int rank, int quarter, int chunk,
+                                                   int bn, int cw) {
+  return ((tail * 2 + rank) * 4 + quarter) * (bn / cw) + chunk;
+}
+
+// Record one arrival on counter `idx` and return how many pieces arrived
+// before (0 .. split_k - 1).  Called after this thread's piece of the
+// partial sums is written and fenced.  The last arrival puts the counter
+// back to zero so the workspace stays clean for the next call.
+__device__ __forceinline__ int split_arrive(const GemmParams& p, int idx) {
+  unsigned long long* c = p.ws_counter + idx;
   unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c);
   int before = -1;
   for (int i = 0; i < (1 << 20); ++i) {

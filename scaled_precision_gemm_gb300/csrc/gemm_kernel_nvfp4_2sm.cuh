@@ -45,9 +45,6 @@ struct Nvfp4PairCfg {
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
   static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
-  static_assert(2 * STAGES + 5 + 2 + kEpiWarps <= kBarBytes / 8 - 2,
-                "no room for the K-split barriers");
-  static_assert(STAGES * kStageBytes / kEpiWarps >= 3 * 4096, "K-split scratch too small");
 
   // Block-scaled descriptor: A, B = E2M1 (1), UE4M3 scales, M = 256, N = 256, K = 64.
   __host__ __device__ static constexpr uint32_t idesc() {
@@ -76,11 +73,8 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint64_t* split_bars = drain + 1;  // K-split pieces: gather (8 warps), broadcast (1)
-  uint64_t* copy_bars = split_bars + 2;  // K-split reduction: one per epilogue warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(copy_bars + Cfg::kEpiWarps);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* split_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -96,9 +90,6 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * Cfg::kEpiWarps);
     mbar_init(drain, 1);
-    mbar_init(&split_bars[0], Cfg::kEpiWarps);
-    mbar_init(&split_bars[1], 1);
-    for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&copy_bars[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -237,7 +228,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
           w.mb = w.mb * 2 + int(rank);
           return w;
         },
-        ctl, int(rank), split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes);
+        ctl, int(rank));
   }
 
   tc_fence_before();

@@ -54,8 +54,7 @@ struct Nvfp4StCfg {
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
 
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert((4 * STAGES + 5 + 2 + 3 * kEpiWarps) * 8 + 16 <= kBarBytes, "barrier area too small");
-  static_assert(STAGES * kStageBytes / kEpiWarps >= 3 * 4096, "K-split scratch too small");
+  static_assert((4 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 <= kBarBytes, "barrier area too small");
   __host__ __device__ static constexpr uint32_t idesc() { return Base::idesc(); }
 };
 
@@ -154,12 +153,9 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* acc_full = bars + 4 * STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint64_t* split_bars = drain + 1;
-  uint64_t* copy_bars = split_bars + 2;
-  uint64_t* res_bars = copy_bars + Cfg::kEpiWarps;  // linear_add residual: 2 per epilogue warp
+  uint64_t* res_bars = drain + 1;  // linear_add residual: 2 per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(res_bars + 2 * Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* split_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -177,9 +173,6 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * Cfg::kEpiWarps);
     mbar_init(drain, 1);
-    mbar_init(&split_bars[0], Cfg::kEpiWarps);
-    mbar_init(&split_bars[1], 1);
-    for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&copy_bars[w], 1);
     for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -336,7 +329,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     epilogue_loop_regdrain<EPI, kScaleScalar, HAS_BIAS, decltype(item_fn), decltype(arrive_fn),
                            ScaleService<STAGES>, true>(
         p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, num_pairs, item_fn, ctl, int(rank),
-        split_bars, split_flag, copy_bars, ring, STAGES * Cfg::kStageBytes, svc, &tmR, res_bars);
+        svc, &tmR, res_bars);
   }
 
   tc_fence_before();

@@ -253,8 +253,14 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
         }
         if (c.block_m == 256 && tail_k_ok) {
           const KSplit k = ksplit_plan(tiles, units, nkb);
-          if (k.split_k > 1 && ksplit_piece_time(k, c.block_n) + fixed < tail) {
-            tail = ksplit_piece_time(k, c.block_n) + fixed;
+          // With fewer tiles than pairs the pieces stream the weights rather
+          // than saturate the tensor pipe, and the narrower tiles' lower
+          // MMA efficiency does not show (measured on GB300, T <= 256:
+          // 160-wide pieces beat 256-wide ones); cost them at full
+          // efficiency (the division by c.eff below is undone).
+          const double narrow = tiles < units ? c.eff : 1.0;
+          if (k.split_k > 1 && (ksplit_piece_time(k, c.block_n) + fixed) * narrow < tail) {
+            tail = (ksplit_piece_time(k, c.block_n) + fixed) * narrow;
             ks = k;
             ways = 1;
           }
@@ -284,7 +290,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   r.workspace_bytes = 0;
   if (r.block_m == 256 && best_ks.split_k > 1) {
     r.split_k = best_ks.split_k;
-    r.workspace_bytes = ksplit_workspace_bytes(best_ks, r.block_n);
+    r.workspace_bytes = ksplit_workspace_bytes(best_ks, r.block_n, epilogue);
     items = tiles - best_ks.tail_tiles + best_ks.tail_tiles * best_ks.split_k;
   } else if (r.block_m == 256 && best_ways > 1) {
     r.split_n = best_ways;

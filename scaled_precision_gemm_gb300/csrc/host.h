@@ -70,17 +70,23 @@ inline KSplit ksplit_plan(int64_t tiles, int64_t units, int64_t nkb) {
 
 // Workspace of a K split with tiles bn columns wide: one 128 x bn fp32 slice
 // per (tail tile, piece, CTA of the pair), then one 64-bit arrival counter
-// per (tail tile, CTA).
-inline int64_t ksplit_workspace_bytes(const KSplit& k, int bn) {
+// per (tail tile, CTA, lane quarter, epilogue chunk: 32 columns, 64 for
+// SwiGLU).
+inline int64_t ksplit_workspace_bytes(const KSplit& k, int bn, int epilogue) {
   if (k.split_k < 2) return 0;
-  return k.tail_tiles * k.split_k * 2 * 128 * int64_t(bn) * 4 + k.tail_tiles * 2 * 8;
+  const int cw = epilogue == SPG_EPI_SWIGLU ? 64 : 32;
+  return k.tail_tiles * k.split_k * 2 * 128 * int64_t(bn) * 4 +
+         k.tail_tiles * 2 * 4 * (bn / cw) * 8;
 }
 
 // Duration of a K-split tail piece in K blocks of the tile: its own K
-// blocks plus the partial sums written by every piece and read back by the
-// last one (about 2.5 K blocks per 128 x 256 fp32 slice, measured).
+// blocks, the partial sums written by every piece and read back where each
+// chunk finishes (about 2.5 K blocks per 128 x 256 fp32 slice), and the
+// finish itself (partial store, fence, arrival, reduction, epilogue: about
+// 6 us on GB300, some 20 K blocks, measured), which makes the split lose
+// at short K.
 inline double ksplit_piece_time(const KSplit& k, int bn) {
-  return k.kb_per_split + 2.5 * k.split_k * (bn / 256.0);
+  return k.kb_per_split + 20.0 + 2.5 * k.split_k * (bn / 256.0);
 }
 
 // The selector behind spg_select_route (no validation).

@@ -107,16 +107,19 @@ def test_route_selector_k_split(lib, monkeypatch):
     monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
     for kind, T, N, K, epi in [("fp8_rowscaled", 256, 5120, 17408, "add"),
-                               ("fp8_rowscaled", 64, 6144, 5120, "linear"),
+                               ("fp8_rowscaled", 64, 6144, 17408, "linear"),
                                ("nvfp4", 256, 5120, 17408, "add"),
-                               ("fp8_tensor", 128, 4096, 4096, "linear")]:
+                               ("fp8_tensor", 128, 4096, 16384, "linear")]:
         plain = spg.select_route(kind, T, N, K, epi)
         assert plain["split_k"] == 1 and plain["workspace_bytes"] == 0
         r = spg.select_route(kind, T, N, K, epi, workspace=True)
         assert r["block_m"] == 256 and 2 <= r["split_k"] <= 4, (kind, T, r)
         tail = r["tiles"] % 76 if r["tiles"] % 76 else 76
         assert r["tiles"] < 76 and tail == r["tiles"]
-        per_tile = r["split_k"] * 2 * 128 * r["block_n"] * 4 + 16
+        # slices (piece x CTA x 128 rows x block_n fp32), then one 8-byte
+        # counter per (CTA, lane quarter, 32-column chunk)
+        cw = 64 if epi == "swiglu" else 32
+        per_tile = r["split_k"] * 2 * 128 * r["block_n"] * 4 + 2 * 4 * (r["block_n"] // cw) * 8
         assert r["workspace_bytes"] == tail * per_tile
         ws = spg.gemm_workspace_bytes(kind, T, N, K, epi)
         # the per-tensor size covers both B layouts
@@ -126,6 +129,8 @@ def test_route_selector_k_split(lib, monkeypatch):
         nkb = (K // 2 if kind == "nvfp4" else K + 127) // 128
         kbps = -(-nkb // r["split_k"])
         assert kbps >= 4 and (r["split_k"] - 1) * kbps < nkb  # no empty piece
+    # short K: the finish costs more than the split saves
+    assert spg.gemm_workspace_bytes("fp8_rowscaled", 64, 6144, 5120, "add") == 0
     # whole waves (19 x 4 pair tiles on 76 pairs): nothing to split
     assert spg.gemm_workspace_bytes("fp8_rowscaled", 19 * 256, 1024, 17408, "add") == 0
     # the tail pin
