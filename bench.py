@@ -9,6 +9,10 @@ timed region, as a deployment does offline.  L2 is flushed (a 512 MB write)
 before every case, outside the CUDA-event brackets; the reported time is the
 sum of the bracketed segments.
 
+The GEMMs go through the library's workspace entry points (a workspace of
+spg_gemm_workspace_bytes per case, allocated once), so the route may split
+the last partial wave along K where its cost model says that pays.
+
 Metric: TFLOP/s = sum(2 T N K) / step time, plus each case's GEMM-only rate
 and its fraction of the dense FP8 tensor peak.
 
@@ -301,9 +305,12 @@ def run_gpu(args):
             sb = torch.empty(1, dtype=torch.float32, device=dev)
             k.out = torch.empty((c["batch"], c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
             spg.quantize_fp8_tensor(b, bc, sb, scratch)   # weight-side operand, offline
+            k.ws = spg.gemm_workspace("fp8_tensor", c["M"], c["N"], c["K"], "linear", c["batch"],
+                                      device=dev)
             k.quant = lambda x, res, ac=ac, sa=sa: spg.quantize_fp8_tensor(x, ac, sa, scratch)
-            k.gemm = lambda c=c, ac=ac, sa=sa, bc=bc, sb=sb, out=k.out: spg.fp8_tensor_gemm(
-                c["layout"], ac, sa, bc, sb, c["M"], c["N"], c["K"], batch=c["batch"], out=out)
+            k.gemm = lambda c=c, ac=ac, sa=sa, bc=bc, sb=sb, out=k.out, k=k: spg.fp8_tensor_gemm(
+                c["layout"], ac, sa, bc, sb, c["M"], c["N"], c["K"], batch=c["batch"], out=out,
+                workspace=k.ws)
             k.launches = 3
             prepared.append(k)
             continue
@@ -313,6 +320,10 @@ def run_gpu(args):
         k.out = torch.empty((T, n_out), dtype=torch.bfloat16, device=dev)
         k.res = inputs[("r", N)][:T] if c["epi"] == "add" else None
         k.res_dev = k.res
+        # The library's workspace (allocated once, like any deployment would):
+        # lets the route split the last partial wave along K where that pays.
+        k.ws = spg.gemm_workspace("fp8_rowscaled" if c["kind"] == "fp8" else "nvfp4", T, N, K,
+                                  c["epi"], device=dev)
         if c["kind"] == "fp8":
             W, sw = inputs[("w", "fp8", K, N)]
             A = torch.empty((T, K), dtype=torch.uint8, device=dev)
@@ -320,7 +331,7 @@ def run_gpu(args):
             k.quant = lambda x, res, A=A, sa=sa, k=k: (spg.quantize_fp8_rows(x, A, sa),
                                                        setattr(k, "res_dev", res))
             k.gemm = lambda A=A, sa=sa, W=W, sw=sw, k=k, epi=c["epi"]: spg.fp8_rowscaled_gemm(
-                A, sa, W, sw, residual=k.res_dev, epilogue=epi, out=k.out)
+                A, sa, W, sw, residual=k.res_dev, epilogue=epi, out=k.out, workspace=k.ws)
             k.launches = 2
         else:
             Wc, sfW, gW = inputs[("w", "nvfp4", K, N)]
@@ -335,7 +346,7 @@ def run_gpu(args):
             k.quant = quant
             k.gemm = lambda A=A, sfA=sfA, gA=gA, Wc=Wc, sfW=sfW, gW=gW, k=k, epi=c["epi"]: \
                 spg.nvfp4_gemm(A, sfA, gA, Wc, sfW, gW, residual=k.res_dev, epilogue=epi,
-                               out=k.out)
+                               out=k.out, workspace=k.ws)
             k.launches = 4     # amax + finalize + quantize + GEMM (plus one memset)
         prepared.append(k)
 
@@ -448,6 +459,8 @@ def run_gpu(args):
                    "cases": [case_name(k.c) for k in prepared],
                    "step": "activation quantization + GEMM with fused epilogue per case",
                    "l2": "flushed (512 MB write) before every case, outside the timed brackets",
+                   "api": "workspace entry points (workspace sized by spg_gemm_workspace_bytes, "
+                          "allocated once; the route may split the last partial wave along K)",
                    "launch": "CUDA graph replay per case" if use_graphs else "eager",
                    "inputs": "bf16 N(0,1) activations/residual, N(0,0.02) weights (splitmix64 "
                              "Box-Muller, seeds 0/1/2); weights quantized once offline"},
