@@ -190,6 +190,10 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     const double full2 = static_cast<double>(t2 / pairs);
     double w2 = (t2 % pairs) ? full2 + 1.0 : full2;
     KSplit ks = ksplit_plan(t2, pairs, nkb);
+    // With fewer tiles than pairs the split pair tile beats the one-CTA tile
+    // only while the pair tile is mostly padding (T <= 128 measured on
+    // GB300: 37-41 vs 43 us at T = 16-64, 45-51 vs 43 us at T = 256).
+    if (t2 < pairs && T > 128 && !forced_tail) ks = KSplit();
     if (ks.split_k > 1 && tail_k_ok) {
       const double wk = full2 + (ksplit_piece_time(ks, 256) + fixed) / (kb + fixed);
       if (wk < w2 || !tail_none_ok) {

@@ -108,7 +108,7 @@ def test_route_selector_k_split(lib, monkeypatch):
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
     for kind, T, N, K, epi in [("fp8_rowscaled", 256, 5120, 17408, "add"),
                                ("fp8_rowscaled", 64, 6144, 17408, "linear"),
-                               ("nvfp4", 256, 5120, 17408, "add"),
+                               ("nvfp4", 128, 5120, 17408, "add"),
                                ("fp8_tensor", 128, 4096, 16384, "linear")]:
         plain = spg.select_route(kind, T, N, K, epi)
         assert plain["split_k"] == 1 and plain["workspace_bytes"] == 0
@@ -129,6 +129,8 @@ def test_route_selector_k_split(lib, monkeypatch):
         nkb = (K // 2 if kind == "nvfp4" else K + 127) // 128
         kbps = -(-nkb // r["split_k"])
         assert kbps >= 4 and (r["split_k"] - 1) * kbps < nkb  # no empty piece
+    # NVFP4 at T = 256: the one-CTA 128 x 128 tile (measured faster there)
+    assert spg.select_route("nvfp4", 256, 5120, 17408, "add", workspace=True)["block_m"] == 128
     # short K: the finish costs more than the split saves
     assert spg.gemm_workspace_bytes("fp8_rowscaled", 64, 6144, 5120, "add") == 0
     # whole waves (19 x 4 pair tiles on 76 pairs): nothing to split
