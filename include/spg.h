@@ -299,12 +299,13 @@ SPG_API spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t ba
 /* Workspace entry points: the GEMMs above, plus a caller-owned device
  * workspace that lets the last partial wave of two-SM tiles (every tile,
  * when the problem has fewer tiles than CTA pairs: narrow T such as decode
- * and small prefill chunks) be split along K into up to 4 pieces.  Each
- * piece writes its fp32 partial sums to the workspace; the CTA whose piece
- * arrives last adds all pieces in split order (so the result does not
- * depend on the arrival order and repeats bit for bit) and runs the fused
- * epilogue.  The result is the same GEMM as the plain entry points define,
- * with fp32 sums taken in a different order.  The pages keep a separate
+ * and small prefill chunks) be split along K into up to 4 pieces, when the
+ * route's cost model says that pays.  Each piece writes its fp32 partial
+ * sums to the workspace; for every 32-column chunk (64 for SwiGLU) of a
+ * lane quarter, the piece that arrives last adds all pieces in split order
+ * (so the result does not depend on the arrival order and repeats bit for
+ * bit) and runs the fused epilogue on it.  The result is the same GEMM as
+ * the plain entry points define, with fp32 sums taken in a different order.  The pages keep a separate
  * small-T route on sm_120 (ninfer PR #160, the paragraph on the quantizer's
  * plane layout); here the tcgen05 pair kernel covers narrow T by this split.
  *
