@@ -88,6 +88,9 @@ typedef struct {
   int32_t split_n;      /* last partial wave: tiles split along N this many ways */
   int32_t split_k;      /* last partial wave: tiles split along K this many ways */
   int64_t workspace_bytes; /* workspace the K split needs (0 without one)     */
+  int32_t swap_ab;      /* 1: operands exchanged (weights on the M side, the   */
+                        /* T tokens on the N side; block_n covers tokens)     */
+  int32_t reserved;     /* 0                                                  */
 } spg_route;
 
 /* Human-readable name of a status code (static string). */

@@ -48,7 +48,8 @@ class Route(ctypes.Structure):
                 ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("smem_bytes", ctypes.c_int32),
                 ("variant", ctypes.c_int32), ("split_n", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
+                ("split_k", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+                ("swap_ab", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 def library_path() -> str:

@@ -344,6 +344,171 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
 
 namespace spg {
 
+// Epilogue of the swapped pair tile (narrow T): TMEM lane = weight row n
+// (the output column), TMEM column = token t (the output row).  Each thread
+// owns one weight row; a 32-token chunk of its accumulator row becomes a
+// column of a 32 x 32 bf16 output block, staged through 64-byte-swizzled
+// shared memory (row t of the block = 64 bytes; each warp writes one row per
+// token with conflict-free 2-byte stores) and TMA-stored.  Scales: p.row_scale
+// holds the weight scales (per lane), p.col_scale the token scales (per
+// column); bias per weight row.  The residual [T, N] arrives by TMA (tmR:
+// the same 32 x 32 box and swizzle as the output) into this warp's blocks
+// of res_smem (one 2 KB block per chunk), requested before the accumulator
+// is ready and completing on res_bars[warp].  p.M = weight rows (N of the
+// layer), p.N = tokens (T).  K-split pieces go through split_piece_finish
+// like the unswapped tile.
+template <int EPI, int BN, typename ItemFn, typename ArriveEmpty>
+__device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CUtensorMap* tmY,
+                                                   uint32_t tmem_base, uint64_t* acc_full,
+                                                   ArriveEmpty arrive_empty, uint8_t* epi_smem,
+                                                   int item_begin, int item_end, int item_step,
+                                                   ItemFn item_fn, const WaitCtl& ctl,
+                                                   int cta_rank, const CUtensorMap* tmR,
+                                                   uint64_t* res_bars, uint8_t* res_smem) {
+  static_assert(EPI != SPG_EPI_SWIGLU, "the swapped tile has no SwiGLU epilogue");
+  constexpr int kBufBytes = 32 * 64;
+  constexpr int kChunks = BN / 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int e = warp - 2;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  uint8_t* stage0 = epi_smem + (e * 2) * kBufBytes;
+  uint8_t* res0 = res_smem + e * kChunks * kBufBytes;
+  uint64_t* res_bar = res_bars + e;
+  uint32_t res_phase = 0;
+  bool res_inflight = false;
+  int it = 0;
+  int chunk_ctr = 0;
+  const int n_w = p.M;  // weight rows = output columns
+  const int n_t = p.N;  // tokens = output rows
+
+  for (int item = item_begin; item < item_end; item += item_step, ++it) {
+    const int buf = it & 1;
+    const uint32_t acc_ph = (it >> 1) & 1;
+    const WorkItem tc = item_fn(item);
+    const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+    const int n0 = tc.mb * 128 + q * 32;  // this warp's first weight row
+    const int n = n0 + lane;
+    const bool live = n0 < n_w;
+    const bool n_ok = n < n_w;
+    const int t0 = tc.nb * BN;  // first token of the tile
+
+    // Epilogue operands, requested before the accumulator is ready: the
+    // weight scale and bias of this thread's row, the token scales (token
+    // t0 + 32 c + lane in sar[c]) and the residual of the first chunk.
+    const float sw = n_ok ? __ldg(p.row_scale + n) : 0.f;
+    float bias = 0.f;
+    if (p.bias_kind != 0 && n_ok) {
+      if (p.bias_kind == 1) {
+        bias = __uint_as_float(uint32_t(__ldg(static_cast<const unsigned short*>(p.bias) + n))
+                               << 16);
+      } else {
+        const uint16_t code = __ldg(static_cast<const uint8_t*>(p.bias) + n);
+        bias = __fmul_rn(e4m3x2_to_float2(uint16_t(code | (code << 8))).x, __ldg(p.bias_scale));
+      }
+    }
+    float sar[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const int t = t0 + c * 32 + lane;
+      sar[c] = t < n_t ? __ldg(p.col_scale + t) : 0.f;
+    }
+    if constexpr (EPI == SPG_EPI_ADD) {
+      if (live) {
+        // The blocks were last read by this warp's generic loads (previous
+        // item): order those before the asynchronous writes.
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(res_bar, kChunks * kBufBytes);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_3d(res0 + c * kBufBytes, tmR, res_bar, n0, t0 + c * 32, 0);
+        }
+        res_inflight = true;
+      }
+    }
+
+    if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
+    tc_fence_after();
+    uint32_t own_mask = live ? 0xffffffffu : 0u;
+    if (tc.split >= 0) own_mask = split_piece_finish<BN, 32, 8>(p, t_row, tc, cta_rank, q, 0, BN, live);
+    own_mask &= (1u << kChunks) - 1u;
+    if constexpr (EPI == SPG_EPI_ADD) {
+      // Every lane observes the completed copies itself.
+      if (res_inflight) {
+        if (!mbar_wait(res_bar, res_phase, ctl, kErrWaitFull)) break;
+        res_inflight = false;
+        res_phase ^= 1u;
+      }
+    }
+    // After a K-split reduction TMEM holds the total of all pieces.
+    const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
+    if (own_mask == 0u) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_empty(buf);
+      continue;
+    }
+    const int last_c = 31 - __clz(own_mask);
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      if (!((own_mask >> c) & 1u)) continue;
+      const int tc0 = t0 + c * 32;  // first token of the chunk
+      uint32_t raw[32];
+      if (have_k) {
+        tmem_ld_32x32b_x32(t_row + c * 32, raw);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) raw[j] = 0u;
+      }
+      unsigned short resv[32];
+      if constexpr (EPI == SPG_EPI_ADD) {
+        // Row j of the block = token tc0 + j; this lane's weight row sits in
+        // 16-byte unit lane / 8 of it, swizzled like the output.
+        const uint8_t* rb = res0 + c * kBufBytes + (lane & 7) * 2;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          resv[j] = *reinterpret_cast<const unsigned short*>(
+              rb + j * 64 + (((lane >> 3) ^ ((j >> 1) & 3)) * 16));
+      }
+      if (have_k) tmem_wait_ld();
+      if (c == last_c) {
+        // Every column of this accumulator buffer has been read: hand it back.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_empty(buf);
+      }
+      uint8_t* sbuf = stage0 + (chunk_ctr & 1) * kBufBytes;
+      ++chunk_ctr;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float v = __uint_as_float(raw[j]) * (sw * __shfl_sync(0xffffffffu, sar[c], j));
+        v += bias;
+        if constexpr (EPI == SPG_EPI_ADD) v += __uint_as_float(uint32_t(resv[j]) << 16);
+        // Row j of the block (token tc0 + j), column `lane` (weight row n),
+        // 16-byte unit swizzled as in the unswapped epilogue.
+        const int unit = (lane >> 3) ^ ((j >> 1) & 3);
+        *reinterpret_cast<__nv_bfloat16*>(sbuf + j * 64 + unit * 16 + (lane & 7) * 2) =
+            __float2bfloat16_rn(v);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (n0 < n_w && tc0 < n_t) tma_store_3d(tmY, sbuf, n0, tc0, 0);
+        bulk_commit();
+      }
+    }
+  }
+  // After an abort no residual copy may still be writing shared memory.
+  if (EPI == SPG_EPI_ADD && res_inflight && lane == 0)
+    mbar_wait_drain(res_bar, res_phase, p.drain_ns, p.err);
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
+}
+
 // Side duty of the register-drain epilogue warps: a functor called while
 // they wait for the accumulator and between output chunks, which must not
 // block.  NoService: none.
@@ -622,12 +787,6 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
       }
       ++chunk_ctr;
     }
-  }
-  if constexpr (kResTma) {
-    // No residual copy may still be writing the staging buffers at exit.
-    if (res_inflight >= 0 && lane == 0)
-      mbar_wait_drain(&res_bars[e * 2 + (res_inflight & 1)], uint32_t(res_inflight >> 1) & 1u,
-                      p.drain_ns, p.err);
   }
   if constexpr (kResTma) {
     // No residual copy may still be writing the staging buffers at exit.

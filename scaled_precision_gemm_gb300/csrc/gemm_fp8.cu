@@ -8,6 +8,17 @@ namespace {
 
 template <int EPI>
 spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
+  if constexpr (EPI != SPG_EPI_SWIGLU) {
+    if (r.swap_ab) {
+      // linear_add gives one ring stage to its residual blocks.
+      constexpr bool kAdd = EPI == SPG_EPI_ADD;
+      if (r.block_n == 64)
+        return launch_gemm_2sm_variant<EPI, 64, kAdd ? 9 : 10, false, false, kScaleRow, true>(
+            m, p, r.grid, s);
+      return launch_gemm_2sm_variant<EPI, 128, kAdd ? 7 : 8, false, false, kScaleRow, true>(
+          m, p, r.grid, s);
+    }
+  }
   if (r.block_m == 256) {
     if (r.block_n == 192)
       return launch_gemm_2sm_variant<EPI, 192, 7, false, false, kScaleRow>(m, p, r.grid, s);
@@ -46,6 +57,37 @@ spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, c
 
   const spg_route r = route_for(SPG_KIND_FP8_ROWSCALED, T, N, K, epilogue, 1, false, workspace,
                                 workspace_bytes);
+  if (r.swap_ab) {
+    // Swapped narrow-T tile: A operand = the weights (256 rows per pair
+    // tile), B operand = the activations (block_n tokens); the epilogue
+    // writes Y [T, N] transposed from the accumulator.
+    GemmMaps maps;
+    const uint32_t t_rows = static_cast<uint32_t>(r.block_n / 2);
+    if (!make_tmap_3d(&maps.a, W, false, K, N, 1, K, K * N, 128, 128, 128) ||
+        !make_tmap_3d(&maps.b, A, false, K, T, 1, K, K * T, 128, t_rows, 128) ||
+        !make_tmap_3d(&maps.y, Y, true, N, T, 1, N * 2, N * 2 * T, 32, 32, 64))
+      return SPG_ERR_CUDA;
+    // The fourth map: the residual, as 32 x 32 blocks like the output.
+    if (epilogue == SPG_EPI_ADD) {
+      if (!make_tmap_3d(&maps.b_narrow, residual, true, N, T, 1, N * 2, N * 2 * T, 32, 32, 64))
+        return SPG_ERR_CUDA;
+    } else {
+      maps.b_narrow = maps.b;
+    }
+    GemmParams p;
+    fill_common_params(p, r, N, T, K, K, N, 1);
+    if (!p.err) return SPG_ERR_CUDA;
+    if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
+    const int pairs = num_sms() / 2;
+    plan_items(p, r, pairs, workspace);
+    spg_route rr = r;
+    rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+    p.row_scale = sw;
+    p.col_scale = sa;
+    p.residual = static_cast<const __nv_bfloat16*>(residual);
+    if (epilogue == SPG_EPI_ADD) return dispatch<SPG_EPI_ADD>(rr, maps, p, stream);
+    return dispatch<SPG_EPI_LINEAR>(rr, maps, p, stream);
+  }
   const int b_rows = r.block_m == 256 ? r.block_n / 2 : r.block_n;  // B rows staged per CTA
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;

@@ -27,7 +27,12 @@
 
 namespace spg {
 
-template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+// SWAP: the operands' roles exchanged for narrow T -- A is the weight matrix
+// (256 weight rows per pair tile, the MMA's M), B the activations (BN
+// tokens, the MMA's N), and the epilogue writes the transposed accumulator
+// (epilogue_loop_swap).  The swapped tile never splits along N, so its
+// fourth tensor map (tmBnarrow) carries the residual of linear_add.
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
 struct Gemm2smCfg {
   static constexpr int kBM = 128;  // rows per CTA (the pair covers 256)
   static constexpr int kBKBytes = 128;
@@ -39,17 +44,26 @@ struct Gemm2smCfg {
   static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
   static constexpr int kEpiWarps = 4;
   static constexpr int kEpiBytes = kEpiWarps * 2 * 32 * 64;
+  // Swapped linear_add: one 32 x 32 bf16 residual block per epilogue warp
+  // and 32-token chunk.
+  static constexpr int kResBytes =
+      (SWAP && EPI == SPG_EPI_ADD) ? kEpiWarps * (BN / 32) * 32 * 64 : 0;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kSmemBytes =
+      1024 + STAGES * kStageBytes + kEpiBytes + kResBytes + kBarBytes;
   static constexpr int kThreads = 192;
 
-  static_assert(BN == 128 || BN == 160 || BN == 192 || BN == 256,
-                "pair tiles are 256 x {128, 160, 192, 256}");
+  static_assert(SWAP ? (BN == 32 || BN == 64 || BN == 128)
+                     : (BN == 128 || BN == 160 || BN == 192 || BN == 256),
+                "pair tiles are 256 x {128, 160, 192, 256} (256 x {32, 64, 128} swapped)");
+  static_assert(!SWAP || (EPI != SPG_EPI_SWIGLU && !A_MN && !B_MN && SCALE == kScaleRow),
+                "the swapped tile serves row-scaled linear / linear_add with K-major operands");
   static_assert(EPI != SPG_EPI_SWIGLU || BN % 64 == 0, "SwiGLU tiles hold whole 64-column chunks");
   static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(2 * STAGES + 6 + (kResBytes ? kEpiWarps : 0) <= kBarBytes / 8,
+                "barrier area too small");
 
   // kind::f8f6f4, E4M3 x E4M3 -> f32, M = 256 (pair), N = BN.
   __host__ __device__ static constexpr uint32_t idesc() {
@@ -58,18 +72,19 @@ struct Gemm2smCfg {
   }
 };
 
-template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmY,
                     const __grid_constant__ CUtensorMap tmBnarrow, const GemmParams p) {
-  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* epi = smem + STAGES * Cfg::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + Cfg::kEpiBytes);
+  uint8_t* res_smem = epi + Cfg::kEpiBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(res_smem + Cfg::kResBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;
@@ -77,6 +92,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint64_t* res_bars = drain + 2;  // swapped linear_add: one per epilogue warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -94,6 +110,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&acc_empty[b], 2 * Cfg::kEpiWarps);
     }
     mbar_init(drain, 1);
+    if constexpr (Cfg::kResBytes != 0)
+      for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -101,7 +119,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmY);
-    if (p.split_ways > 1) prefetch_tmap(&tmBnarrow);
+    if (p.split_ways > 1 || Cfg::kResBytes != 0) prefetch_tmap(&tmBnarrow);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
@@ -219,16 +237,19 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    epilogue_loop<EPI, SCALE, BN>(
-        p, &tmY, tmem_base, acc_full,
-        [&](int b) { mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0)); }, epi, pair,
-        p.total_items, num_pairs,
-        [&](int item) {
-          WorkItem w = work_item(item, p, BN);
-          w.mb = w.mb * 2 + int(rank);
-          return w;
-        },
-        ctl, int(rank));
+    auto arrive_fn = [&](int b) { mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0)); };
+    auto item_fn = [&](int item) {
+      WorkItem w = work_item(item, p, BN);
+      w.mb = w.mb * 2 + int(rank);
+      return w;
+    };
+    if constexpr (SWAP)
+      epilogue_loop_swap<EPI, BN>(p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair,
+                                  p.total_items, num_pairs, item_fn, ctl, int(rank), &tmBnarrow,
+                                  res_bars, res_smem);
+    else
+      epilogue_loop<EPI, SCALE, BN>(p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair,
+                                    p.total_items, num_pairs, item_fn, ctl, int(rank));
   }
 
   tc_fence_before();

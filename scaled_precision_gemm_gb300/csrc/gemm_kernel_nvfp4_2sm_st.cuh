@@ -54,7 +54,8 @@ struct Nvfp4StCfg {
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
 
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert((4 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 <= kBarBytes, "barrier area too small");
+  static_assert((4 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 + 4 * STAGES <= kBarBytes,
+                "barrier area too small");
   __host__ __device__ static constexpr uint32_t idesc() { return Base::idesc(); }
 };
 
@@ -84,12 +85,24 @@ __device__ __forceinline__ void store_stage_scales(uint32_t tmem_base, uint32_t 
 // The epilogue warps' side duty: store the scales of every stage of this
 // warp's parity whose scale tiles have landed, for its lane quarter, and
 // signal each one as soon as its stores are done (non-blocking).
+//
+// Stage uses alternate between the two halves of the warps while the ring
+// has an odd number of stages, so the previous use of a ring slot belongs to
+// the other half.  A parity test alone cannot tell "use n has landed" from
+// "use n - STAGES has not landed yet" (both phases have the same parity
+// distance), so a use is tested only once landed[slot] -- the count of uses
+// of that slot seen complete, raised by whichever warp saw them -- shows the
+// previous use complete.  Without this guard a warp that ran ahead at the
+// start of a launch stored scales for a later use into a slot whose current
+// use the MMAs had not yet read (measured on GB300: whole lane quarters of a
+// kernel's first tiles wrong in a few of 40 launches).
 template <int STAGES>
 struct ScaleService {
   static constexpr bool kActive = true;
   int next;           // next stage to serve (this warp's parity)
   int end;            // stages of this CTA pair
   uint64_t* sf_full;         // this CTA's scale-tile barriers
+  int* landed;               // per ring slot: uses seen complete (shared)
   uint64_t* sf_ready;        // the leader's stage barriers (local in the leader)
   uint32_t sf_ready_leader;  // the same, as cluster addresses (peer CTA)
   bool leader;
@@ -101,13 +114,18 @@ struct ScaleService {
   __device__ __forceinline__ void operator()() {
     while (next < end) {
       const int s = next % STAGES;
-      const uint32_t par = uint32_t(next / STAGES) & 1u;
-      const int ready = __shfl_sync(
-          0xffffffffu, lane == 0 ? (mbar_test_wait(smem_u32(&sf_full[s]), par) ? 1 : 0) : 0, 0);
+      const int u = next / STAGES;  // use of slot s
+      const uint32_t par = uint32_t(u) & 1u;
+      int ready = 0;
+      if (lane == 0)
+        ready = (u == 0 || *reinterpret_cast<volatile int*>(&landed[s]) >= u) &&
+                mbar_test_wait(smem_u32(&sf_full[s]), par);
+      ready = __shfl_sync(0xffffffffu, ready, 0);
       if (!ready) return;
       // Every lane acquires the completed phase before it reads the tiles.
       (void)mbar_test_wait(smem_u32(&sf_full[s]), par);
       __syncwarp();
+      if (lane == 0) atomicMax(&landed[s], u + 1);
       const uint8_t* ssfa = ring + s * stage_bytes + sf_offset;
       store_stage_scales(tmem_base, sf_col_base + uint32_t(s) * sf_cols_per_stage, ssfa,
                          ssfa + 2048, q, lane);
@@ -156,6 +174,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* res_bars = drain + 1;  // linear_add residual: 2 per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(res_bars + 2 * Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* landed = abort_flag + 1;  // STAGES counters (ScaleService)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -175,6 +194,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     mbar_init(drain, 1);
     for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) landed[s] = 0;
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -309,6 +329,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     svc.next = (warp - 2) >> 2;
     svc.end = my_stages;
     svc.sf_full = sf_full;
+    svc.landed = landed;
     svc.sf_ready = sf_ready;
     svc.sf_ready_leader = mapa_shared(smem_u32(sf_ready), 0);
     svc.leader = rank == 0;

@@ -40,11 +40,11 @@ spg_status launch_gemm_variant(const GemmMaps& maps, const GemmParams& p, int gr
 }
 
 // Two-SM variant: clusters of 2 CTAs, grid = 2 x pairs.
-template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
 spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, int grid,
                                    cudaStream_t stream) {
-  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
-  auto kern = gemm_kernel_2sm<EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
+  auto kern = gemm_kernel_2sm<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;

@@ -145,6 +145,19 @@ bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t 
 // problems therefore fall back to narrower or one-CTA tiles, which is the
 // AstrAI "small CTA below a tile-count threshold" rule in the same terms.
 namespace {
+// Whether the swapped narrow-T tile is the default for this shape (T <= 128
+// already checked): its 256-row weight tiles must fit one wave, and above
+// T = 16 they must leave at least half of the pairs free for the K split.
+// Measured on GB300 (linear / linear_add, with a workspace): N = 5120 and
+// 6144 (20, 24 tiles) run 17-30% faster swapped at every T <= 128; N =
+// 17408 (68 tiles, no split possible) is faster swapped at T <= 16 (23-25
+// against 31 us) and slower above it (25 against 22.5 us).
+bool swap_default(int64_t T, int64_t N, int pairs) {
+  const int64_t tiles = (N + 255) / 256;
+  if (tiles > pairs) return false;
+  return T <= 16 || 2 * tiles <= pairs;
+}
+
 struct Candidate {
   int block_m, block_n, stages;
   double eff;
@@ -179,6 +192,42 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const double fixed = 6.0;  // per-tile fixed cost in 128-byte-deep K blocks
   KSplit best_ks;
   int best_ways = 1;
+  // Swapped pair tile for narrow T (FP8 row-scaled, one problem, linear /
+  // linear_add): the weight rows fill the MMA's 256-row M side and the
+  // tokens its N side (64 or 128 wide), so every staged byte but the small
+  // token tile is weight stream, where the unswapped tile stages a 256-row
+  // activation tile that is mostly out-of-range padding.  SPG_FORCE_VARIANT
+  // = swap pins it; any other forced variant disables it.
+  const bool swap_ok = kind == SPG_KIND_FP8_ROWSCALED && nb == 1 && epilogue != SPG_EPI_SWIGLU &&
+                       !b_mn_major && T >= 1 && T <= 128;
+  const bool swap = swap_ok && (forced_name ? std::strcmp(forced_name, "swap") == 0
+                                            : swap_default(T, N, pairs));
+  if (swap) {
+    r.block_m = 256;
+    r.block_n = T <= 64 ? 64 : 128;
+    r.block_k = 128;
+    const bool add = epilogue == SPG_EPI_ADD;
+    r.stages = r.block_n == 64 ? (add ? 9 : 10) : (add ? 7 : 8);
+    r.variant = 6;
+    r.swap_ab = 1;
+    r.tiles = (N + 255) / 256;
+    r.split_n = 1;
+    r.split_k = 1;
+    int64_t items = r.tiles;
+    // The K split of the last partial wave, priced as for the unswapped
+    // pieces at full efficiency (the pieces stream weights).
+    KSplit k = tail_k_ok ? ksplit_plan(r.tiles, pairs, nkb) : KSplit();
+    if (k.split_k > 1 && tail_none_ok && ksplit_piece_time(k, r.block_n) >= kb) k = KSplit();
+    if (k.split_k > 1) {
+      r.split_k = k.split_k;
+      r.workspace_bytes = ksplit_workspace_bytes(k, r.block_n, epilogue);
+      items = r.tiles - k.tail_tiles + k.tail_tiles * k.split_k;
+    }
+    r.grid = static_cast<int>(2 * (items < pairs ? items : pairs));
+    r.smem_bytes = 1024 + r.stages * (128 * 128 + r.block_n / 2 * 128) + 4 * 2 * 2048 +
+                   (add ? 4 * (r.block_n / 32) * 2048 : 0) + 256;
+    return r;
+  }
   if (kind == SPG_KIND_NVFP4) {
     // Two-SM 256x256 pair tile (optionally with a K split of its last
     // partial wave), or the one-CTA 128x128 tile when its waves are cheaper

@@ -102,6 +102,38 @@ def test_route_selector_forced_variants(lib, monkeypatch):
     assert r["tiles"] == 4 * ((5120 + r["block_n"] - 1) // r["block_n"])
 
 
+def test_route_selector_swap(lib, monkeypatch):
+    """The swapped narrow-T tile: FP8 row-scaled, one problem, linear or
+    linear_add, T <= 128; token tile 64 or 128 wide, weights in 256-row tiles."""
+    monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "swap")
+    for T, bn in [(1, 64), (64, 64), (65, 128), (128, 128)]:
+        for epi in ["linear", "add"]:
+            r = spg.select_route("fp8_rowscaled", T, 5120, 17408, epi, workspace=True)
+            assert r["swap_ab"] == 1 and r["block_m"] == 256 and r["block_n"] == bn, (T, r)
+            assert r["tiles"] == 20 and r["split_k"] == 3 and r["split_n"] == 1
+            assert r["workspace_bytes"] == 20 * (3 * 2 * 128 * bn * 4 + 2 * 4 * (bn // 32) * 8)
+            assert r["grid"] == 2 * min(60, 76)
+            assert r["smem_bytes"] <= 232448
+            plain = spg.select_route("fp8_rowscaled", T, 5120, 17408, epi)
+            assert plain["swap_ab"] == 1 and plain["split_k"] == 1 and plain["grid"] == 40
+    # the default: swapped while the weight tiles leave half of the pairs
+    # free (or T <= 16 and one wave of tiles)
+    monkeypatch.delenv("SPG_FORCE_VARIANT")
+    for T, N, swapped in [(1, 5120, 1), (64, 6144, 1), (128, 9728, 1), (128, 9984, 0),
+                          (16, 17408, 1), (17, 17408, 0), (16, 19712, 0), (129, 5120, 0)]:
+        r = spg.select_route("fp8_rowscaled", T, N, 17408, "add", workspace=True)
+        assert r["swap_ab"] == swapped, (T, N, r)
+    # a short K is not split when the finish costs more than it saves
+    r = spg.select_route("fp8_rowscaled", 64, 2048, 1024, "add", workspace=True)
+    assert r["swap_ab"] == 1 and r["split_k"] == 1
+    # not swapped: wider T, SwiGLU, batches, other GEMM kinds
+    assert spg.select_route("fp8_rowscaled", 129, 5120, 17408, "add")["swap_ab"] == 0
+    assert spg.select_route("fp8_rowscaled", 64, 5120, 17408, "swiglu")["swap_ab"] == 0
+    assert spg.select_route("fp8_tensor", 64, 5120, 17408, "linear", 2)["swap_ab"] == 0
+    assert spg.select_route("nvfp4", 64, 5120, 17408, "add")["swap_ab"] == 0
+
+
 def test_route_selector_k_split(lib, monkeypatch):
     """Workspace routes split the last partial wave along K; the plain routes never do."""
     monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
@@ -132,7 +164,7 @@ def test_route_selector_k_split(lib, monkeypatch):
     # NVFP4 at T = 256: the one-CTA 128 x 128 tile (measured faster there)
     assert spg.select_route("nvfp4", 256, 5120, 17408, "add", workspace=True)["block_m"] == 128
     # short K: the finish costs more than the split saves
-    assert spg.gemm_workspace_bytes("fp8_rowscaled", 64, 6144, 5120, "add") == 0
+    assert spg.gemm_workspace_bytes("fp8_rowscaled", 256, 6144, 5120, "add") == 0
     # whole waves (19 x 4 pair tiles on 76 pairs): nothing to split
     assert spg.gemm_workspace_bytes("fp8_rowscaled", 19 * 256, 1024, 17408, "add") == 0
     # the tail pin
