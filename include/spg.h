@@ -310,7 +310,10 @@ SPG_API spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t ba
  * bit) and runs the fused epilogue on it.  The result is the same GEMM as
  * the plain entry points define, with fp32 sums taken in a different order.  The pages keep a separate
  * small-T route on sm_120 (ninfer PR #160, the paragraph on the quantizer's
- * plane layout); here the tcgen05 pair kernel covers narrow T by this split.
+ * plane layout); here the tcgen05 pair kernel covers narrow T by this split
+ * and, for fp8_rowscaled_gemm(_ws) linear / linear_add at T <= 128, by a
+ * swapped pair tile (the weights on the MMA's 256-row side, the tokens on
+ * its N side; spg_route.swap_ab), which the plain entry points use too.
  *
  * workspace: device memory, 16-byte aligned, at least
  *   spg_gemm_workspace_bytes(kind, T, N, K, epilogue, batch) bytes for the
