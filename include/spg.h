@@ -84,7 +84,11 @@ typedef struct {
   int32_t grid;         /* persistent CTAs launched                           */
   int64_t tiles;        /* output tiles of the whole problem (all batches)    */
   int32_t smem_bytes;   /* dynamic shared memory per CTA                      */
-  int32_t variant;      /* kernel variant index inside the library            */
+  int32_t variant;      /* kernel variant index inside the library (FP8:      */
+                        /* 0-3 pair tiles 256/192/160/128 wide, 4-5 one-CTA  */
+                        /* 256/128, 6 swapped pair tile; NVFP4: 0 pair tile  */
+                        /* with copied scales, 2 one-CTA, 3 pair tile with   */
+                        /* warp-stored scales)                               */
   int32_t split_n;      /* last partial wave: tiles split along N this many ways */
   int32_t split_k;      /* last partial wave: tiles split along K this many ways */
   int64_t workspace_bytes; /* workspace the K split needs (0 without one)     */
@@ -96,7 +100,8 @@ typedef struct {
 /* Human-readable name of a status code (static string). */
 SPG_API const char* spg_status_string(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor).  2.00: spg_route grew the
+ * swap_ab / reserved fields (its size changed). */
 SPG_API int spg_version(void);
 
 /* Bound, in nanoseconds, of every in-kernel wait of later launches

@@ -381,7 +381,9 @@ extern "C" const char* spg_status_string(int s) {
   }
 }
 
-extern "C" int spg_version(void) { return 101; }
+static_assert(sizeof(spg_route) == 72, "spg_route layout (the Python binding mirrors it)");
+
+extern "C" int spg_version(void) { return 200; }
 
 extern "C" void spg_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed);
