@@ -88,7 +88,8 @@ typedef struct {
                         /* 0-3 pair tiles 256/192/160/128 wide, 4-5 one-CTA  */
                         /* 256/128, 6 swapped pair tile; NVFP4: 0 pair tile  */
                         /* with copied scales, 2 one-CTA, 3 pair tile with   */
-                        /* warp-stored scales)                               */
+                        /* warp-stored scales, 4 CUDA-core GEMV for T <= 4:  */
+                        /* block_m 1, block_n 2 weight rows per warp)        */
   int32_t split_n;      /* last partial wave: tiles split along N this many ways */
   int32_t split_k;      /* last partial wave: tiles split along K this many ways */
   int64_t workspace_bytes; /* workspace the K split needs (0 without one)     */

@@ -2,10 +2,25 @@
 // E4M3 scale per 16 elements, scale tiles loaded whole, linear_add and the
 // fused SwiGLU route).
 #include "gemm_launch.cuh"
+#include "gemv_nvfp4.cuh"
 
 using namespace spg;
 
 namespace {
+
+template <int EPI, int TT>
+spg_status launch_gemv(const GemvParams& p, cudaStream_t s) {
+  const int grid = (p.N / 2 + 3) / 4;  // one warp per weight-row pair, 4 per CTA
+  gemv_nvfp4_kernel<EPI, TT><<<grid, 128, 0, s>>>(p);
+  return launch_status();
+}
+
+template <int EPI>
+spg_status launch_gemv_tokens(const GemvParams& p, cudaStream_t s) {
+  if (p.T == 1) return launch_gemv<EPI, 1>(p, s);
+  if (p.T == 2) return launch_gemv<EPI, 2>(p, s);
+  return launch_gemv<EPI, 4>(p, s);
+}
 
 template <int EPI>
 spg_status launch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
@@ -44,6 +59,36 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
 
   const spg_route r =
       route_for(SPG_KIND_NVFP4, T, N, K, epilogue, 1, false, workspace, workspace_bytes);
+  if (r.variant == 4) {
+    // Decode-sized T: the CUDA-core GEMV (no tensor maps, no workspace).
+    GemvParams g;
+    g.A = A;
+    g.sfA = sfA;
+    g.gA = gA;
+    g.W = W;
+    g.sfW = sfW;
+    g.gW = gW;
+    g.bias = bias;
+    g.bias_scale = bias_scale;
+    g.bias_kind = 0;
+    if (bias) {
+      if (!aligned16(bias) || (bias_scale && !aligned16(bias_scale))) return SPG_ERR_MISALIGNED;
+      g.bias_kind = bias_scale ? 2 : 1;
+    } else if (bias_scale) {
+      return SPG_ERR_INVALID_ARG;
+    }
+    g.residual = static_cast<const __nv_bfloat16*>(residual);
+    g.Y = static_cast<__nv_bfloat16*>(Y);
+    g.T = static_cast<int>(T);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    g.n_out = static_cast<int>(epilogue == SPG_EPI_SWIGLU ? N / 2 : N);
+    switch (epilogue) {
+      case SPG_EPI_LINEAR: return launch_gemv_tokens<SPG_EPI_LINEAR>(g, stream);
+      case SPG_EPI_ADD: return launch_gemv_tokens<SPG_EPI_ADD>(g, stream);
+      default: return launch_gemv_tokens<SPG_EPI_SWIGLU>(g, stream);
+    }
+  }
   const int64_t kh = K / 2;
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;

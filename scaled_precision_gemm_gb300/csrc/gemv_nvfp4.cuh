@@ -1,0 +1,201 @@
+// NVFP4 GEMV for decode-sized T (T <= 4) on the CUDA cores, sm_103a.
+//
+// With a handful of tokens the NVFP4 GEMM is a stream of weight codes: a
+// tensor-core tile would pad T to 128 rows and wait on its pipeline's fill
+// and finish.  Here one warp owns two consecutive weight rows (a SwiGLU
+// gate/up pair) and its lanes walk K in 32-element chunks (16 code bytes =
+// two 16-element scale blocks), four chunks in flight per lane.
+//
+// Arithmetic: an E2M1 code becomes an int8 holding twice its value (a
+// 16-entry table applied to four codes at a time with byte permutes), so a
+// block's dot product sum_i (2 a_i)(2 w_i) is an exact integer (dp4a).  It
+// is multiplied by the product of the two blocks' E4M3 scales (exact in
+// fp32) and accumulated in fp32; the lanes' sums are added across the warp
+// and scaled by 1/4.  The epilogue then applies gA * gW, the bias, and the
+// residual or SwiGLU in the order of the tensor-core epilogue.  Relative to
+// the tile kernels only the fp32 summation order differs.
+//
+// Scale reads follow the blocked layout (512-byte tiles of 128 rows x 64 K
+// elements; row r, block b at ((r / 128) * K/64 + b / 4) * 512 + (r % 32) *
+// 16 + ((r % 128) / 32) * 4 + b % 4): the two blocks of a chunk are one
+// aligned 16-bit load.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace spg {
+
+struct GemvParams {
+  const uint8_t* A;    // [T, K/2] codes
+  const uint8_t* sfA;  // blocked scales of A
+  const float* gA;
+  const uint8_t* W;    // [N, K/2] codes
+  const uint8_t* sfW;  // blocked scales of W
+  const float* gW;
+  const void* bias;          // per weight row, or nullptr
+  const float* bias_scale;   // bias_kind 2
+  int bias_kind;             // 0 none, 1 bf16, 2 E4M3 x bias_scale
+  const __nv_bfloat16* residual;  // [T, N] (linear_add)
+  __nv_bfloat16* Y;               // [T, n_out]
+  int T, N, K, n_out;
+};
+
+// Four E2M1 codes (16 bits, element i in nibble i) -> four int8 holding
+// twice the values (element i in byte i).
+__device__ __forceinline__ uint32_t e2m1x4_to_s8x2(uint32_t codes16) {
+  const uint32_t mag = codes16 & 0x7777u;
+  // twice the magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 and their negatives
+  const uint32_t pos = __byte_perm(0x03020100u, 0x0C080604u, mag);
+  const uint32_t neg = __byte_perm(0xFDFEFF00u, 0xF4F8FAFCu, mag);
+  // byte i from neg (selector i + 4) where the code's sign bit is set
+  return __byte_perm(pos, neg, 0x3210u | ((codes16 >> 1) & 0x4444u));
+}
+
+// 32 codes (one 16-byte chunk) -> 8 words of int8 (block 0 in q[0..3],
+// block 1 in q[4..7]).
+__device__ __forceinline__ void decode_chunk(const uint4& v, uint32_t (&q)[8]) {
+  q[0] = e2m1x4_to_s8x2(v.x & 0xFFFFu);
+  q[1] = e2m1x4_to_s8x2(v.x >> 16);
+  q[2] = e2m1x4_to_s8x2(v.y & 0xFFFFu);
+  q[3] = e2m1x4_to_s8x2(v.y >> 16);
+  q[4] = e2m1x4_to_s8x2(v.z & 0xFFFFu);
+  q[5] = e2m1x4_to_s8x2(v.z >> 16);
+  q[6] = e2m1x4_to_s8x2(v.w & 0xFFFFu);
+  q[7] = e2m1x4_to_s8x2(v.w >> 16);
+}
+
+// Byte offset of row r's scale tile base in the blocked layout (chunk 0).
+__device__ __forceinline__ int gemv_sf_row_offset(int r, int kt) {
+  return (r >> 7) * kt * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+
+__device__ __forceinline__ float gemv_bias(const GemvParams& p, int n) {
+  if (p.bias_kind == 1)
+    return __uint_as_float(uint32_t(__ldg(static_cast<const unsigned short*>(p.bias) + n)) << 16);
+  const uint16_t c = __ldg(static_cast<const uint8_t*>(p.bias) + n);
+  return __fmul_rn(e4m3x2_to_float2(uint16_t(c | (c << 8))).x, __ldg(p.bias_scale));
+}
+
+// TT: tokens the instantiation holds (1, 2 or 4); p.T <= TT.  Grid: one
+// warp per pair of weight rows, 4 warps per CTA.
+template <int EPI, int TT>
+__global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) {
+  constexpr int kUnroll = 4;
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (pair * 2 >= p.N) return;  // warp-uniform
+  const int n0 = pair * 2;
+  const int kh = p.K / 2;
+  const int nchunks = p.K / 32;
+  const int kt = p.K / 64;
+  const uint4* w0 = reinterpret_cast<const uint4*>(p.W + int64_t(n0) * kh);
+  const uint4* w1 = reinterpret_cast<const uint4*>(p.W + int64_t(n0 + 1) * kh);
+  const int sw0 = gemv_sf_row_offset(n0, kt);
+  const int sw1 = gemv_sf_row_offset(n0 + 1, kt);
+  float acc[2][TT];
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
+
+  for (int c0 = lane; c0 < nchunks; c0 += 32 * kUnroll) {
+    // The weight stream of kUnroll chunks first (read once: evict-first).
+    uint4 wv[kUnroll][2];
+    uint16_t ws[kUnroll][2];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nchunks) {
+        const int so = (c >> 1) * 512 + (c & 1) * 2;
+        wv[u][0] = __ldcs(w0 + c);
+        wv[u][1] = __ldcs(w1 + c);
+        ws[u][0] = __ldg(reinterpret_cast<const unsigned short*>(p.sfW + sw0 + so));
+        ws[u][1] = __ldg(reinterpret_cast<const unsigned short*>(p.sfW + sw1 + so));
+      } else {
+        wv[u][0] = wv[u][1] = make_uint4(0u, 0u, 0u, 0u);
+        ws[u][0] = ws[u][1] = 0;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nchunks) break;
+      const int so = (c >> 1) * 512 + (c & 1) * 2;
+      uint32_t wq[2][8];
+      decode_chunk(wv[u][0], wq[0]);
+      decode_chunk(wv[u][1], wq[1]);
+      const float2 sw[2] = {e4m3x2_to_float2(ws[u][0]), e4m3x2_to_float2(ws[u][1])};
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        if (t >= p.T) break;
+        const uint4 av = __ldg(reinterpret_cast<const uint4*>(p.A + int64_t(t) * kh) + c);
+        const float2 sa = e4m3x2_to_float2(__ldg(reinterpret_cast<const unsigned short*>(
+            p.sfA + gemv_sf_row_offset(t, kt) + so)));
+        uint32_t aq[8];
+        decode_chunk(av, aq);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          int d0 = __dp4a(int(aq[0]), int(wq[r][0]), 0);
+          d0 = __dp4a(int(aq[1]), int(wq[r][1]), d0);
+          d0 = __dp4a(int(aq[2]), int(wq[r][2]), d0);
+          d0 = __dp4a(int(aq[3]), int(wq[r][3]), d0);
+          int d1 = __dp4a(int(aq[4]), int(wq[r][4]), 0);
+          d1 = __dp4a(int(aq[5]), int(wq[r][5]), d1);
+          d1 = __dp4a(int(aq[6]), int(wq[r][6]), d1);
+          d1 = __dp4a(int(aq[7]), int(wq[r][7]), d1);
+          acc[r][t] = fmaf(float(d0), sa.x * sw[r].x, acc[r][t]);
+          acc[r][t] = fmaf(float(d1), sa.y * sw[r].y, acc[r][t]);
+        }
+      }
+    }
+  }
+
+  // Sum over the lanes (every lane ends with the totals).
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
+
+  const float s = __ldg(p.gA) * __ldg(p.gW);
+  if constexpr (EPI == SPG_EPI_SWIGLU) {
+    // rows n0 (gate) and n0 + 1 (up) give output column n0 / 2
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      if (lane == t && t < p.T) {
+        float gate = (acc[0][t] * 0.25f) * s;
+        float up = (acc[1][t] * 0.25f) * s;
+        if (p.bias_kind) {
+          gate += gemv_bias(p, n0);
+          up += gemv_bias(p, n0 + 1);
+        }
+        const float o = __fdividef(gate, 1.f + __expf(-gate)) * up;
+        p.Y[int64_t(t) * p.n_out + pair] = __float2bfloat16_rn(o);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        if (lane == r * TT + t && t < p.T) {
+          const int n = n0 + r;
+          float v = (acc[r][t] * 0.25f) * s;
+          if (p.bias_kind) v += gemv_bias(p, n);
+          if constexpr (EPI == SPG_EPI_ADD)
+            v += __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(
+                                                    p.residual) +
+                                                int64_t(t) * p.N + n))
+                                 << 16);
+          p.Y[int64_t(t) * p.n_out + n] = __float2bfloat16_rn(v);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace spg

@@ -228,6 +228,29 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
                    (add ? 4 * (r.block_n / 32) * 2048 : 0) + 256;
     return r;
   }
+  // NVFP4 at decode-sized T: the CUDA-core GEMV (variant 4; two weight rows
+  // per warp, 4 warps per CTA; no workspace).  It is bound by its decode
+  // arithmetic, so it is the default only where it measured faster than
+  // the tile routes on GB300: T <= 2 with N <= 16384 (N = 5120, K = 17408:
+  // 26.6 / 34.8 us at T = 1 / 2 against 41.0 / 36.9 for the best tile; the
+  // 34816-wide SwiGLU and T = 4 ran faster tiled).  SPG_FORCE_VARIANT=gemv
+  // takes it for any T <= 4; any other forced variant disables it.
+  const bool gemv_forced = forced_name && std::strcmp(forced_name, "gemv") == 0;
+  if (kind == SPG_KIND_NVFP4 && nb == 1 && T >= 1 &&
+      (gemv_forced ? T <= 4 : (!forced_name && T <= 2 && N <= 16384))) {
+    r.block_m = 1;
+    r.block_n = 2;
+    r.block_k = 32;
+    r.stages = 0;
+    r.acc_buffers = 0;
+    r.variant = 4;
+    r.tiles = N / 2;
+    r.grid = static_cast<int>((N / 2 + 3) / 4);
+    r.split_n = 1;
+    r.split_k = 1;
+    r.smem_bytes = 0;
+    return r;
+  }
   if (kind == SPG_KIND_NVFP4) {
     // Two-SM 256x256 pair tile (optionally with a K split of its last
     // partial wave), or the one-CTA 128x128 tile when its waves are cheaper
