@@ -11,7 +11,20 @@ namespace {
 template <int EPI, int TT>
 spg_status launch_gemv(const GemvParams& p, cudaStream_t s) {
   const int grid = (p.N / 2 + 3) / 4;  // one warp per weight-row pair, 4 per CTA
-  gemv_nvfp4_kernel<EPI, TT><<<grid, 128, 0, s>>>(p);
+  const int64_t smem = gemv_smem_bytes(TT, p.K);  // <= 200 KB (the route checks)
+  auto kern = gemv_nvfp4_kernel<EPI, TT>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024),
+                    "cudaFuncSetAttribute") != SPG_OK)
+      return SPG_ERR_CUDA;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  kern<<<grid, 128, static_cast<size_t>(smem), s>>>(p);
   return launch_status();
 }
 

@@ -7,8 +7,9 @@
 // two 16-element scale blocks), four chunks in flight per lane.
 //
 // Arithmetic: an E2M1 code becomes an int8 holding twice its value (a
-// 16-entry table applied to four codes at a time with byte permutes), so a
-// block's dot product sum_i (2 a_i)(2 w_i) is an exact integer (dp4a).  It
+// 16-entry table applied to four codes at a time with byte permutes; the
+// activations once per CTA into shared memory, the weights as they stream),
+// so a block's dot product sum_i (2 a_i)(2 w_i) is an exact integer (dp4a).  It
 // is multiplied by the product of the two blocks' E4M3 scales (exact in
 // fp32) and accumulated in fp32; the lanes' sums are added across the warp
 // and scaled by 1/4.  The epilogue then applies gA * gW, the bias, and the
@@ -79,18 +80,41 @@ __device__ __forceinline__ float gemv_bias(const GemvParams& p, int n) {
   return __fmul_rn(e4m3x2_to_float2(uint16_t(c | (c << 8))).x, __ldg(p.bias_scale));
 }
 
+// Shared-memory bytes of the decoded activations of one CTA: per token two
+// planes of K/32 16-byte words (the int8 of each chunk's two blocks) and
+// K/32 float2 (the two blocks' scales).
+__host__ __device__ constexpr int64_t gemv_smem_bytes(int tt, int64_t K) {
+  return int64_t(tt) * (K / 32) * 40;
+}
+
 // TT: tokens the instantiation holds (1, 2 or 4); p.T <= TT.  Grid: one
-// warp per pair of weight rows, 4 warps per CTA.
+// warp per pair of weight rows, 4 warps per CTA.  The CTA first decodes the
+// activations once into shared memory (they are read by every row).
 template <int EPI, int TT>
 __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) {
   constexpr int kUnroll = 4;
+  extern __shared__ uint4 gemv_smem[];
   const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (pair * 2 >= p.N) return;  // warp-uniform
-  const int n0 = pair * 2;
   const int kh = p.K / 2;
   const int nchunks = p.K / 32;
   const int kt = p.K / 64;
+  uint4* aq_s = gemv_smem;  // [TT][2][nchunks]
+  float2* sa_s = reinterpret_cast<float2*>(gemv_smem + 2 * TT * nchunks);  // [TT][nchunks]
+  for (int i = threadIdx.x; i < p.T * nchunks; i += blockDim.x) {
+    const int t = i / nchunks;
+    const int c = i - t * nchunks;
+    uint32_t q[8];
+    decode_chunk(__ldg(reinterpret_cast<const uint4*>(p.A + int64_t(t) * kh) + c), q);
+    aq_s[(t * 2) * nchunks + c] = make_uint4(q[0], q[1], q[2], q[3]);
+    aq_s[(t * 2 + 1) * nchunks + c] = make_uint4(q[4], q[5], q[6], q[7]);
+    sa_s[t * nchunks + c] = e4m3x2_to_float2(__ldg(reinterpret_cast<const unsigned short*>(
+        p.sfA + gemv_sf_row_offset(t, kt) + (c >> 1) * 512 + (c & 1) * 2)));
+  }
+  __syncthreads();
+
+  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (pair * 2 >= p.N) return;  // warp-uniform, after the CTA's only barrier
+  const int n0 = pair * 2;
   const uint4* w0 = reinterpret_cast<const uint4*>(p.W + int64_t(n0) * kh);
   const uint4* w1 = reinterpret_cast<const uint4*>(p.W + int64_t(n0 + 1) * kh);
   const int sw0 = gemv_sf_row_offset(n0, kt);
@@ -123,7 +147,6 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
     for (int u = 0; u < kUnroll; ++u) {
       const int c = c0 + 32 * u;
       if (c >= nchunks) break;
-      const int so = (c >> 1) * 512 + (c & 1) * 2;
       uint32_t wq[2][8];
       decode_chunk(wv[u][0], wq[0]);
       decode_chunk(wv[u][1], wq[1]);
@@ -131,21 +154,19 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
         if (t >= p.T) break;
-        const uint4 av = __ldg(reinterpret_cast<const uint4*>(p.A + int64_t(t) * kh) + c);
-        const float2 sa = e4m3x2_to_float2(__ldg(reinterpret_cast<const unsigned short*>(
-            p.sfA + gemv_sf_row_offset(t, kt) + so)));
-        uint32_t aq[8];
-        decode_chunk(av, aq);
+        const uint4 a0 = aq_s[(t * 2) * nchunks + c];
+        const uint4 a1 = aq_s[(t * 2 + 1) * nchunks + c];
+        const float2 sa = sa_s[t * nchunks + c];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          int d0 = __dp4a(int(aq[0]), int(wq[r][0]), 0);
-          d0 = __dp4a(int(aq[1]), int(wq[r][1]), d0);
-          d0 = __dp4a(int(aq[2]), int(wq[r][2]), d0);
-          d0 = __dp4a(int(aq[3]), int(wq[r][3]), d0);
-          int d1 = __dp4a(int(aq[4]), int(wq[r][4]), 0);
-          d1 = __dp4a(int(aq[5]), int(wq[r][5]), d1);
-          d1 = __dp4a(int(aq[6]), int(wq[r][6]), d1);
-          d1 = __dp4a(int(aq[7]), int(wq[r][7]), d1);
+          int d0 = __dp4a(int(a0.x), int(wq[r][0]), 0);
+          d0 = __dp4a(int(a0.y), int(wq[r][1]), d0);
+          d0 = __dp4a(int(a0.z), int(wq[r][2]), d0);
+          d0 = __dp4a(int(a0.w), int(wq[r][3]), d0);
+          int d1 = __dp4a(int(a1.x), int(wq[r][4]), 0);
+          d1 = __dp4a(int(a1.y), int(wq[r][5]), d1);
+          d1 = __dp4a(int(a1.z), int(wq[r][6]), d1);
+          d1 = __dp4a(int(a1.w), int(wq[r][7]), d1);
           acc[r][t] = fmaf(float(d0), sa.x * sw[r].x, acc[r][t]);
           acc[r][t] = fmaf(float(d1), sa.y * sw[r].y, acc[r][t]);
         }

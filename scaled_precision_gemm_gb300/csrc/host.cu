@@ -228,16 +228,19 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
                    (add ? 4 * (r.block_n / 32) * 2048 : 0) + 256;
     return r;
   }
-  // NVFP4 at decode-sized T: the CUDA-core GEMV (variant 4; two weight rows
-  // per warp, 4 warps per CTA; no workspace).  It is bound by its decode
-  // arithmetic, so it is the default only where it measured faster than
-  // the tile routes on GB300: T <= 2 with N <= 16384 (N = 5120, K = 17408:
-  // 26.6 / 34.8 us at T = 1 / 2 against 41.0 / 36.9 for the best tile; the
-  // 34816-wide SwiGLU and T = 4 ran faster tiled).  SPG_FORCE_VARIANT=gemv
-  // takes it for any T <= 4; any other forced variant disables it.
-  const bool gemv_forced = forced_name && std::strcmp(forced_name, "gemv") == 0;
-  if (kind == SPG_KIND_NVFP4 && nb == 1 && T >= 1 &&
-      (gemv_forced ? T <= 4 : (!forced_name && T <= 2 && N <= 16384))) {
+  // NVFP4 at decode-sized T (1-4 tokens): the CUDA-core GEMV (variant 4;
+  // two weight rows per warp, 4 warps per CTA; no workspace).  Measured on
+  // GB300 against the best tile route: linear_add N = 5120, K = 17408:
+  // 24.6 / 30.7 / 36.9 us at T = 1 / 2 / 4 against 41.0 / 36.9 / 38.9;
+  // K = 6144: 14.3 / 14.3 / 20.5 against 20.5; the 34816-wide SwiGLU ties
+  // (36.9-38.9 us).  SPG_FORCE_VARIANT=gemv pins it, any other forced
+  // variant disables it.  Its CTAs hold the decoded activations in shared
+  // memory (40 bytes per token slot and 32 K elements; 1, 2 or 4 slots), so
+  // K is bounded.
+  const int64_t gemv_tt = T == 1 ? 1 : (T == 2 ? 2 : 4);
+  if (kind == SPG_KIND_NVFP4 && nb == 1 && T >= 1 && T <= 4 &&
+      gemv_tt * (K / 32) * 40 <= 200 * 1024 &&
+      (!forced_name || std::strcmp(forced_name, "gemv") == 0)) {
     r.block_m = 1;
     r.block_n = 2;
     r.block_k = 32;
@@ -248,7 +251,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     r.grid = static_cast<int>((N / 2 + 3) / 4);
     r.split_n = 1;
     r.split_k = 1;
-    r.smem_bytes = 0;
+    r.smem_bytes = static_cast<int32_t>(gemv_tt * (K / 32) * 40);
     return r;
   }
   if (kind == SPG_KIND_NVFP4) {

@@ -109,20 +109,21 @@ def test_route_selector_gemv(lib, monkeypatch):
     T > 4 does not."""
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
     monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
-    for T in (1, 2):
+    for T, slots in [(1, 1), (2, 2), (3, 4), (4, 4)]:
         for epi in ("linear", "add", "swiglu"):
             r = spg.select_route("nvfp4", T, 5120, 17408, epi, workspace=True)
             assert r["variant"] == 4 and r["block_n"] == 2 and r["grid"] == 640
-            assert r["split_k"] == 1 and r["workspace_bytes"] == 0 and r["smem_bytes"] == 0
+            assert r["split_k"] == 1 and r["workspace_bytes"] == 0
+            assert r["smem_bytes"] == slots * (17408 // 32) * 40  # decoded activations
     assert spg.gemm_workspace_bytes("nvfp4", 1, 5120, 17408, "add") == 0
-    # tiled where the GEMV measured slower: T > 2, or the 34816-wide SwiGLU
-    assert spg.select_route("nvfp4", 3, 5120, 17408, "add")["variant"] != 4
-    assert spg.select_route("nvfp4", 1, 34816, 5120, "swiglu")["variant"] != 4
+    assert spg.select_route("nvfp4", 1, 34816, 5120, "swiglu")["variant"] == 4
     assert spg.select_route("fp8_rowscaled", 1, 5120, 17408, "add")["variant"] != 4
     monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
     assert spg.select_route("nvfp4", 1, 5120, 17408, "add")["variant"] == 3
     monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv")
-    assert spg.select_route("nvfp4", 4, 34816, 5120, "swiglu")["variant"] == 4
+    # the decoded activations must fit the CTA's shared memory
+    assert spg.select_route("nvfp4", 4, 256, 40960, "add")["variant"] == 4
+    assert spg.select_route("nvfp4", 4, 256, 41216, "add")["variant"] != 4
     assert spg.select_route("nvfp4", 5, 5120, 17408, "add")["variant"] != 4
 
 

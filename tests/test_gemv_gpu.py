@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture
 def gemv_route(monkeypatch):
-    """The GEMV pinned (the default takes it only at T <= 2, N <= 16384)."""
+    """The GEMV pinned (the default route for T <= 4 as well)."""
     monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv")
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
 
