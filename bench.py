@@ -5,9 +5,9 @@ T in {1024, 4096, 8192} for the two weight shapes (K=17408, N=5120) and
 (K=6144, N=5120).  For each of the six (T, K) cases a step quantizes the bf16
 activations to E4M3 codes with per-row scales and runs the row-scaled GEMM
 with the fused bf16 residual add.  Weights are quantized once, outside the
-timed region, as a deployment does offline.  L2 is flushed (a 512 MB write)
-before every case, outside the CUDA-event brackets; the reported time is the
-sum of the bracketed segments.
+timed region, as a deployment does offline.  L2 is flushed (a 512 MB write,
+read back) before every case, outside the CUDA-event brackets; the reported
+time is the sum of the bracketed segments.
 
 The GEMMs go through the library's workspace entry points (a workspace of
 spg_gemm_workspace_bytes per case, allocated once), so the route may split
@@ -19,8 +19,10 @@ and its fraction of the dense FP8 tensor peak.
 Other workloads (--workload): fp8_swiglu (T in {1024, 4096}, K=5120,
 N=34816 and the plain-linear widths 14336/16384/34816), nvfp4 (linear_add
 and linear_swiglu at T in {256, 1024, 4096, 8192}), fp8_tensor (the
-per-tensor training shapes).  ``--impl reference`` times the CPU oracle on
-a bounded sample of the same workload.
+per-tensor training shapes), decode (linear_add at narrow T: FP8 T in {1,
+16, 64, 128}, NVFP4 T in {1, 2, 4}; its roofline is the HBM copy peak).
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -75,6 +77,15 @@ def workload_cases(name):
             cases += [dict(kind="nvfp4", T=T, K=17408, N=5120, epi="add"),
                       dict(kind="nvfp4", T=T, K=6144, N=5120, epi="add"),
                       dict(kind="nvfp4", T=T, K=5120, N=34816, epi="swiglu")]
+        return cases
+    if name == "decode":
+        # Narrow T (decode and small batches) at the linear_add widths: the
+        # weights stream once, so these are HBM-bound (swapped FP8 tile with
+        # the K split, the NVFP4 GEMV at T <= 4).
+        cases = [dict(kind="fp8", T=T, K=K, N=5120, epi="add", w_std=0.02)
+                 for T in (1, 16, 64, 128) for K in (17408, 6144)]
+        cases += [dict(kind="nvfp4", T=T, K=K, N=5120, epi="add")
+                  for T in (1, 2, 4) for K in (17408, 6144)]
         return cases
     if name == "fp8_tensor":
         return [dict(kind="tensor", layout=l, M=M, N=N, K=K, batch=b) for (l, M, N, K, b) in [
@@ -284,6 +295,7 @@ def run_gpu(args):
 
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_words = flush.view(torch.float32)
     scratch = torch.empty(4, dtype=torch.float32, device=dev)
 
     # Per case: preallocated buffers, quant(x, res) (activation quantization of
@@ -372,7 +384,11 @@ def run_gpu(args):
         """Run every case once; returns (segment events, gemm-only events, launches)."""
         seg, gem, launches = [], [], 0
         for k in prepared:
-            flush.zero_()                                  # L2 flush, outside the brackets
+            # L2 flush, outside the brackets: write a buffer larger than L2,
+            # then read it back so the lines left behind are clean (the GEMM
+            # is not charged for writing the flush's dirty lines back).
+            flush.zero_()
+            flush_words.sum()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e2 = torch.cuda.Event(enable_timing=True)
@@ -445,11 +461,26 @@ def run_gpu(args):
     dom_peak = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
     achieved = case_flops(dc) / (dom_ms * 1e-3) / 1e12
     traffic = recorded_traffic(case_name(dc))
+    if args.workload == "decode":
+        # weight-streaming cases: bytes against the HBM copy peak
+        ach_gbs = case_bytes(dc) / (dom_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": case_name(dc), "achieved": round(ach_gbs, 1),
+                    "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
+                    "frac": round(ach_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                    "peak_source": f"{peaks['source']} HBM copy {peaks['hbm_gbs']} GB/s",
+                    "algorithmic_bytes": case_bytes(dc)}
+    else:
+        roofline = {"bound": "tensor", "kernel": case_name(dc), "achieved": round(achieved, 1),
+                    "peak": round(dom_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / dom_peak, 4), "traffic": traffic,
+                    "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
+                                   f"nominal {dtype} ratio {NOMINAL_RATIO[dtype]}",
+                    "algorithmic_bytes": case_bytes(dc)}
 
     # ---------------- e2e: host buffers through the public API
     e2e = None if args.no_e2e else run_e2e(args, spg, torch, dev, prepared, inputs)
 
-    dtype_line = "e2m1" if args.workload == "nvfp4" else "e4m3"
+    dtype_line = {"nvfp4": "e2m1", "decode": "e4m3/e2m1"}.get(args.workload, "e4m3")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -458,18 +489,14 @@ def run_gpu(args):
         "config": {"workload": args.workload,
                    "cases": [case_name(k.c) for k in prepared],
                    "step": "activation quantization + GEMM with fused epilogue per case",
-                   "l2": "flushed (512 MB write) before every case, outside the timed brackets",
+                   "l2": "flushed (512 MB write, then read back so no dirty lines remain) "
+                         "before every case, outside the timed brackets",
                    "api": "workspace entry points (workspace sized by spg_gemm_workspace_bytes, "
                           "allocated once; the route may split the last partial wave along K)",
                    "launch": "CUDA graph replay per case" if use_graphs else "eager",
                    "inputs": "bf16 N(0,1) activations/residual, N(0,0.02) weights (splitmix64 "
                              "Box-Muller, seeds 0/1/2); weights quantized once offline"},
-        "roofline": {"bound": "tensor", "kernel": case_name(dc), "achieved": round(achieved, 1),
-                     "peak": round(dom_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(achieved / dom_peak, 4), "traffic": traffic,
-                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
-                                    f"nominal {dtype} ratio {NOMINAL_RATIO[dtype]}",
-                     "algorithmic_bytes": case_bytes(dc)},
+        "roofline": roofline,
         "per_case": per_case,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -668,7 +695,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="spg", choices=["spg", "reference"])
     ap.add_argument("--workload", default="fp8_linear_add",
-                    choices=["fp8_linear_add", "fp8_swiglu", "nvfp4", "fp8_tensor"])
+                    choices=["fp8_linear_add", "fp8_swiglu", "nvfp4", "fp8_tensor", "decode"])
     ap.add_argument("--cpu-rows", type=int, default=32,
                     help="activation rows per case in the CPU-oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=4,
