@@ -61,6 +61,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
+# ------------------------------------------------------------ ranks
+def job_throughput(ms_local, flops_per_rank, world, dist=None, device=None):
+    """Whole-job throughput of a replica run (weak scaling): every rank does
+    `flops_per_rank` of work and the job lasts as long as its slowest rank.
+    Returns (the max over ranks of `ms_local`, all ranks' TFLOP/s)."""
+    ms = float(ms_local)
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ workloads
 def workload_cases(name):
     if name == "fp8_linear_add":
@@ -430,13 +444,8 @@ def run_gpu(args):
     clk = clocks.stop()
 
     step_ms = [sum(a.elapsed_time(b) for a, b in s) for s in all_seg]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     flops_step = sum(case_flops(k.c) for k in prepared)
-    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    total_ms, value = job_throughput(sum(step_ms), flops_step * args.steps, world, dist, dev)
 
     peaks = load_peaks()
     per_case = []
@@ -478,7 +487,7 @@ def run_gpu(args):
                     "algorithmic_bytes": case_bytes(dc)}
 
     # ---------------- e2e: host buffers through the public API
-    e2e = None if args.no_e2e else run_e2e(args, spg, torch, dev, prepared, inputs)
+    e2e = None if args.no_e2e else run_e2e(args, spg, torch, dev, prepared, inputs, dist, world)
 
     dtype_line = {"nvfp4": "e2m1", "decode": "e4m3/e2m1"}.get(args.workload, "e4m3")
     line = {
@@ -511,7 +520,7 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, spg, torch, dev, prepared, inputs):
+def run_e2e(args, spg, torch, dev, prepared, inputs, dist=None, world=1):
     """Same workload through the public API with HOST buffers: per case the
     bf16 activations (and residual) are copied from pinned host memory, the
     step runs on those device copies, and the bf16 output is copied back to
@@ -580,12 +589,12 @@ def run_e2e(args, spg, torch, dev, prepared, inputs):
         compute.wait_stream(st)
     e1.record(compute)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
     wall_ms = (time.perf_counter() - t0) * 1e3 / reps
     for k in prepared:          # restore the device-resident inputs
         k.quant(k.x, k.res)
     flops = sum(case_flops(k.c) for k in prepared)
-    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    ms, value = job_throughput(e0.elapsed_time(e1) / reps, flops, world, dist, dev)
+    return {"value": round(value, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall_ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "copies": "two copy streams overlapping compute (pinned host buffers)"}
