@@ -1,0 +1,75 @@
+"""Route-selector invariants over a sweep of shapes (host only): what the
+kernels rely on when the route is launched.
+
+* a pair route launches an even grid of at most 2 x 76 CTAs, a one-CTA route
+  at most 152, the GEMV one CTA per 4 weight-row pairs;
+* dynamic shared memory stays within the 232,448-byte opt-in limit (the
+  GEMV within its 200 KB bound);
+* a K split has 2-4 pieces, none empty, each at least 4 K blocks, and the
+  workspace query returns exactly the plan's bytes (the per-tensor GEMM:
+  at least, it covers both B layouts); plain routes never split K;
+* the swapped tile is FP8 row-scaled, linear / linear_add, T <= 128, one
+  problem; the GEMV is NVFP4 with T <= 4.
+"""
+import itertools
+
+import pytest
+
+import scaled_precision_gemm_gb300 as spg
+
+SMEM_MAX = 232448
+PAIRS = 76
+
+
+def nkb(kind, K):
+    return (K // 2 + 127) // 128 if kind == "nvfp4" else (K + 127) // 128
+
+
+SHAPES = list(itertools.product([1, 3, 16, 64, 100, 128, 129, 256, 1000, 1024, 4096, 8192],
+                                [128, 5120, 6144, 17408, 34816],
+                                [256, 1024, 5120, 6144, 17408]))
+
+
+@pytest.fixture(autouse=True)
+def _no_pins(monkeypatch):
+    monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+    monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
+
+
+@pytest.mark.parametrize("kind", ["fp8_rowscaled", "nvfp4", "fp8_tensor"])
+@pytest.mark.parametrize("epi", ["linear", "add", "swiglu"])
+def test_route_invariants(kind, epi):
+    if kind == "fp8_tensor" and epi != "linear":
+        pytest.skip("the per-tensor GEMM has the linear epilogue only")
+    for T, N, K in SHAPES:
+        if kind == "nvfp4" and K % 256:
+            continue
+        for ws in (False, True):
+            r = spg.select_route(kind, T, N, K, epi, workspace=ws)
+            tag = (kind, epi, T, N, K, ws, r)
+            assert r["grid"] >= 1, tag
+            if r["variant"] == 4 and kind == "nvfp4":
+                assert T <= 4 and r["grid"] == (N // 2 + 3) // 4, tag
+                assert r["smem_bytes"] <= 200 * 1024 and r["split_k"] == 1, tag
+                continue
+            assert r["smem_bytes"] <= SMEM_MAX, tag
+            if r["block_m"] == 256:
+                assert r["grid"] % 2 == 0 and r["grid"] <= 2 * PAIRS, tag
+            else:
+                assert r["grid"] <= 2 * PAIRS, tag
+            if r["swap_ab"]:
+                assert kind == "fp8_rowscaled" and epi != "swiglu" and T <= 128, tag
+                assert r["block_n"] == (64 if T <= 64 else 128), tag
+            if not ws:
+                assert r["split_k"] == 1 and r["workspace_bytes"] == 0, tag
+            if r["split_k"] > 1:
+                s, n = r["split_k"], nkb(kind, K)
+                kbps = -(-n // s)
+                assert 2 <= s <= 4 and kbps >= 4 and (s - 1) * kbps < n, tag
+                assert r["split_n"] == 1 and r["workspace_bytes"] > 0, tag
+            if ws:
+                need = spg.gemm_workspace_bytes(kind, T, N, K, epi)
+                if kind == "fp8_tensor":
+                    assert need >= r["workspace_bytes"], tag
+                else:
+                    assert need == r["workspace_bytes"], tag
