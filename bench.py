@@ -177,7 +177,9 @@ class ClockSampler:
         self.nvml = None
         self.handle = None
         self.device_index = device_index
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks.csv")
+        # optional per-sample record of the SM clock (the JSON line carries
+        # the summary either way)
+        self.path = os.environ.get("SPG_CLOCKS_CSV") or None
         try:
             self._open_nvml()
         except Exception:
@@ -237,12 +239,13 @@ class ClockSampler:
         self.thread.join()
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
-        try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            with open(self.path, "w") as f:
-                f.write("sm_mhz\n" + "\n".join(str(v) for v in self.samples) + "\n")
-        except OSError:
-            pass
+        if self.path:
+            try:
+                os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
+                with open(self.path, "w") as f:
+                    f.write("sm_mhz\n" + "\n".join(str(v) for v in self.samples) + "\n")
+            except OSError:
+                pass
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples),
                 "source": "NVML, 2 ms polling during the timed steps"}
