@@ -1,28 +1,33 @@
 """Benchmark of the scaled-precision GEMM hot path on one GB300.
 
-Default workload (one "step"): the FP8 E4M3 row-scaled linear_add layer at
-T in {1024, 4096, 8192} for the two weight shapes (K=17408, N=5120) and
-(K=6144, N=5120).  For each of the six (T, K) cases a step quantizes the bf16
-activations to E4M3 codes with per-row scales and runs the row-scaled GEMM
-with the fused bf16 residual add.  Weights are quantized once, outside the
-timed region, as a deployment does offline.  L2 is flushed (a 512 MB write,
-read back) before every case, outside the CUDA-event brackets; the reported
-time is the sum of the bracketed segments.
+Default workload ``prefill`` (one "step"): the FP8 E4M3 row-scaled
+linear_add layer at T in {1024, 4096, 8192} for the two weight shapes
+(K=17408, N=5120) and (K=6144, N=5120), and the NVFP4 block-scaled layers at
+the same T: linear_add at both weight shapes and linear_swiglu at (K=5120,
+N=34816).  For each of the fifteen cases a step quantizes the bf16
+activations (FP8: E4M3 codes with per-row scales; NVFP4: the global scale,
+then E2M1 codes with blocked E4M3 scales) and runs the GEMM with its fused
+epilogue (bf16 residual add, or SwiGLU over interleaved gate/up columns).
+Weights are quantized once, outside the timed region, as a deployment does
+offline.  L2 is flushed (a 512 MB write, read back) before every case,
+outside the CUDA-event brackets; the reported time is the sum of the
+bracketed segments.
 
 The GEMMs go through the library's workspace entry points (a workspace of
 spg_gemm_workspace_bytes per case, allocated once), so the route may split
 the last partial wave along K where its cost model says that pays.
 
 Metric: TFLOP/s = sum(2 T N K) / step time, plus each case's GEMM-only rate
-and its fraction of the dense FP8 tensor peak.
+and its fraction of the dense tensor peak of its format (FP8, or FP4 for
+NVFP4), and the roofline of the longest GEMM of each format.
 
-Other workloads (--workload): fp8_swiglu (T in {1024, 4096}, K=5120,
-N=34816 and the plain-linear widths 14336/16384/34816), nvfp4 (linear_add
-and linear_swiglu at T in {256, 1024, 4096, 8192}), fp8_tensor (the
-per-tensor training shapes), decode (linear_add at narrow T: FP8 T in {1,
-16, 64, 128}, NVFP4 T in {1, 2, 4}; its roofline is the HBM copy peak).
-``--impl reference`` times the CPU oracle on a bounded sample of the same
-workload.
+Other workloads (--workload): fp8_linear_add (the six FP8 cases alone),
+fp8_swiglu (T in {1024, 4096}, K=5120, N=34816 and the plain-linear widths
+14336/16384/34816), nvfp4 (linear_add and linear_swiglu at T in {256, 1024,
+4096, 8192}), fp8_tensor (the per-tensor training shapes), decode
+(linear_add at narrow T: FP8 T in {1, 16, 64, 128}, NVFP4 T in {1, 2, 4};
+its roofline is the HBM copy peak).  ``--impl reference`` times the CPU
+oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -77,6 +82,16 @@ def job_throughput(ms_local, flops_per_rank, world, dist=None, device=None):
 
 # ------------------------------------------------------------ workloads
 def workload_cases(name):
+    if name == "prefill":
+        # The headline workload: FP8 row-scaled linear_add and NVFP4
+        # linear_add / linear_swiglu at the three prefill widths, so one step
+        # exercises both flavours of the metric.
+        cases = workload_cases("fp8_linear_add")
+        for T in (1024, 4096, 8192):
+            cases += [dict(kind="nvfp4", T=T, K=17408, N=5120, epi="add"),
+                      dict(kind="nvfp4", T=T, K=6144, N=5120, epi="add"),
+                      dict(kind="nvfp4", T=T, K=5120, N=34816, epi="swiglu")]
+        return cases
     if name == "fp8_linear_add":
         return [dict(kind="fp8", T=T, K=K, N=5120, epi="add", w_std=0.02)
                 for T in (1024, 4096, 8192) for K in (17408, 6144)]
@@ -465,34 +480,49 @@ def run_gpu(args):
                          "step_us": round(sms * 1e3, 2), "gemm_tflops": round(tf, 1),
                          "frac_of_peak": round(tf / peak, 4),
                          "gemm_gbs": round(case_bytes(c) / (gms * 1e-3) / 1e9, 1)})
-    # dominant kernel: the case with the longest GEMM
-    dom_i = max(range(len(per_case)), key=lambda i: per_case[i]["gemm_us"])
-    dc = prepared[dom_i].c
-    dtype = "fp4" if dc["kind"] == "nvfp4" else "fp8"
-    dom_ms = per_case[dom_i]["gemm_us"] * 1e-3
-    dom_peak = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
-    achieved = case_flops(dc) / (dom_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(case_name(dc))
-    if args.workload == "decode":
-        # weight-streaming cases: bytes against the HBM copy peak
-        ach_gbs = case_bytes(dc) / (dom_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": case_name(dc), "achieved": round(ach_gbs, 1),
+    # Dominant kernel: the case with the longest GEMM; the same figures for
+    # the longest GEMM of each flavour (FP8 against the FP8 peak, NVFP4
+    # against the FP4 peak).
+    def roofline_of(i):
+        dc = prepared[i].c
+        dtype = "fp4" if dc["kind"] == "nvfp4" else "fp8"
+        dom_ms = per_case[i]["gemm_us"] * 1e-3
+        traffic = recorded_traffic(case_name(dc))
+        if args.workload == "decode":
+            # weight-streaming cases: bytes against the HBM copy peak
+            ach_gbs = case_bytes(dc) / (dom_ms * 1e-3) / 1e9
+            return {"bound": "hbm", "kernel": case_name(dc), "achieved": round(ach_gbs, 1),
                     "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
                     "frac": round(ach_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
                     "peak_source": f"{peaks['source']} HBM copy {peaks['hbm_gbs']} GB/s",
                     "algorithmic_bytes": case_bytes(dc)}
-    else:
-        roofline = {"bound": "tensor", "kernel": case_name(dc), "achieved": round(achieved, 1),
-                    "peak": round(dom_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(achieved / dom_peak, 4), "traffic": traffic,
-                    "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
-                                   f"nominal {dtype} ratio {NOMINAL_RATIO[dtype]}",
-                    "algorithmic_bytes": case_bytes(dc)}
+        dom_peak = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
+        achieved = case_flops(dc) / (dom_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": case_name(dc), "achieved": round(achieved, 1),
+                "peak": round(dom_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / dom_peak, 4), "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
+                               f"nominal {dtype}:bf16 ratio {NOMINAL_RATIO[dtype]}",
+                "algorithmic_bytes": case_bytes(dc), "algorithmic_flops": case_flops(dc)}
+
+    dom_i = max(range(len(per_case)), key=lambda i: per_case[i]["gemm_us"])
+    roofline = roofline_of(dom_i)
+    by_flavour = {}
+    for flav, kinds in (("fp8", ("fp8", "tensor")), ("fp4", ("nvfp4",))):
+        idx = [i for i, k in enumerate(prepared) if k.c["kind"] in kinds]
+        if idx and args.workload != "decode":
+            r = roofline_of(max(idx, key=lambda i: per_case[i]["gemm_us"]))
+            fl = sum(case_flops(prepared[i].c) for i in idx)
+            us = sum(per_case[i]["gemm_us"] for i in idx)
+            r["all_cases_tflops"] = round(fl / (us * 1e-6) / 1e12, 1)
+            r["all_cases_frac"] = round(r["all_cases_tflops"] / r["peak"], 4)
+            by_flavour[flav] = r
 
     # ---------------- e2e: host buffers through the public API
     e2e = None if args.no_e2e else run_e2e(args, spg, torch, dev, prepared, inputs, dist, world)
 
-    dtype_line = {"nvfp4": "e2m1", "decode": "e4m3/e2m1"}.get(args.workload, "e4m3")
+    dtype_line = {"nvfp4": "e2m1", "decode": "e4m3/e2m1",
+                  "prefill": "e4m3/e2m1"}.get(args.workload, "e4m3")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -506,9 +536,11 @@ def run_gpu(args):
                    "api": "workspace entry points (workspace sized by spg_gemm_workspace_bytes, "
                           "allocated once; the route may split the last partial wave along K)",
                    "launch": "CUDA graph replay per case" if use_graphs else "eager",
-                   "inputs": "bf16 N(0,1) activations/residual, N(0,0.02) weights (splitmix64 "
+                   "inputs": "bf16 N(0,1) activations/residual; weights N(0,0.02) for FP8 "
+                             "linear_add, N(0,1) otherwise (splitmix64 "
                              "Box-Muller, seeds 0/1/2); weights quantized once offline"},
         "roofline": roofline,
+        "roofline_by_flavour": by_flavour,
         "per_case": per_case,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -706,8 +738,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="spg", choices=["spg", "reference"])
-    ap.add_argument("--workload", default="fp8_linear_add",
-                    choices=["fp8_linear_add", "fp8_swiglu", "nvfp4", "fp8_tensor", "decode"])
+    ap.add_argument("--workload", default="prefill",
+                    choices=["prefill", "fp8_linear_add", "fp8_swiglu", "nvfp4", "fp8_tensor",
+                             "decode"])
     ap.add_argument("--cpu-rows", type=int, default=32,
                     help="activation rows per case in the CPU-oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=4,
