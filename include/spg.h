@@ -111,11 +111,26 @@ SPG_API int spg_version(void);
 SPG_API void spg_set_wait_timeout_ns(uint64_t ns);
 
 /* Test hook for failure detection: while enabled, every launch of the
- * one-CTA GEMM kernels makes its epilogue wait on a barrier that nothing
- * arrives on, so that wait runs out after the bound set above, the kernel
- * records code 0x106 and every role drains and returns without a fault.
- * Host-side setting; not thread-safe against concurrent launches. */
+ * tile GEMM kernels (one-CTA and two-SM) makes its epilogue wait on a
+ * barrier that nothing arrives on, so that wait runs out after the bound set
+ * above, the kernel records code 0x106 and every role drains and returns
+ * without a fault (in a CTA pair the two producers first settle which of
+ * their copies are still landing).  Host-side setting; not thread-safe
+ * against concurrent launches. */
 SPG_API void spg_debug_inject_stall(int enable);
+
+/* Test hook: the route selector reads the environment variables
+ * SPG_FORCE_VARIANT (pin a kernel variant) and SPG_FORCE_TAIL (pin how the
+ * last partial wave is split: none | n | k) once, on its first call; this
+ * makes the next call read them again.  Host-side setting; not thread-safe
+ * against concurrent launches. */
+SPG_API void spg_debug_reload_env(void);
+
+/* Counts of tensor-map (TMA descriptor) cache hits and misses since the
+ * library was loaded.  Each GEMM call needs 3 to 6 descriptors; a descriptor
+ * encoded for the same base pointer, shape, strides, box and swizzle is
+ * reused.  Both pointers must be non-null (host memory). */
+SPG_API void spg_debug_tmap_cache_stats(uint64_t* hits, uint64_t* misses);
 
 /* Synchronizes `stream`, then reads and clears the library's device error
  * word.  Returns SPG_OK, SPG_ERR_TIMEOUT (a bounded wait ran out in some

@@ -73,6 +73,9 @@ def load_library():
             "spg_version": (i32, []),
             "spg_set_wait_timeout_ns": (None, [u64]),
             "spg_debug_inject_stall": (None, [i32]),
+            "spg_debug_reload_env": (None, []),
+            "spg_debug_tmap_cache_stats": (None, [ctypes.POINTER(ctypes.c_uint64),
+                                                  ctypes.POINTER(ctypes.c_uint64)]),
             "spg_last_device_error": (st, [vp]),
             "spg_last_device_error_code": (st, [vp, ctypes.POINTER(ctypes.c_uint32)]),
             "spg_quantize_fp8_rows": (st, [vp, i64, i64, vp, vp, vp]),
@@ -111,6 +114,29 @@ def load_library():
             f.argtypes = args
         _lib = lib
         return lib
+
+
+_FORCE_VARS = ("SPG_FORCE_VARIANT", "SPG_FORCE_TAIL")
+_forced_seen = None
+
+
+def _lib_for_call():
+    """The library, after telling it when the route-pinning variables changed
+    (it reads them once and caches them; tests pin routes by setting them)."""
+    global _forced_seen
+    lib = load_library()
+    cur = tuple(os.environ.get(v) for v in _FORCE_VARS)
+    if cur != _forced_seen:
+        lib.spg_debug_reload_env()
+        _forced_seen = cur
+    return lib
+
+
+def tmap_cache_stats():
+    """(hits, misses) of the library's tensor-map cache."""
+    h, m = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    load_library().spg_debug_tmap_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    return int(h.value), int(m.value)
 
 
 def status_string(s: int) -> str:
@@ -173,7 +199,8 @@ def select_route(kind, T, N, K, epilogue="linear", batch=1, workspace=False) -> 
     r = Route()
     k = KINDS[kind] if isinstance(kind, str) else int(kind)
     e = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
-    fn = load_library().spg_select_route_ws if workspace else load_library().spg_select_route
+    lib = _lib_for_call()
+    fn = lib.spg_select_route_ws if workspace else lib.spg_select_route
     _check(fn(k, T, N, K, e, batch, ctypes.byref(r)), "spg_select_route")
     return {f: getattr(r, f) for f, _ in Route._fields_}
 
@@ -182,7 +209,7 @@ def gemm_workspace_bytes(kind, T, N, K, epilogue="linear", batch=1) -> int:
     """Bytes of workspace that let the workspace entry points split K."""
     k = KINDS[kind] if isinstance(kind, str) else int(kind)
     e = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
-    return int(load_library().spg_gemm_workspace_bytes(k, T, N, K, e, batch))
+    return int(_lib_for_call().spg_gemm_workspace_bytes(k, T, N, K, e, batch))
 
 
 def gemm_workspace(kind, T, N, K, epilogue="linear", batch=1, device="cuda"):
@@ -340,17 +367,18 @@ def fp8_rowscaled_gemm(A, sa, W, sw, residual=None, epilogue="linear", out=None,
     out = torch.empty((T, n_out), dtype=torch.bfloat16, device=A.device) if out is None else out
     _need(out, "out", torch.bfloat16, 2)
     _check_bias(bias, bias_scale, N)
+    lib = _lib_for_call()
     res = _ptr(residual if e == 1 else None)
     if workspace is not None:
         wp, wn = _ws(workspace)
-        st = load_library().fp8_rowscaled_gemm_ws(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
+        st = lib.fp8_rowscaled_gemm_ws(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
                                                   _ptr(bias), _ptr(bias_scale), res, _ptr(out),
                                                   T, N, K, e, wp, wn, _stream(A))
     elif bias is None:
-        st = load_library().fp8_rowscaled_gemm(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), res,
+        st = lib.fp8_rowscaled_gemm(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), res,
                                                _ptr(out), T, N, K, e, _stream(A))
     else:
-        st = load_library().fp8_rowscaled_gemm_bias(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
+        st = lib.fp8_rowscaled_gemm_bias(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw),
                                                     _ptr(bias), _ptr(bias_scale), res, _ptr(out),
                                                     T, N, K, e, _stream(A))
     _check(st, "fp8_rowscaled_gemm")
@@ -380,17 +408,18 @@ def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=Non
     out = torch.empty((T, n_out), dtype=torch.bfloat16, device=A.device) if out is None else out
     _need(out, "out", torch.bfloat16, 2)
     _check_bias(bias, bias_scale, N)
+    lib = _lib_for_call()
     res = _ptr(residual if e == 1 else None)
     if workspace is not None:
         wp, wn = _ws(workspace)
-        st = load_library().nvfp4_gemm_ws(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW),
+        st = lib.nvfp4_gemm_ws(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW),
                                           _ptr(gW), _ptr(bias), _ptr(bias_scale), res, _ptr(out),
                                           T, N, K, e, wp, wn, _stream(A))
     elif bias is None:
-        st = load_library().nvfp4_gemm(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW),
+        st = lib.nvfp4_gemm(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW),
                                        res, _ptr(out), T, N, K, e, _stream(A))
     else:
-        st = load_library().nvfp4_gemm_bias(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW),
+        st = lib.nvfp4_gemm_bias(_ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW),
                                             _ptr(gW), _ptr(bias), _ptr(bias_scale), res,
                                             _ptr(out), T, N, K, e, _stream(A))
     _check(st, "nvfp4_gemm")
@@ -420,7 +449,7 @@ def fp8_tensor_gemm(layout: str, A, sA, B, sB, M, N, K, batch=1, strideA=None, s
     if out.numel() < (batch - 1) * strideC + M * N:
         raise ValueError("output buffer too small")
     _check_bias(bias, bias_scale, N)
-    lib = load_library()
+    lib = _lib_for_call()
     if workspace is not None:
         wp, wn = _ws(workspace)
         st = lib.fp8_tensor_gemm_ws(layout[0].encode(), layout[1].encode(), batch, _ptr(A),

@@ -48,7 +48,7 @@ struct Gemm2smCfg {
   // and 32-token chunk.
   static constexpr int kResBytes =
       (SWAP && EPI == SPG_EPI_ADD) ? kEpiWarps * (BN / 32) * 32 * 64 : 0;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes =
       1024 + STAGES * kStageBytes + kEpiBytes + kResBytes + kBarBytes;
   static constexpr int kThreads = 192;
@@ -62,7 +62,8 @@ struct Gemm2smCfg {
   static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert(2 * STAGES + 6 + (kResBytes ? kEpiWarps : 0) <= kBarBytes / 8,
+  // barriers, tmem slot + abort flag, residual barriers, stall barrier, PairExit
+  static_assert((2 * STAGES + 7 + kEpiWarps) * 8 + sizeof(PairExit) <= kBarBytes,
                 "barrier area too small");
 
   // kind::f8f6f4, E4M3 x E4M3 -> f32, M = 256 (pair), N = BN.
@@ -93,6 +94,8 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint64_t* res_bars = drain + 2;  // swapped linear_add: one per epilogue warp
+  uint64_t* stall = res_bars + Cfg::kEpiWarps;  // test hook: nothing arrives on it
+  PairExit* pexit = reinterpret_cast<PairExit*>(stall + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -112,6 +115,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(drain, 1);
     if constexpr (Cfg::kResBytes != 0)
       for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
+    mbar_init(stall, 1);
+    mbar_init(&pexit->bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -137,6 +142,7 @@ __global__ void __launch_bounds__(192, 1)
       int s = 0;
       uint32_t ph = 0;
       uint32_t issued = 0;
+      uint32_t tx[STAGES] = {};  // this CTA's copy bytes per ring slot (last use)
       bool ok = true;
       for (int item = pair; ok && item < p.total_items; item += num_pairs) {
         const WorkItem tc = work_item(item, p, BN);
@@ -166,6 +172,7 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_3d_pair(sb, &tmB, bar, nb0, kx, zb);
           else
             tma_load_3d_pair(sb, narrow ? &tmBnarrow : &tmB, bar, kx, nb0, zb);
+          tx[s] = Cfg::kABytes + b_bytes;
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -173,15 +180,13 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // The leader's full barriers count both CTAs' bytes: waiting on the
-      // last ones means no TMA write of the pair is still in flight.
-      if (rank == 0) {
-        const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
-        for (uint32_t i = 0; i < outstanding; ++i) {
-          const uint32_t idx = issued - 1 - i;
-          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
-        }
-      }
+      // The leader's full barriers count both CTAs' bytes: once the two
+      // producers' accounts are settled and the last stages have landed, no
+      // TMA write of the pair is in flight.
+      if (rank == 0)
+        pair_exit_drain<STAGES>(pexit, full, issued, tx, p);
+      else
+        pair_exit_publish<STAGES>(pexit, issued, tx);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer (leader)
@@ -235,6 +240,9 @@ __global__ void __launch_bounds__(192, 1)
       tc_commit_pair(drain);
       mbar_wait_drain(drain, 0, p.drain_ns, p.err);
     }
+  } else if (p.debug_stall && !mbar_wait(stall, 0, ctl, kErrInjectedStall)) {
+    // Test hook: the epilogue waited on a barrier nothing arrives on; the CTA
+    // has aborted and its other roles drain and return.
   } else {
     // -------------------------------------------------------------- epilogue
     auto arrive_fn = [&](int b) { mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0)); };

@@ -4,6 +4,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cstddef>
+
 #include "common.h"
 #include "ptx.cuh"
 
@@ -205,6 +207,79 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
       atomicCAS(err, 0u, kErrDrain);
       return false;
     }
+  }
+}
+
+// Drain-mode wait with a cluster-scope acquire (the phase is completed by a
+// release from the other CTA of the pair).
+__device__ __forceinline__ bool mbar_wait_drain_cluster(uint64_t* bar, uint32_t parity,
+                                                        uint64_t timeout_ns, unsigned int* err) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if ((i & 15u) == 15u && (globaltimer_ns() - t0 > timeout_ns || i > (1u << 30))) {
+      atomicCAS(err, 0u, kErrDrain);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------- pair exit
+// In the two-SM kernels both CTAs' operand copies complete on the leader's
+// full[] barriers, and the leader's producer posts the expected bytes of both
+// halves.  Normally both producers issue the same stages; after a time-out
+// they may stop after different numbers of stages, and then the leader alone
+// cannot tell which copies are still landing.  So at exit the peer's producer
+// publishes, in the leader's PairExit, how many stages it issued and the
+// bytes of its copies into each ring slot (its last use of each), and the
+// leader's producer (pair_exit_drain) settles every stage of the last ring's
+// worth that only one side issued -- the arrival and bytes of peer copies
+// the leader never announced, or the announced bytes of a peer half that was
+// never issued -- and waits (bounded) for every one of them.  After that no
+// copy of either CTA is in flight, and both CTAs pass the final cluster
+// barrier only after it.
+constexpr int kPairExitMaxStages = 12;
+struct PairExit {
+  uint64_t bar;        // leader: one arrival, released by the peer's producer
+  uint32_t issued;     // the peer's count of issued stages
+  uint32_t pad;
+  uint32_t bytes[kPairExitMaxStages];  // the peer's copy bytes per ring slot
+};
+
+// Peer CTA's producer: publish its issued count and per-slot bytes.
+template <int STAGES>
+__device__ __forceinline__ void pair_exit_publish(PairExit* px, uint32_t issued,
+                                                  const uint32_t (&bytes)[STAGES]) {
+  static_assert(STAGES <= kPairExitMaxStages, "PairExit holds at most 12 ring slots");
+  const uint32_t base = mapa_shared(smem_u32(px), 0);
+  st_cluster_u32(base + uint32_t(offsetof(PairExit, issued)), issued);
+#pragma unroll
+  for (int s = 0; s < STAGES; ++s)
+    st_cluster_u32(base + uint32_t(offsetof(PairExit, bytes)) + 4u * s, bytes[s]);
+  mbar_arrive_cluster(base + uint32_t(offsetof(PairExit, bar)));
+}
+
+// Leader CTA's producer: wait for the peer's account, settle the stages only
+// one side issued and wait for every stage still outstanding.  `bytes` are
+// the leader's own copy bytes per ring slot (the same as the peer's for a
+// stage both issue).
+template <int STAGES>
+__device__ __forceinline__ void pair_exit_drain(PairExit* px, uint64_t* full, uint32_t issued,
+                                                const uint32_t (&bytes)[STAGES],
+                                                const GemmParams& p) {
+  uint32_t peer = issued;
+  if (mbar_wait_drain_cluster(&px->bar, 0, p.drain_ns, p.err))
+    peer = *reinterpret_cast<volatile uint32_t*>(&px->issued);
+  const uint32_t hi = issued > peer ? issued : peer;
+  const uint32_t lo = hi > uint32_t(STAGES) ? hi - uint32_t(STAGES) : 0u;
+  for (uint32_t idx = lo; idx < hi; ++idx) {
+    const uint32_t s = idx % uint32_t(STAGES);
+    if (idx >= issued)
+      mbar_arrive_expect_tx(&full[s], reinterpret_cast<volatile uint32_t*>(px->bytes)[s]);
+    else if (idx >= peer)
+      mbar_complete_tx(&full[s], bytes[s]);
+    mbar_wait_drain(&full[s], (idx / uint32_t(STAGES)) & 1u, p.drain_ns, p.err);
   }
 }
 

@@ -37,14 +37,15 @@ struct Nvfp4PairCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kEpiWarps = 8;
   static constexpr int kEpiBytes = kEpiWarps * 2 * 32 * 64;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
 
   static_assert(kTmemUsed <= kTmemCols, "TMEM budget exceeded");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert(2 * STAGES + 5 <= kBarBytes / 8 - 2, "barrier area too small");
+  // barriers, tmem slot + abort flag, stall barrier, PairExit
+  static_assert((2 * STAGES + 5) * 8 + sizeof(PairExit) <= kBarBytes, "barrier area too small");
 
   // Block-scaled descriptor: A, B = E2M1 (1), UE4M3 scales, M = 256, N = 256, K = 64.
   __host__ __device__ static constexpr uint32_t idesc() {
@@ -75,6 +76,8 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint64_t* stall = drain + 2;  // test hook: nothing arrives on it
+  PairExit* pexit = reinterpret_cast<PairExit*>(stall + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -90,6 +93,8 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * Cfg::kEpiWarps);
     mbar_init(drain, 1);
+    mbar_init(stall, 1);
+    mbar_init(&pexit->bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -116,6 +121,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       uint32_t issued = 0;
+      uint32_t tx[STAGES] = {};  // this CTA's copy bytes per ring slot (last use)
       bool ok = true;
       const int64_t tpr = p.sf_tiles_per_row_block;
       const int a_row_blocks = (p.M + 127) / 128;
@@ -151,6 +157,7 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
           tma_load_3d_pair(ssfa, &tmSFA, bar, 0, a_rb_sf * int(tpr) + k_tile, 0);
           tma_load_3d_pair(ssfb, &tmSFB, bar, 0, b_rb0 * int(tpr) + k_tile, 0);
           tma_load_3d_pair(ssfb + 2048, &tmSFB, bar, 0, b_rb1 * int(tpr) + k_tile, 0);
+          tx[s] = Cfg::kStageBytes;
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -158,13 +165,12 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
           }
         }
       }
-      if (rank == 0) {
-        const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
-        for (uint32_t i = 0; i < outstanding; ++i) {
-          const uint32_t idx = issued - 1 - i;
-          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
-        }
-      }
+      // Both CTAs' copies complete on the leader's barriers: settle the two
+      // producers' accounts, then wait for the last stages.
+      if (rank == 0)
+        pair_exit_drain<STAGES>(pexit, full, issued, tx, p);
+      else
+        pair_exit_publish<STAGES>(pexit, issued, tx);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer (leader)
@@ -217,6 +223,9 @@ __global__ void __launch_bounds__(Nvfp4PairCfg<EPI, STAGES>::kThreads, 1)
       tc_commit_pair(drain);
       mbar_wait_drain(drain, 0, p.drain_ns, p.err);
     }
+  } else if (p.debug_stall && !mbar_wait(stall, 0, ctl, kErrInjectedStall)) {
+    // Test hook: the epilogue waited on a barrier nothing arrives on; the CTA
+    // has aborted and its other roles drain and return.
   } else {
     // -------------------------------------------------------------- epilogue
     epilogue_loop_regdrain<EPI, kScaleScalar, HAS_BIAS>(

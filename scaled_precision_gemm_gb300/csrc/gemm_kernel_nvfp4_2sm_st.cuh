@@ -54,7 +54,10 @@ struct Nvfp4StCfg {
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
 
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert((4 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 + 4 * STAGES <= kBarBytes,
+  // barriers, residual barriers, tmem slot + abort flag, slot-use counters,
+  // stall barrier, PairExit
+  static_assert((4 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 + 4 * STAGES + 8 + 8 +
+                        sizeof(PairExit) <= kBarBytes,
                 "barrier area too small");
   __host__ __device__ static constexpr uint32_t idesc() { return Base::idesc(); }
 };
@@ -181,6 +184,10 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(res_bars + 2 * Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* landed = abort_flag + 1;  // STAGES counters (ScaleService)
+  // test hook barrier (nothing arrives on it), then the pair's exit record
+  uint64_t* stall = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(landed + STAGES) + 7) & ~uintptr_t(7));
+  PairExit* pexit = reinterpret_cast<PairExit*>(stall + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -201,6 +208,8 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     *abort_flag = 0;
     for (int s = 0; s < STAGES; ++s) landed[s] = 0;
+    mbar_init(stall, 1);
+    mbar_init(&pexit->bar, 1);
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -227,6 +236,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       uint32_t issued = 0;
+      uint32_t tx[STAGES] = {};  // this CTA's code-copy bytes per ring slot (last use)
       bool ok = true;
       const int64_t tpr = p.sf_tiles_per_row_block;
       const int a_row_blocks = (p.M + 127) / 128;
@@ -265,6 +275,7 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
           const int kx = kb * Cfg::kBKBytes;
           tma_load_3d_pair(sa, &tmA, bar, kx, m0, 0);
           tma_load_3d_pair(sb, &tmB, bar, kx, n0, 0);
+          tx[s] = Cfg::kABytes + Cfg::kBBytes;
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -273,14 +284,18 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
         }
       }
       // No copy may still be writing this CTA's memory (or signalling the
-      // leader's barriers) at exit.
+      // leader's barriers) at exit: the scale tiles land on this CTA's own
+      // barriers; both CTAs' code copies land on the leader's, whose
+      // accounts the two producers settle.
       const uint32_t outstanding = issued < uint32_t(STAGES) ? issued : uint32_t(STAGES);
       for (uint32_t i = 0; i < outstanding; ++i) {
         const uint32_t idx = issued - 1 - i;
         mbar_wait_drain(&sf_full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
-        if (rank == 0)
-          mbar_wait_drain(&full[idx % STAGES], (idx / STAGES) & 1u, p.drain_ns, p.err);
       }
+      if (rank == 0)
+        pair_exit_drain<STAGES>(pexit, full, issued, tx, p);
+      else
+        pair_exit_publish<STAGES>(pexit, issued, tx);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer (leader)
@@ -324,6 +339,10 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
       tc_commit_pair(drain);
       mbar_wait_drain(drain, 0, p.drain_ns, p.err);
     }
+  } else if (p.debug_stall && !mbar_wait(stall, 0, ctl, kErrInjectedStall)) {
+    // Test hook: the epilogue (and with it the scale service) waited on a
+    // barrier nothing arrives on; the CTA has aborted and its other roles
+    // drain and return.
   } else {
     // ------------------------------------- epilogue + scale-factor stores
     int my_stages = 0;

@@ -98,39 +98,145 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
+// Encoded descriptors are cached: a GEMM call builds 3 to 6 of them, and
+// eager calls with the same operands (decode steps, repeated layers) would
+// otherwise re-encode them every time.  A descriptor holds nothing but the
+// arguments it was encoded from, so an entry is reused exactly when every
+// argument matches; a freed and re-allocated buffer at the same address with
+// the same shape gets the same, still correct, descriptor.  Direct-mapped,
+// kTmapCacheSize entries, one lock.
+namespace {
+enum TmapType : int { kTmapU8 = 0, kTmapBf16 = 1, kTmapU32 = 2 };
+
+struct TmapKey {
+  const void* base;
+  uint64_t d0, d1, d2, s1, s2;
+  uint32_t b0, b1;
+  int type, swizzle;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s1 == o.s1 && s2 == o.s2 &&
+           b0 == o.b0 && b1 == o.b1 && type == o.type && swizzle == o.swizzle;
+  }
+};
+
+struct TmapEntry {
+  CUtensorMap map;
+  TmapKey key;
+  bool valid;
+};
+
+constexpr int kTmapCacheSize = 256;
+TmapEntry g_tmap_cache[kTmapCacheSize];
+std::mutex g_tmap_mu;
+std::atomic<uint64_t> g_tmap_hits{0}, g_tmap_misses{0};
+
+uint32_t tmap_slot(const TmapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+  for (uint64_t v : {k.d0, k.d1, k.d2, k.s1, k.s2, uint64_t(k.b0) << 32 | k.b1,
+                     uint64_t(k.type) << 8 | uint64_t(k.swizzle)})
+    h = (h ^ v) * 0xBF58476D1CE4E5B9ull;
+  return static_cast<uint32_t>(h >> 40) % kTmapCacheSize;
+}
+
+bool encode_tmap(CUtensorMap* out, const TmapKey& k) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
+  const cuuint64_t strides[2] = {k.s1, k.s2};
+  const cuuint32_t box[3] = {k.b0, k.b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (k.swizzle == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  else if (k.swizzle == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  else if (k.swizzle == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUtensorMapDataType dt = k.type == kTmapBf16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : k.type == kTmapU32 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(out, dt, 3, const_cast<void*>(k.base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool cached_tmap(CUtensorMap* out, const TmapKey& k) {
+  const uint32_t slot = tmap_slot(k);
+  {
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    const TmapEntry& e = g_tmap_cache[slot];
+    if (e.valid && e.key == k) {
+      *out = e.map;
+      g_tmap_hits.fetch_add(1, std::memory_order_relaxed);
+      return true;
+    }
+  }
+  if (!encode_tmap(out, k)) return false;
+  g_tmap_misses.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  TmapEntry& e = g_tmap_cache[slot];
+  e.map = *out;
+  e.key = k;
+  e.valid = true;
+  return true;
+}
+}  // namespace
+
 bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, uint64_t d1,
                   uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
                   uint32_t box1, int swizzle_bytes) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-  const cuuint32_t box[3] = {box0, box1, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  else if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
-  else if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
-  const CUresult r =
-      fn(out, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const TmapKey k{base, d0, d1, d2, stride1_bytes, stride2_bytes, box0, box1,
+                  bf16 ? kTmapBf16 : kTmapU8, swizzle_bytes};
+  return cached_tmap(out, k);
 }
 
 bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   // Encoded with a third dimension of extent 1 so the kernels' 3-D TMA
   // instruction form applies to it as to every other operand.
-  const cuuint64_t dims[3] = {d0, d1, 1};
-  const cuuint64_t strides[2] = {stride1_bytes, stride1_bytes * d1};
-  const cuuint32_t box[3] = {box0, box1, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const TmapKey k{base, d0, d1, 1, stride1_bytes, stride1_bytes * d1, box0, box1, kTmapU32, 0};
+  return cached_tmap(out, k);
+}
+
+void tmap_cache_stats(uint64_t* hits, uint64_t* misses) {
+  *hits = g_tmap_hits.load(std::memory_order_relaxed);
+  *misses = g_tmap_misses.load(std::memory_order_relaxed);
+}
+
+// ------------------------------------------------------------ forced routes
+// SPG_FORCE_VARIANT / SPG_FORCE_TAIL pin a tile shape or a tail split for
+// A/B runs and tests.  They are read from the environment once, on first
+// use, and again only when spg_debug_reload_env() is called, so the
+// selector does no environment lookup per call.
+namespace {
+struct ForcedRoute {
+  char variant[32];
+  char tail[16];
+};
+std::mutex g_forced_mu;
+ForcedRoute g_forced;
+bool g_forced_loaded = false;
+
+void copy_env(char* dst, size_t n, const char* name) {
+  const char* v = std::getenv(name);
+  dst[0] = 0;
+  if (v) {
+    std::strncpy(dst, v, n - 1);
+    dst[n - 1] = 0;
+  }
+}
+
+ForcedRoute forced_route() {
+  std::lock_guard<std::mutex> lk(g_forced_mu);
+  if (!g_forced_loaded) {
+    copy_env(g_forced.variant, sizeof g_forced.variant, "SPG_FORCE_VARIANT");
+    copy_env(g_forced.tail, sizeof g_forced.tail, "SPG_FORCE_TAIL");
+    g_forced_loaded = true;
+  }
+  return g_forced;
+}
+}  // namespace
+
+void reload_forced_route() {
+  std::lock_guard<std::mutex> lk(g_forced_mu);
+  g_forced_loaded = false;
 }
 
 // ---------------------------------------------------------------- routes
@@ -178,12 +284,11 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   // SPG_FORCE_VARIANT pins the tile shape for A/B runs and tests:
   // 2sm | 2sm192 | 2sm160 | 2sm128 (pair tiles), 1sm256 | 1sm128 (one CTA).
   // SPG_FORCE_TAIL = none | n | k pins how the last partial wave is split.
-  const char* forced_name = std::getenv("SPG_FORCE_VARIANT");
-  if (forced_name && !*forced_name) forced_name = nullptr;
+  const ForcedRoute forced = forced_route();
+  const char* forced_name = forced.variant[0] ? forced.variant : nullptr;
   const bool force_one_cta =
       forced_name && (!std::strcmp(forced_name, "1sm256") || !std::strcmp(forced_name, "1sm128"));
-  const char* forced_tail = std::getenv("SPG_FORCE_TAIL");
-  if (forced_tail && !*forced_tail) forced_tail = nullptr;
+  const char* forced_tail = forced.tail[0] ? forced.tail : nullptr;
   const bool tail_n_ok = !forced_tail || !std::strcmp(forced_tail, "n");
   const bool tail_k_ok = allow_ksplit && (!forced_tail || !std::strcmp(forced_tail, "k"));
   const bool tail_none_ok = !forced_tail || !std::strcmp(forced_tail, "none");
@@ -225,7 +330,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     }
     r.grid = static_cast<int>(2 * (items < pairs ? items : pairs));
     r.smem_bytes = 1024 + r.stages * (128 * 128 + r.block_n / 2 * 128) + 4 * 2 * 2048 +
-                   (add ? 4 * (r.block_n / 32) * 2048 : 0) + 256;
+                   (add ? 4 * (r.block_n / 32) * 2048 : 0) + 512;
     return r;
   }
   // NVFP4 at decode-sized T (1-4 tokens): the CUDA-core GEMV (variant 4;
@@ -387,7 +492,8 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     stage_bytes = 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
     if (r.block_m == 256) epi_warps = 4;
   }
-  r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + (r.variant == 3 ? 512 : 256);
+  // barrier area: 512 bytes in the two-SM kernels, 256 in the one-CTA ones
+  r.smem_bytes = 1024 + r.stages * stage_bytes + epi_warps * 2 * 2048 + (r.block_m == 256 ? 512 : 256);
   return r;
 }
 
@@ -413,6 +519,12 @@ extern "C" int spg_version(void) { return 200; }
 
 extern "C" void spg_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed);
+}
+
+extern "C" void spg_debug_reload_env(void) { reload_forced_route(); }
+
+extern "C" void spg_debug_tmap_cache_stats(uint64_t* hits, uint64_t* misses) {
+  if (hits && misses) tmap_cache_stats(hits, misses);
 }
 
 extern "C" void spg_debug_inject_stall(int enable) {

@@ -21,6 +21,13 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
 bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
 
+// Hits and misses of the tensor-map cache behind the two functions above.
+void tmap_cache_stats(uint64_t* hits, uint64_t* misses);
+
+// Make the route selector read SPG_FORCE_VARIANT / SPG_FORCE_TAIL again on
+// its next call.
+void reload_forced_route();
+
 // Tail split of a two-SM schedule along N (see plan_items): with `units` CTA
 // pairs and `tiles` tiles of width bn, the tiles of the last partial wave
 // are split into `ways` (1, 2 or 4) narrower items, each a whole number of

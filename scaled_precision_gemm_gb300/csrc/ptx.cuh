@@ -398,6 +398,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Store a 32-bit word to a shared::cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Mark `bytes` of the current phase's expected transaction count of a local
+// mbarrier as done without a copy (for bytes that will never arrive).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier of either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m,

@@ -237,3 +237,26 @@ def test_oracle_is_not_imported_by_the_package():
     assert "oracle" not in re.sub(r'""".*?"""', "", src, flags=re.S)
     assert all("oracle" not in open(os.path.join(ROOT, "scaled_precision_gemm_gb300", "csrc", f)).read()
                for f in os.listdir(os.path.join(ROOT, "scaled_precision_gemm_gb300", "csrc")))
+
+
+def test_forced_route_is_read_once_until_reload(lib, monkeypatch):
+    """The selector reads SPG_FORCE_VARIANT once; a later change of the
+    variable takes effect only after spg_debug_reload_env (the binding calls
+    it when it sees the variable change)."""
+    def route():
+        r = spg.Route()
+        assert lib.spg_select_route(0, 1000, 5120, 6144, 0, 1, ctypes.byref(r)) == 0
+        return r.block_m, r.block_n
+
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm128")
+    lib.spg_debug_reload_env()
+    assert route() == (256, 128)
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "1sm256")
+    assert route() == (256, 128)          # not re-read yet
+    lib.spg_debug_reload_env()
+    assert route() == (128, 256)
+    # through the binding, the change is noticed without an explicit reload
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm160")
+    assert spg.select_route("fp8_rowscaled", 1000, 5120, 6144)["block_n"] == 160
+    monkeypatch.delenv("SPG_FORCE_VARIANT")
+    lib.spg_debug_reload_env()

@@ -1,7 +1,7 @@
 """Failure detection without a GPU fault.
 
 Every in-kernel wait is bounded in time.  With the test hook
-spg_debug_inject_stall, the epilogue of the one-CTA kernel waits on a barrier
+spg_debug_inject_stall, the epilogue of every GEMM kernel waits on a barrier
 that nothing arrives on (a flag nothing sets), under a 20 ms bound: the wait
 runs out, the kernel records the code in the device error word, the producer
 and MMA roles see the abort flag, drain the copies and MMAs in flight, free
@@ -51,6 +51,56 @@ def test_wait_timeout_is_reported_and_context_survives(monkeypatch):
     torch.cuda.synchronize()
     assert spg.last_device_error() == 0
     assert_within_tol(to_f64(y), oracle.fp8_rowscaled_gemm(A, sa, W, sw), "after time-out")
+
+
+def _nvfp4_inputs(T, N, K):
+    from tests.helpers import sf_rowmajor_to_blocked
+    x, w = normal_bf16((T, K), seed=0), normal_bf16((N, K), seed=1)
+    gA, gW = oracle.nvfp4_global_scale(x), oracle.nvfp4_global_scale(w)
+    A, sfA = oracle.quantize_nvfp4(x, gA)
+    W, sfW = oracle.quantize_nvfp4(w, gW)
+    dev = (cuda(A), cuda(sf_rowmajor_to_blocked(sfA, T, K)),
+           torch.tensor([gA], dtype=torch.float32, device=DEV), cuda(W),
+           cuda(sf_rowmajor_to_blocked(sfW, N, K)),
+           torch.tensor([gW], dtype=torch.float32, device=DEV))
+    return (A, sfA, gA, W, sfW, gW), dev
+
+
+@pytest.mark.parametrize("variant", ["2sm", "swap", "2sm_cp", "2sm_st"])
+def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypatch):
+    """The same check on the two-SM kernels: both CTAs' epilogues stall, every
+    wait of the pair runs out or sees the abort, the two producers settle
+    their copies on the leader's barriers and the pair exits cleanly."""
+    monkeypatch.setenv("SPG_FORCE_VARIANT", variant)
+    if variant in ("2sm", "swap"):
+        T, N, K = (64, 1024, 4096) if variant == "swap" else (512, 512, 4096)
+        A, sa, W, sw = _inputs(T, N, K)
+        args = (cuda(A), cuda(sa), cuda(W), cuda(sw))
+        call = lambda: spg.fp8_rowscaled_gemm(*args)
+        ref = lambda: oracle.fp8_rowscaled_gemm(A, sa, W, sw)
+        assert spg.select_route("fp8_rowscaled", T, N, K)["swap_ab"] == (variant == "swap")
+    else:
+        T, N, K = 512, 512, 4096
+        host, dev = _nvfp4_inputs(T, N, K)
+        call = lambda: spg.nvfp4_gemm(*dev)
+        ref = lambda: oracle.nvfp4_gemm(*host)
+        assert spg.select_route("nvfp4", T, N, K)["variant"] == (0 if variant == "2sm_cp" else 3)
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    spg.set_wait_timeout_ns(20_000_000)
+    spg.debug_inject_stall(True)
+    try:
+        call()
+        code = spg.last_device_error_code()
+    finally:
+        spg.debug_inject_stall(False)
+        spg.set_wait_timeout_ns(2_000_000_000)
+    assert code == INJECTED, hex(code)
+    assert spg.last_device_error() == 0
+    y = call()
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    assert_within_tol(to_f64(y), ref(), f"{variant} after time-out")
 
 
 def test_status_codes_are_distinct_for_host_errors():
