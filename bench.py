@@ -732,6 +732,79 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_host_overhead(args):
+    """Host time per eager GEMM call through the C ABI (ctypes, arguments
+    marshalled once): the library's argument checks, route selection,
+    tensor-map set-up and the launch itself, with the tensor-map cache on and
+    off.  Calls are enqueued in batches of 100 (each batch well inside the
+    launch queue) and the device is synchronised between batches, outside the
+    host timer."""
+    import ctypes
+    import torch
+
+    import scaled_precision_gemm_gb300 as spg
+    from scaled_precision_gemm_gb300 import build as spg_build
+
+    spg_build.build()
+    lib = spg.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    out = {}
+    shapes = [("fp8", 16, 17408, 5120), ("fp8", 8192, 17408, 5120),
+              ("nvfp4", 1, 17408, 5120), ("nvfp4", 8192, 17408, 5120)]
+    for kind, T, K, N in shapes:
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        kbytes = K if kind == "fp8" else K // 2
+        A = torch.randint(0, 0x70, (T, kbytes), dtype=torch.uint8, device=dev, generator=g)
+        W = torch.randint(0, 0x70, (N, kbytes), dtype=torch.uint8, device=dev, generator=g)
+        res = torch.zeros((T, N), dtype=torch.bfloat16, device=dev)
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        ws = spg.gemm_workspace("fp8_rowscaled" if kind == "fp8" else "nvfp4", T, N, K, "add",
+                                device=dev)
+        wsn = 0 if ws is None else ws.numel()
+        if kind == "fp8":
+            sa = torch.full((T,), 1e-3, device=dev)
+            sw = torch.full((N,), 1e-3, device=dev)
+            fn = lib.fp8_rowscaled_gemm_ws
+            cargs = (vp(A), vp(sa), vp(W), vp(sw), None, None, vp(res), vp(Y), T, N, K, 1,
+                     vp(ws), wsn, stream)
+        else:
+            sfA = torch.full((spg.nvfp4_sf_bytes(T, K),), 0x38, dtype=torch.uint8, device=dev)
+            sfW = torch.full((spg.nvfp4_sf_bytes(N, K),), 0x38, dtype=torch.uint8, device=dev)
+            g1 = torch.ones(4, device=dev)
+            fn = lib.nvfp4_gemm_ws
+            cargs = (vp(A), vp(sfA), vp(g1), vp(W), vp(sfW), vp(g1), None, None, vp(res), vp(Y),
+                     T, N, K, 1, vp(ws), wsn, stream)
+        name = f"{kind}_add_T{T}_K{K}_N{N}"
+        route = spg.select_route("fp8_rowscaled" if kind == "fp8" else "nvfp4", T, N, K, "add",
+                                 workspace=True)
+        res_d = {"variant": route["variant"], "swap_ab": route["swap_ab"]}
+        for mode in ("cache_on", "cache_off"):
+            lib.spg_debug_set_tmap_cache(1 if mode == "cache_on" else 0)
+            for _ in range(20):
+                assert fn(*cargs) == 0
+            torch.cuda.synchronize()
+            per = []
+            for _ in range(10):
+                t0 = time.perf_counter()
+                for _ in range(100):
+                    fn(*cargs)
+                per.append((time.perf_counter() - t0) / 100 * 1e6)
+                torch.cuda.synchronize()
+            res_d[mode + "_us"] = round(statistics.median(per), 2)
+        lib.spg_debug_set_tmap_cache(1)
+        out[name] = res_d
+    # the cost of the ctypes call itself: a host-only entry point
+    n0 = time.perf_counter()
+    for _ in range(10000):
+        lib.spg_version()
+    out["ctypes_call_floor_us"] = round((time.perf_counter() - n0) / 10000 * 1e6, 3)
+    print(json.dumps({"host_overhead": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -750,7 +823,12 @@ def main():
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch eagerly in the timed region instead of replaying CUDA graphs")
     ap.add_argument("--case", default=None, help="run only this case of the workload")
+    ap.add_argument("--host-overhead", action="store_true",
+                    help="only measure host time per eager GEMM call (tensor-map cache on/off)")
     args = ap.parse_args()
+    if args.host_overhead:
+        run_host_overhead(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

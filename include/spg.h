@@ -132,6 +132,11 @@ SPG_API void spg_debug_reload_env(void);
  * reused.  Both pointers must be non-null (host memory). */
 SPG_API void spg_debug_tmap_cache_stats(uint64_t* hits, uint64_t* misses);
 
+/* Switch the tensor-map cache on (the default) or off; off also empties it.
+ * For timing the host side of a call with and without the cache.  Host-side
+ * setting; not thread-safe against concurrent launches. */
+SPG_API void spg_debug_set_tmap_cache(int enable);
+
 /* Synchronizes `stream`, then reads and clears the library's device error
  * word.  Returns SPG_OK, SPG_ERR_TIMEOUT (a bounded wait ran out in some
  * earlier launch) or SPG_ERR_CUDA (the stream reported an error). */

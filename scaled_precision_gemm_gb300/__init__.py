@@ -74,6 +74,7 @@ def load_library():
             "spg_set_wait_timeout_ns": (None, [u64]),
             "spg_debug_inject_stall": (None, [i32]),
             "spg_debug_reload_env": (None, []),
+            "spg_debug_set_tmap_cache": (None, [i32]),
             "spg_debug_tmap_cache_stats": (None, [ctypes.POINTER(ctypes.c_uint64),
                                                   ctypes.POINTER(ctypes.c_uint64)]),
             "spg_last_device_error": (st, [vp]),

@@ -129,6 +129,7 @@ constexpr int kTmapCacheSize = 256;
 TmapEntry g_tmap_cache[kTmapCacheSize];
 std::mutex g_tmap_mu;
 std::atomic<uint64_t> g_tmap_hits{0}, g_tmap_misses{0};
+std::atomic<int> g_tmap_cache_on{1};
 
 uint32_t tmap_slot(const TmapKey& k) {
   uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
@@ -158,6 +159,7 @@ bool encode_tmap(CUtensorMap* out, const TmapKey& k) {
 }
 
 bool cached_tmap(CUtensorMap* out, const TmapKey& k) {
+  if (!g_tmap_cache_on.load(std::memory_order_relaxed)) return encode_tmap(out, k);
   const uint32_t slot = tmap_slot(k);
   {
     std::lock_guard<std::mutex> lk(g_tmap_mu);
@@ -193,6 +195,14 @@ bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t 
   // instruction form applies to it as to every other operand.
   const TmapKey k{base, d0, d1, 1, stride1_bytes, stride1_bytes * d1, box0, box1, kTmapU32, 0};
   return cached_tmap(out, k);
+}
+
+void set_tmap_cache(bool on) {
+  g_tmap_cache_on.store(on ? 1 : 0, std::memory_order_relaxed);
+  if (!on) {
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    for (TmapEntry& e : g_tmap_cache) e.valid = false;
+  }
 }
 
 void tmap_cache_stats(uint64_t* hits, uint64_t* misses) {
@@ -522,6 +532,8 @@ extern "C" void spg_set_wait_timeout_ns(uint64_t ns) {
 }
 
 extern "C" void spg_debug_reload_env(void) { reload_forced_route(); }
+
+extern "C" void spg_debug_set_tmap_cache(int enable) { set_tmap_cache(enable != 0); }
 
 extern "C" void spg_debug_tmap_cache_stats(uint64_t* hits, uint64_t* misses) {
   if (hits && misses) tmap_cache_stats(hits, misses);

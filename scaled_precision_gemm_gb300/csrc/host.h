@@ -21,8 +21,10 @@ bool make_tmap_3d(CUtensorMap* out, const void* base, bool bf16, uint64_t d0, ui
 bool make_tmap_2d_u32(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
 
-// Hits and misses of the tensor-map cache behind the two functions above.
+// Hits and misses of the tensor-map cache behind the two functions above;
+// switching the cache off (A/B timing of the host path) also empties it.
 void tmap_cache_stats(uint64_t* hits, uint64_t* misses);
+void set_tmap_cache(bool on);
 
 // Make the route selector read SPG_FORCE_VARIANT / SPG_FORCE_TAIL again on
 // its next call.
