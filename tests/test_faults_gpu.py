@@ -95,7 +95,12 @@ def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypat
     finally:
         spg.debug_inject_stall(False)
         spg.set_wait_timeout_ns(2_000_000_000)
-    assert code == INJECTED, hex(code)
+    # In the warp-stored-scale kernel the stalled epilogue warps are also the
+    # scale writers, so the MMA issuer's wait for the first stage's scales
+    # (code 0x102, ring slot full) runs out at about the same time as the
+    # injected wait; whichever expires first is recorded.
+    expected = {INJECTED, 0x102} if variant == "2sm_st" else {INJECTED}
+    assert code in expected, hex(code)
     assert spg.last_device_error() == 0
     y = call()
     torch.cuda.synchronize()
