@@ -8,6 +8,7 @@
 #include "gemm_kernel_2sm.cuh"
 #include "gemm_kernel_nvfp4_2sm.cuh"
 #include "gemm_kernel_nvfp4_2sm_st.cuh"
+#include "gemm_kernel_nvfp4_mc.cuh"
 #include "host.h"
 
 namespace spg {
@@ -115,6 +116,42 @@ spg_status launch_nvfp4_2sm_st_variant(const GemmMaps& maps, const GemmParams& p
                                        cudaStream_t stream) {
   using Cfg = Nvfp4StCfg<EPI, STAGES>;
   auto kern = gemm_kernel_nvfp4_2sm_st<EPI, STAGES, HAS_BIAS>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes),
+                    "cudaFuncSetAttribute") != SPG_OK)
+      return SPG_ERR_CUDA;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, maps.sfa, maps.sfb,
+                                     maps.r, p),
+                  "cudaLaunchKernelEx") != SPG_OK)
+    return SPG_ERR_CUDA;
+  return launch_status();
+}
+
+// NVFP4 on clusters of two sharing B by multicast, one-CTA MMAs.
+template <int EPI, int STAGES, bool HAS_BIAS>
+spg_status launch_nvfp4_mc_variant(const GemmMaps& maps, const GemmParams& p, int grid,
+                                   cudaStream_t stream) {
+  using Cfg = Nvfp4McCfg<EPI, STAGES>;
+  auto kern = gemm_kernel_nvfp4_mc<EPI, STAGES, HAS_BIAS>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;

@@ -37,6 +37,10 @@ spg_status launch_gemv_tokens(const GemvParams& p, cudaStream_t s) {
 
 template <int EPI>
 spg_status launch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
+  if (r.block_m == 256 && r.variant == 5) {
+    if (p.bias_kind) return launch_nvfp4_mc_variant<EPI, 3, true>(m, p, r.grid, s);
+    return launch_nvfp4_mc_variant<EPI, 3, false>(m, p, r.grid, s);
+  }
   if (r.block_m == 256 && r.variant == 3) {
     if (p.bias_kind) return launch_nvfp4_2sm_st_variant<EPI, 5, true>(m, p, r.grid, s);
     return launch_nvfp4_2sm_st_variant<EPI, 5, false>(m, p, r.grid, s);

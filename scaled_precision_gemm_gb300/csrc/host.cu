@@ -406,7 +406,9 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     // tensor pipe for +5-12% over the copies) or copied by the tensor core
     // (variant 0, 2sm_cp).
     const bool st_scales = forced_name ? std::strcmp(forced_name, "2sm_cp") != 0 : true;
-    r.variant = one_cta ? 2 : (st_scales ? 3 : 0);
+    const bool mc = forced_name && std::strcmp(forced_name, "2sm_mc") == 0;
+    r.variant = one_cta ? 2 : (mc ? 5 : (st_scales ? 3 : 0));
+    if (r.variant == 5) r.stages = 3;
   } else {
     // Pair tiles first (widths 256/192/160/128), then one-CTA tiles.  The
     // efficiencies are steady-state tensor-pipe fractions measured on GB300
@@ -494,7 +496,8 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   r.grid = static_cast<int>((g < 1 ? 1 : g) * (r.block_m == 256 ? 2 : 1));
   int stage_bytes, epi_warps = 4;
   if (kind == SPG_KIND_NVFP4 && r.block_m == 256) {
-    stage_bytes = 128 * 128 + 128 * 128 + 2048 + 4096;
+    // pair tiles stage half of B per CTA; the multicast tile stages all of it
+    stage_bytes = 128 * 128 + (r.variant == 5 ? 2 : 1) * 128 * 128 + 2048 + 4096;
     epi_warps = 8;
   } else if (kind == SPG_KIND_NVFP4) {
     stage_bytes = 128 * 128 + 128 * 128 + 2048 + 2048;

@@ -50,7 +50,7 @@ def test_fp8_rowscaled_bias(T, N, K, epi, kind, variant):
 
 @pytest.mark.parametrize("kind", ["bf16", "fp8"])
 @pytest.mark.parametrize("epi", ["linear", "add", "swiglu"])
-@pytest.mark.parametrize("nv_variant", ["auto", "1sm128", "2sm_cp", "2sm_st"])
+@pytest.mark.parametrize("nv_variant", ["auto", "1sm128", "2sm_cp", "2sm_st", "2sm_mc"])
 def test_nvfp4_bias(epi, kind, nv_variant, monkeypatch):
     if nv_variant == "auto":
         monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)

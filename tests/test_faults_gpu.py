@@ -66,7 +66,7 @@ def _nvfp4_inputs(T, N, K):
     return (A, sfA, gA, W, sfW, gW), dev
 
 
-@pytest.mark.parametrize("variant", ["2sm", "swap", "2sm_cp", "2sm_st"])
+@pytest.mark.parametrize("variant", ["2sm", "swap", "2sm_cp", "2sm_st", "2sm_mc"])
 def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypatch):
     """The same check on the two-SM kernels: both CTAs' epilogues stall, every
     wait of the pair runs out or sees the abort, the two producers settle
@@ -84,7 +84,8 @@ def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypat
         host, dev = _nvfp4_inputs(T, N, K)
         call = lambda: spg.nvfp4_gemm(*dev)
         ref = lambda: oracle.nvfp4_gemm(*host)
-        assert spg.select_route("nvfp4", T, N, K)["variant"] == (0 if variant == "2sm_cp" else 3)
+        assert spg.select_route("nvfp4", T, N, K)["variant"] == {"2sm_cp": 0, "2sm_st": 3,
+                                                                 "2sm_mc": 5}[variant]
     torch.cuda.synchronize()
     assert spg.last_device_error() == 0
     spg.set_wait_timeout_ns(20_000_000)
@@ -95,11 +96,11 @@ def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypat
     finally:
         spg.debug_inject_stall(False)
         spg.set_wait_timeout_ns(2_000_000_000)
-    # In the warp-stored-scale kernel the stalled epilogue warps are also the
+    # In the warp-stored-scale kernels the stalled epilogue warps are also the
     # scale writers, so the MMA issuer's wait for the first stage's scales
     # (code 0x102, ring slot full) runs out at about the same time as the
     # injected wait; whichever expires first is recorded.
-    expected = {INJECTED, 0x102} if variant == "2sm_st" else {INJECTED}
+    expected = {INJECTED, 0x102} if variant in ("2sm_st", "2sm_mc") else {INJECTED}
     assert code in expected, hex(code)
     assert spg.last_device_error() == 0
     y = call()

@@ -152,10 +152,11 @@ def test_fp8_k5120_full_size_sampled(T, N, epi):
 
 
 # ----------------------------------------------------------------- NVFP4
-@pytest.fixture(params=["auto", "1sm128", "2sm_cp", "2sm_st"])
+@pytest.fixture(params=["auto", "1sm128", "2sm_cp", "2sm_st", "2sm_mc"])
 def nv_variant(request, monkeypatch):
     """Pin the NVFP4 kernel: two-SM 256x256 with its scales copied into TMEM
-    by the tensor core (2sm_cp) or written by warps (2sm_st), or the one-CTA
+    by the tensor core (2sm_cp) or written by warps (2sm_st), the cluster of
+    two one-CTA tiles sharing the weight tile by multicast (2sm_mc), or the one-CTA
     128x128 tile."""
     if request.param == "auto":
         monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
@@ -316,3 +317,32 @@ def test_nvfp4_pair_kernels_agree_and_repeat(epi, monkeypatch):
     rows = _sample_rows(T, n=4)
     ref = oracle.nvfp4_gemm(A, sfA, gA, W, sfW, gW, res, epi, rows=rows)
     assert_within_tol(to_f64(base[torch.from_numpy(rows).to(DEV)]), ref, f"nvfp4 {epi} repeat")
+
+
+@pytest.mark.parametrize("epi", ["add", "swiglu"])
+def test_nvfp4_multicast_kernel_repeats(epi, monkeypatch):
+    """The multicast-cluster NVFP4 kernel (one-CTA MMAs, weight tile shared
+    by multicast, scales stored by each CTA's own warps) gives the same bits
+    on every one of many launches -- a missed ordering between the scale
+    stores, the two producers' multicast copies, the residual copies or the
+    accumulator hand-back shows up as a launch that differs -- and matches
+    the oracle."""
+    T, N, K = 4096, 5120, 5120
+    A, sfA, gA, W, sfW, gW = nvfp4_inputs(T, N, K, seed=93)
+    res = normal_bf16((T, N), seed=94) if epi == "add" else None
+    dA, dW = cuda(A), cuda(W)
+    dsA, dsW = cuda(sf_rowmajor_to_blocked(sfA, T, K)), cuda(sf_rowmajor_to_blocked(sfW, N, K))
+    tgA = torch.tensor([gA], dtype=torch.float32, device=DEV)
+    tgW = torch.tensor([gW], dtype=torch.float32, device=DEV)
+    dr = None if res is None else cuda_bf16(res)
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_mc")
+    assert spg.select_route("nvfp4", T, N, K, epi)["variant"] == 5
+    base = spg.nvfp4_gemm(dA, dsA, tgA, dW, dsW, tgW, residual=dr, epilogue=epi).clone()
+    for _ in range(12):
+        y = spg.nvfp4_gemm(dA, dsA, tgA, dW, dsW, tgW, residual=dr, epilogue=epi)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), base.view(torch.int16))
+    assert spg.last_device_error() == 0
+    rows = _sample_rows(T, n=4)
+    ref = oracle.nvfp4_gemm(A, sfA, gA, W, sfW, gW, res, epi, rows=rows)
+    assert_within_tol(to_f64(base[torch.from_numpy(rows).to(DEV)]), ref, f"nvfp4 mc {epi} repeat")

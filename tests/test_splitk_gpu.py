@@ -249,7 +249,7 @@ def run_nvfp4_ws(A, sfA, gA, W, sfW, gW, res, epi, ws, bias=None, bias_scale=Non
 @pytest.mark.parametrize("T,N,K", [(1, 16, 2048), (64, 512, 4096), (200, 272, 2304),
                                    (333, 400, 3072)])
 @pytest.mark.parametrize("bias", [False, True])
-@pytest.mark.parametrize("kernel", ["2sm_cp", "2sm_st"])
+@pytest.mark.parametrize("kernel", ["2sm_cp", "2sm_st", "2sm_mc"])
 def test_nvfp4_splitk_ragged(T, N, K, epi, bias, kernel, monkeypatch):
     monkeypatch.setenv("SPG_FORCE_TAIL", "k")
     monkeypatch.setenv("SPG_FORCE_VARIANT", kernel)
