@@ -3,8 +3,8 @@
 //
 // A cluster computes one 256 x 256 output tile, like the pair kernels: CTA r
 // owns rows 128r .. 128r + 127.  Unlike them, each CTA issues its own
-// tcgen05.mma.cta_group::1 (M = 128, two N = 128 halves per 64-element
-// k-step) into its own TMEM, so every operand and every scale an MMA reads
+// tcgen05.mma.cta_group::1 (M = 128, N = 256, one per 64-element k-step)
+// into its own TMEM, so every operand and every scale an MMA reads
 // lives in its own CTA.  The 256 weight rows of a stage are fetched once
 // from L2: CTA r loads rows 128r .. 128r + 127 of B and their scale tiles
 // with a multicast copy that lands in both CTAs' shared memory.
@@ -71,9 +71,12 @@ struct Nvfp4McCfg {
                     kBarBytes,
                 "barrier area too small");
 
-  // Block-scaled descriptor: A, B = E2M1 (1), UE4M3 scales, M = 128, N = 128, K = 64.
+  // Block-scaled descriptor: A, B = E2M1 (1), UE4M3 scales, M = 128, N = 256, K = 64.
+  // One instruction covers both 128-row halves of B (its scales: the two
+  // 4-column groups after A's), so each k-step reads A from shared memory
+  // once.
   __host__ __device__ static constexpr uint32_t idesc() {
-    return (1u << 7) | (1u << 10) | (uint32_t(128 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    return (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
   }
 };
 
@@ -264,13 +267,9 @@ __global__ void __launch_bounds__(Nvfp4McCfg<EPI, STAGES>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < Cfg::kKSteps; ++j) {
             const uint32_t col = sf_col0 + uint32_t(j * Cfg::kSfColsPerKStep);
-            const uint64_t adesc = smem_desc(sa + j * 32, 16, 1024, kSwizzle128B);
-            const uint32_t acc = (kb != w.kb_begin) || j != 0;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              mma_nvf4(tmem_base + uint32_t(h * 128), adesc,
-                       smem_desc(sb + h * Cfg::kBHalfBytes + j * 32, 16, 1024, kSwizzle128B),
-                       kIdesc, col, col + 4 + 4 * h, acc);
+            mma_nvf4(tmem_base, smem_desc(sa + j * 32, 16, 1024, kSwizzle128B),
+                     smem_desc(sb + j * 32, 16, 1024, kSwizzle128B), kIdesc, col, col + 4,
+                     (kb != w.kb_begin) || j != 0);
           }
           tc_commit_multicast(&empty[s], kBoth);
           if (++s == STAGES) {
