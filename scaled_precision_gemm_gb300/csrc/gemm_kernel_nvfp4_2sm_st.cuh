@@ -21,10 +21,20 @@
 // of the MMAs.
 //
 // Barriers (per stage s): full[s] (leader; both CTAs' A/B codes), sf_full[s]
-// (each CTA; its scale tiles), sf_ready[s] (leader; 8 arrivals: the 4 scale
-// writers of each CTA; the MMA issuer waits with a cluster-scope acquire),
+// (each CTA; its scale tiles), sf_ready[s] (leader; 5 arrivals: the 4 scale
+// writers of the leader and one forwarded for the peer's 4; the MMA issuer
+// waits with a cluster-scope acquire), peer_ready[s] (peer; its 4 writers),
 // empty[s] (both CTAs; multicast commit after the stage's MMAs).  Every wait
 // is bounded.
+//
+// The peer's scale writers do not signal the leader themselves: a
+// cluster-scope release arrival holds the issuing warp about 0.8 us (median;
+// 1.3 us at the 90th percentile, measured in this kernel on GB300), and a
+// writer warp serves every other stage, so the MMAs waited for it.  They
+// arrive on a barrier of their own CTA (cheap), and three otherwise idle
+// warps of the peer (its MMA warp and two forwarder warps) take turns
+// forwarding one cluster-scope arrival per stage, so three of those slow
+// releases are in flight at once.
 #pragma once
 
 #include "gemm_epilogue.cuh"
@@ -51,12 +61,13 @@ struct Nvfp4StCfg {
   static constexpr int kEpiBytes = kEpiWarps * 2 * 32 * 64;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + kBarBytes;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kFwdWarps = 2;  // forwarder warps after the epilogue warps
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kFwdWarps;
 
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  // barriers, residual barriers, tmem slot + abort flag, slot-use counters,
-  // stall barrier, PairExit
-  static_assert((4 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 + 4 * STAGES + 8 + 8 +
+  // barriers, residual barriers, tmem slot + abort flag, slot-use counters
+  // (writers and forwarders), stall barrier, PairExit
+  static_assert((5 * STAGES + 3 + 2 * kEpiWarps) * 8 + 8 + 8 * STAGES + 8 + 8 +
                         sizeof(PairExit) <= kBarBytes,
                 "barrier area too small");
   __host__ __device__ static constexpr uint32_t idesc() { return Base::idesc(); }
@@ -107,8 +118,8 @@ struct ScaleService {
   int end;            // stages of this CTA pair
   uint64_t* sf_full;         // this CTA's scale-tile barriers
   int* landed;               // per ring slot: uses seen complete (shared)
-  uint64_t* sf_ready;        // the leader's stage barriers (local in the leader)
-  uint32_t sf_ready_leader;  // the same, as cluster addresses (peer CTA)
+  uint64_t* sf_ready;        // stage barriers the writers arrive on (this CTA)
+  uint32_t sf_ready_leader;  // unused (0)
   bool leader;
   uint8_t* ring;
   int stage_bytes, sf_offset;  // ring stride; scale tiles' offset in a stage
@@ -138,17 +149,14 @@ struct ScaleService {
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      // Release (CTA scope in the leader, cluster scope from the peer), so
-      // the leader's cluster-scope acquire orders these TMEM stores before
-      // its MMAs.  Measured on GB300: a relaxed arrival instead runs the
-      // kernel at ~5.4 PFLOP/s but lets MMAs read stale scales (outputs
-      // differed in up to half of repeated launches), while each
-      // cluster-scope release holds its warp ~1 us.
+      // Release at CTA scope on a barrier of this CTA: the MMA issuer's own
+      // stage barrier in the leader; in the peer, the barrier its forwarders
+      // wait on, whose cluster-scope release then orders these TMEM stores
+      // before the leader's cluster-scope acquire and its MMAs (causality
+      // is transitive).  A relaxed arrival is not enough: the MMAs could
+      // read the scales before the stores land.
       if (lane == 0) {
-        if (leader)
-          mbar_arrive(&sf_ready[s]);
-        else
-          mbar_arrive_cluster(sf_ready_leader + uint32_t(s * 8));
+        mbar_arrive(&sf_ready[s]);
         // Off the path to the MMAs: the other half tests use u + 1 of this
         // slot only after it has landed, long after this.
         atomicMax(&landed[s], u + 1);
@@ -176,17 +184,19 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* sf_full = bars + 2 * STAGES;
-  uint64_t* sf_ready = bars + 3 * STAGES;
-  uint64_t* acc_full = bars + 4 * STAGES;
+  uint64_t* sf_ready = bars + 3 * STAGES;    // leader: writers + forwarded peer arrivals
+  uint64_t* peer_ready = bars + 4 * STAGES;  // peer: its 4 writers, read by the forwarders
+  uint64_t* acc_full = bars + 5 * STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint64_t* res_bars = drain + 1;  // linear_add residual: 2 per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(res_bars + 2 * Cfg::kEpiWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* landed = abort_flag + 1;  // STAGES counters (ScaleService)
+  int* landed = abort_flag + 1;       // STAGES counters (ScaleService)
+  int* forwarded = landed + STAGES;  // STAGES counters: uses forwarded per slot
   // test hook barrier (nothing arrives on it), then the pair's exit record
   uint64_t* stall = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(landed + STAGES) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(forwarded + STAGES) + 7) & ~uintptr_t(7));
   PairExit* pexit = reinterpret_cast<PairExit*>(stall + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -200,14 +210,15 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&sf_full[s], 1);
-      mbar_init(&sf_ready[s], 8);
+      mbar_init(&sf_ready[s], 5);
+      mbar_init(&peer_ready[s], 4);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * Cfg::kEpiWarps);
     mbar_init(drain, 1);
     for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     *abort_flag = 0;
-    for (int s = 0; s < STAGES; ++s) landed[s] = 0;
+    for (int s = 0; s < STAGES; ++s) landed[s] = forwarded[s] = 0;
     mbar_init(stall, 1);
     mbar_init(&pexit->bar, 1);
     fence_mbarrier_init();
@@ -297,6 +308,44 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
       else
         pair_exit_publish<STAGES>(pexit, issued, tx);
     }
+  } else if ((warp == 1 && rank == 1) || warp >= 2 + Cfg::kEpiWarps) {
+    // ------------------------------------------- forwarders (peer CTA only)
+    // Forwarder f (the peer's MMA warp, then the forwarder warps) takes the
+    // stages n with n % 3 == f: it waits until the peer's 4 writers have
+    // stored stage n's scales (peer_ready), then releases one arrival at
+    // cluster scope on the leader's sf_ready.  Uses of a ring slot come 5
+    // stages apart and rotate over the forwarders; a parity test cannot tell
+    // use u complete from use u - 2, so use u is tested only once
+    // forwarded[slot] shows use u - 1 passed on.
+    if (rank == 1 && lane == 0) {
+      const int f = warp == 1 ? 0 : warp - (2 + Cfg::kEpiWarps) + 1;
+      int my_stages = 0;
+      for (int item = pair; item < p.total_items; item += num_pairs) {
+        const WorkItem w = work_item(item, p, Cfg::kBN);
+        my_stages += w.kb_end - w.kb_begin;
+      }
+      const uint32_t leader_ready = mapa_shared(smem_u32(sf_ready), 0);
+      for (int n = f; n < my_stages; n += 1 + Cfg::kFwdWarps) {
+        const int s = n % STAGES;
+        const int u = n / STAGES;
+        const uint64_t t0 = globaltimer_ns();
+        bool ok = false;
+        for (uint32_t i = 1;; ++i) {
+          if (*reinterpret_cast<volatile int*>(&forwarded[s]) >= u) {
+            ok = true;
+            break;
+          }
+          if ((i & 15u) == 0 && (*ctl.abort_flag || globaltimer_ns() - t0 > ctl.timeout_ns)) {
+            *ctl.abort_flag = 1;
+            atomicCAS(ctl.err, 0u, kErrWaitFull);
+            break;
+          }
+        }
+        if (!ok || !mbar_wait(&peer_ready[s], uint32_t(u) & 1u, ctl, kErrWaitFull)) break;
+        atomicMax(&forwarded[s], u + 1);
+        mbar_arrive_cluster(leader_ready + uint32_t(s * 8));
+      }
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer (leader)
     if (lane == 0 && rank == 0) {
@@ -355,8 +404,8 @@ __global__ void __launch_bounds__(Nvfp4StCfg<EPI, STAGES>::kThreads, 1)
     svc.end = my_stages;
     svc.sf_full = sf_full;
     svc.landed = landed;
-    svc.sf_ready = sf_ready;
-    svc.sf_ready_leader = mapa_shared(smem_u32(sf_ready), 0);
+    svc.sf_ready = rank == 0 ? sf_ready : peer_ready;
+    svc.sf_ready_leader = 0;
     svc.leader = rank == 0;
     svc.ring = ring;
     svc.stage_bytes = Cfg::kStageBytes;
