@@ -98,9 +98,11 @@ def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypat
         spg.set_wait_timeout_ns(2_000_000_000)
     # In the warp-stored-scale kernels the stalled epilogue warps are also the
     # scale writers, so the MMA issuer's wait for the first stage's scales
-    # (code 0x102, ring slot full) runs out at about the same time as the
-    # injected wait; whichever expires first is recorded.
-    expected = {INJECTED, 0x102} if variant in ("2sm_st", "2sm_mc") else {INJECTED}
+    # (0x102, ring slot full) and the producer's wait for a ring slot the
+    # MMAs never free (0x101, ring slot free) start at about the same time as
+    # the injected wait and run out with it; whichever expires first is
+    # recorded.
+    expected = {INJECTED, 0x101, 0x102} if variant in ("2sm_st", "2sm_mc") else {INJECTED}
     assert code in expected, hex(code)
     assert spg.last_device_error() == 0
     y = call()
