@@ -5,7 +5,12 @@
 // All of them are HBM-bound streaming kernels: 16-byte vector loads of the
 // bf16 input, every fp32 step as one IEEE-rounded operation (__fdiv_rn,
 // __fmul_rn) so that codes and scales are bit-for-bit those of the plain
-// definition, and hardware cvt.rn.satfinite conversions for the codes.
+// definition, and hardware cvt.rn.satfinite conversions for the codes.  The
+// per-element IEEE division makes them partly ALU-bound (measured on GB300:
+// the FP8 row quantizer takes 88 us at T = 8192, K = 17408, and 63.5 us --
+// the HBM copy rate -- with the division replaced by a multiply, which is
+// not bit-exact; a reciprocal multiply with an exact fallback near the
+// rounding points measured slower than the division itself).
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -15,9 +20,6 @@
 
 namespace spg {
 namespace {
-
-constexpr int kRowThreads = 256;
-constexpr int kRowRegVecs = 9;  // 16-byte vectors per thread kept in registers
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -62,33 +64,39 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 }
 
 // One CTA per row: amax over the row, s = amax/448, codes = E4M3(x/s).
-__global__ void __launch_bounds__(kRowThreads) quantize_fp8_rows_kernel(
+// THREADS x VECS 16-byte vectors of the row stay in registers between the
+// two passes; longer rows re-read their remainder.  Rows up to 8192
+// elements take a 128-thread CTA, so more rows are in flight per SM
+// (measured on GB300 at T = 8192: K = 5120 45 -> 33 us, K = 6144 47 -> 37 us
+// against the 256-thread CTA).
+template <int THREADS, int VECS>
+__global__ void __launch_bounds__(THREADS) quantize_fp8_rows_kernel(
     const uint4* __restrict__ x, int64_t K, uint2* __restrict__ codes, float* __restrict__ scales) {
-  __shared__ float red[kRowThreads / 32];
+  __shared__ float red[THREADS / 32];
   const int64_t row = blockIdx.x;
   const int64_t nvec = K / 8;
   const uint4* xr = x + row * nvec;
   uint2* cr = codes + row * nvec;
-  uint4 cache[kRowRegVecs];
+  uint4 cache[VECS];
   float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < kRowRegVecs; ++j) {
-    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRowThreads;
+  for (int j = 0; j < VECS; ++j) {
+    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * THREADS;
     if (i < nvec) {
       cache[j] = __ldg(xr + i);
       amax = fmaxf(amax, vec_amax(cache[j]));
     }
   }
-  for (int64_t i = threadIdx.x + int64_t(kRowRegVecs) * kRowThreads; i < nvec; i += kRowThreads)
+  for (int64_t i = threadIdx.x + int64_t(VECS) * THREADS; i < nvec; i += THREADS)
     amax = fmaxf(amax, vec_amax(__ldg(xr + i)));
-  amax = block_max<kRowThreads>(amax, red);
+  amax = block_max<THREADS>(amax, red);
   const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
 #pragma unroll
-  for (int j = 0; j < kRowRegVecs; ++j) {
-    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRowThreads;
+  for (int j = 0; j < VECS; ++j) {
+    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * THREADS;
     if (i < nvec) cr[i] = vec_encode_e4m3(cache[j], s);
   }
-  for (int64_t i = threadIdx.x + int64_t(kRowRegVecs) * kRowThreads; i < nvec; i += kRowThreads)
+  for (int64_t i = threadIdx.x + int64_t(VECS) * THREADS; i < nvec; i += THREADS)
     cr[i] = vec_encode_e4m3(__ldg(xr + i), s);
   if (threadIdx.x == 0) scales[row] = s;
 }
@@ -287,8 +295,13 @@ extern "C" spg_status spg_quantize_fp8_rows(const void* x, int64_t rows, int64_t
   if (K == 0 || K % 8 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
   if (rows > 0x7FFFFFFF) return SPG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return SPG_ERR_MISALIGNED;
-  quantize_fp8_rows_kernel<<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(
-      static_cast<const uint4*>(x), K, reinterpret_cast<uint2*>(codes), scales);
+  const unsigned grid = static_cast<unsigned>(rows);
+  const uint4* xv = static_cast<const uint4*>(x);
+  uint2* cv = reinterpret_cast<uint2*>(codes);
+  if (K / 8 <= 128 * 8)
+    quantize_fp8_rows_kernel<128, 8><<<grid, 128, 0, stream>>>(xv, K, cv, scales);
+  else
+    quantize_fp8_rows_kernel<256, 9><<<grid, 256, 0, stream>>>(xv, K, cv, scales);
   return launch_status();
 }
 
