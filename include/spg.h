@@ -120,9 +120,10 @@ SPG_API void spg_set_wait_timeout_ns(uint64_t ns);
 SPG_API void spg_debug_inject_stall(int enable);
 
 /* Test hook: the route selector reads the environment variables
- * SPG_FORCE_VARIANT (pin a kernel variant) and SPG_FORCE_TAIL (pin how the
- * last partial wave is split: none | n | k) once, on its first call; this
- * makes the next call read them again.  Host-side setting; not thread-safe
+ * SPG_FORCE_VARIANT (pin a kernel variant), SPG_FORCE_TAIL (pin how the
+ * last partial wave is split: none | n | k) and SPG_FORCE_GROUP_M (m-blocks
+ * per rasterization group) once, on its first call; this makes the next
+ * call read them again.  Host-side setting; not thread-safe
  * against concurrent launches. */
 SPG_API void spg_debug_reload_env(void);
 
@@ -369,6 +370,43 @@ SPG_API spg_status fp8_tensor_gemm_ws(char layout_a, char layout_b, int64_t batc
                                       int64_t strideC, int64_t M, int64_t N, int64_t K,
                                       void* workspace, int64_t workspace_bytes,
                                       spg_stream_t stream);
+
+/* Activation operators: the GEMMs above taking bf16 activations X [T, K]
+ * (row-major, 16-byte aligned) and quantizing them inside the call, the
+ * operator the pages time (ninfer PR #160 "The NVFP4 TMA route reads
+ * activation scales as one tile", the operator table, which counts the
+ * bf16 activation read; ninfer PR #167 "The fp8 A8 GEMM stages its operands
+ * through TMA", the A8 call sites with per-row activation scales).
+ *   fp8_rowscaled_linear_bf16 = spg_quantize_fp8_rows(X) -> (A, sa), then
+ *     fp8_rowscaled_gemm_ws(A, sa, W, sw, ...);
+ *   nvfp4_linear_bf16 = spg_nvfp4_global_scale(X) -> gA,
+ *     spg_quantize_nvfp4(X, gA) -> (A, sfA), then nvfp4_gemm_ws(A, sfA, gA, ...).
+ * The codes, scales and result are exactly those of that sequence.  At
+ * NVFP4 decode widths (T <= 4, the GEMV route) the whole operator is one
+ * kernel: each CTA of the GEMV quantizes X into its shared memory itself and
+ * nothing but Y is written (no workspace is needed).  Otherwise the
+ * quantizer and the GEMM run back to back on `stream`, the codes and scales
+ * held in the workspace.
+ * workspace: device memory, 16-byte aligned, owned by the caller, at least
+ *   spg_act_workspace_bytes(kind, T, N, K, epilogue) bytes for the full
+ *   route (activation codes and scales, then the GEMM's K-split workspace);
+ *   the activation part alone is required (SPG_ERR_INVALID_ARG with less),
+ *   the K split is taken only when the rest is there too.  One workspace
+ *   serves one call at a time.  spg_act_workspace_bytes returns 0 when the
+ *   call needs none (the fused decode kernel) or the arguments are invalid.
+ * Other arguments, requirements and errors as for the _ws GEMM entry points
+ * (NVFP4: K % 256 == 0; FP8: K % 16 == 0). */
+SPG_API int64_t spg_act_workspace_bytes(int kind, int64_t T, int64_t N, int64_t K, int epilogue);
+SPG_API spg_status fp8_rowscaled_linear_bf16(const void* X, const uint8_t* W, const float* sw,
+                                             const void* bias, const float* bias_scale,
+                                             const void* residual, void* Y, int64_t T, int64_t N,
+                                             int64_t K, int epilogue, void* workspace,
+                                             int64_t workspace_bytes, spg_stream_t stream);
+SPG_API spg_status nvfp4_linear_bf16(const void* X, const uint8_t* W, const uint8_t* sfW,
+                                     const float* gW, const void* bias, const float* bias_scale,
+                                     const void* residual, void* Y, int64_t T, int64_t N,
+                                     int64_t K, int epilogue, void* workspace,
+                                     int64_t workspace_bytes, spg_stream_t stream);
 
 /* Per-shape tile / route selector (host only, no device query after the
  * first call).  kind: spg_kind; T: rows of the output (M for the tensor

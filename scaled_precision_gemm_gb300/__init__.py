@@ -21,6 +21,7 @@ __all__ = [
     "fp8_scale_ring", "quantize_fp8_tensor_delayed",
     "nvfp4_global_scale", "quantize_nvfp4",
     "nvfp4_sf_bytes", "nvfp4_sf_offset", "fp8_rowscaled_gemm", "nvfp4_gemm", "fp8_tensor_gemm",
+    "act_workspace_bytes", "act_workspace", "fp8_rowscaled_linear_bf16", "nvfp4_linear_bf16",
     "select_route", "last_device_error", "set_wait_timeout_ns", "status_string",
 ]
 
@@ -108,6 +109,11 @@ def load_library():
                                    vp, i64, vp]),
             "fp8_tensor_gemm_ws": (st, [ctypes.c_char, ctypes.c_char, i64, vp, i64, vp, vp, i64,
                                         vp, vp, vp, vp, i64, i64, i64, i64, vp, i64, vp]),
+            "spg_act_workspace_bytes": (i64, [i32, i64, i64, i64, i32]),
+            "fp8_rowscaled_linear_bf16": (st, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                               vp, i64, vp]),
+            "nvfp4_linear_bf16": (st, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
+                                       i64, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -117,7 +123,7 @@ def load_library():
         return lib
 
 
-_FORCE_VARS = ("SPG_FORCE_VARIANT", "SPG_FORCE_TAIL")
+_FORCE_VARS = ("SPG_FORCE_VARIANT", "SPG_FORCE_TAIL", "SPG_FORCE_GROUP_M")
 _forced_seen = None
 
 
@@ -424,6 +430,81 @@ def nvfp4_gemm(A, sfA, gA, W, sfW, gW, residual=None, epilogue="linear", out=Non
                                             _ptr(gW), _ptr(bias), _ptr(bias_scale), res,
                                             _ptr(out), T, N, K, e, _stream(A))
     _check(st, "nvfp4_gemm")
+    return out
+
+
+_ACT_KINDS = {"fp8_rowscaled": 0, "nvfp4": 1}
+
+
+def act_workspace_bytes(kind, T, N, K, epilogue="linear") -> int:
+    """Bytes of workspace the activation operators take (0: none needed)."""
+    return int(load_library().spg_act_workspace_bytes(_ACT_KINDS[kind], T, N, K,
+                                                      _epi(epilogue)))
+
+
+def act_workspace(kind, T, N, K, epilogue="linear", device="cuda"):
+    """A workspace tensor (uint8) for the activation operators, or None when
+    the call needs none."""
+    n = act_workspace_bytes(kind, T, N, K, epilogue)
+    return torch.empty((n,), dtype=torch.uint8, device=device) if n > 0 else None
+
+
+def _act_common(X, N, epilogue, residual, out, bias, bias_scale):
+    _need(X, "X", torch.bfloat16, 2)
+    T, K = X.shape
+    e = _epi(epilogue)
+    if e == 1:
+        _need(residual, "residual", torch.bfloat16, 2)
+        if tuple(residual.shape) != (T, N):
+            raise ValueError("residual must be [T, N]")
+    n_out = N // 2 if e == 2 else N
+    out = torch.empty((T, n_out), dtype=torch.bfloat16, device=X.device) if out is None else out
+    _need(out, "out", torch.bfloat16, 2)
+    _check_bias(bias, bias_scale, N)
+    return T, K, e, out
+
+
+def fp8_rowscaled_linear_bf16(X, W, sw, residual=None, epilogue="linear", out=None, bias=None,
+                              bias_scale=None, workspace=None):
+    """The FP8 row-scaled operator on bf16 activations X [T, K]: per-row
+    quantization of X, then the GEMM (workspace: act_workspace(...), made
+    here when not given)."""
+    _need(W, "W", torch.uint8, 2)
+    _need(sw, "sw", torch.float32)
+    N = W.shape[0]
+    T, K, e, out = _act_common(X, N, epilogue, residual, out, bias, bias_scale)
+    if W.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if workspace is None:
+        workspace = act_workspace("fp8_rowscaled", T, N, K, epilogue, device=X.device)
+    wp, wn = _ws(workspace)
+    st = _lib_for_call().fp8_rowscaled_linear_bf16(
+        _ptr(X), _ptr(W), _ptr(sw), _ptr(bias), _ptr(bias_scale),
+        _ptr(residual if e == 1 else None), _ptr(out), T, N, K, e, wp, wn, _stream(X))
+    _check(st, "fp8_rowscaled_linear_bf16")
+    return out
+
+
+def nvfp4_linear_bf16(X, W, sfW, gW, residual=None, epilogue="linear", out=None, bias=None,
+                      bias_scale=None, workspace=None):
+    """The NVFP4 operator on bf16 activations X [T, K]: global scale, block
+    quantization of X, then the block-scaled GEMM -- one kernel at T <= 4
+    (workspace: act_workspace(...), made here when not given)."""
+    for t, n, d in ((W, "W", torch.uint8), (sfW, "sfW", torch.uint8), (gW, "gW", torch.float32)):
+        _need(t, n, d)
+    N = W.shape[0]
+    T, K, e, out = _act_common(X, N, epilogue, residual, out, bias, bias_scale)
+    if 2 * W.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if sfW.numel() < nvfp4_sf_bytes(N, K):
+        raise ValueError("weight scale buffer smaller than the blocked layout")
+    if workspace is None:
+        workspace = act_workspace("nvfp4", T, N, K, epilogue, device=X.device)
+    wp, wn = _ws(workspace)
+    st = _lib_for_call().nvfp4_linear_bf16(
+        _ptr(X), _ptr(W), _ptr(sfW), _ptr(gW), _ptr(bias), _ptr(bias_scale),
+        _ptr(residual if e == 1 else None), _ptr(out), T, N, K, e, wp, wn, _stream(X))
+    _check(st, "nvfp4_linear_bf16")
     return out
 
 

@@ -8,33 +8,6 @@ using namespace spg;
 
 namespace {
 
-template <int EPI, int TT>
-spg_status launch_gemv(const GemvParams& p, cudaStream_t s) {
-  const int grid = (p.N / 2 + 3) / 4;  // one warp per weight-row pair, 4 per CTA
-  const int64_t smem = gemv_smem_bytes(TT, p.K);  // <= 200 KB (the route checks)
-  auto kern = gemv_nvfp4_kernel<EPI, TT>;
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         200 * 1024),
-                    "cudaFuncSetAttribute") != SPG_OK)
-      return SPG_ERR_CUDA;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
-  }
-  kern<<<grid, 128, static_cast<size_t>(smem), s>>>(p);
-  return launch_status();
-}
-
-template <int EPI>
-spg_status launch_gemv_tokens(const GemvParams& p, cudaStream_t s) {
-  if (p.T == 1) return launch_gemv<EPI, 1>(p, s);
-  if (p.T == 2) return launch_gemv<EPI, 2>(p, s);
-  return launch_gemv<EPI, 4>(p, s);
-}
-
 template <int EPI>
 spg_status launch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cudaStream_t s) {
   if (r.block_m == 256 && r.variant == 5) {
@@ -82,6 +55,7 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
     g.A = A;
     g.sfA = sfA;
     g.gA = gA;
+    g.X = nullptr;
     g.W = W;
     g.sfW = sfW;
     g.gW = gW;
@@ -100,11 +74,7 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
     g.N = static_cast<int>(N);
     g.K = static_cast<int>(K);
     g.n_out = static_cast<int>(epilogue == SPG_EPI_SWIGLU ? N / 2 : N);
-    switch (epilogue) {
-      case SPG_EPI_LINEAR: return launch_gemv_tokens<SPG_EPI_LINEAR>(g, stream);
-      case SPG_EPI_ADD: return launch_gemv_tokens<SPG_EPI_ADD>(g, stream);
-      default: return launch_gemv_tokens<SPG_EPI_SWIGLU>(g, stream);
-    }
+    return launch_gemv_epilogue(g, epilogue, stream);
   }
   const int64_t kh = K / 2;
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;

@@ -24,7 +24,13 @@
 
 #include <cuda_bf16.h>
 
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.h"
+#include "nvfp4_encode.cuh"
 #include "ptx.cuh"
 
 namespace spg {
@@ -33,6 +39,11 @@ struct GemvParams {
   const uint8_t* A;    // [T, K/2] codes
   const uint8_t* sfA;  // blocked scales of A
   const float* gA;
+  // bf16 [T, K] activations, or nullptr.  When set, A / sfA / gA are unused:
+  // every CTA quantizes X itself (global scale, block scales, codes) into
+  // its shared memory, so the GEMV is the whole quantize-and-multiply
+  // operator in one launch.
+  const __nv_bfloat16* X;
   const uint8_t* W;    // [N, K/2] codes
   const uint8_t* sfW;  // blocked scales of W
   const float* gW;
@@ -80,6 +91,31 @@ __device__ __forceinline__ float gemv_bias(const GemvParams& p, int n) {
   return __fmul_rn(e4m3x2_to_float2(uint16_t(c | (c << 8))).x, __ldg(p.bias_scale));
 }
 
+// CTAs per cluster of the operator form (bf16 activations quantized in the
+// kernel): the cluster shares one quantization of X through distributed
+// shared memory.  The kernel reads the cluster size it was launched with
+// (at most kGemvMaxCluster).
+constexpr int kGemvCluster = 4;  // measured against 8 on GB300: equal or faster on every decode shape
+constexpr int kGemvMaxCluster = 8;
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b)
+               : "memory");
+}
+
 // Shared-memory bytes of the decoded activations of one CTA: per token two
 // planes of K/32 16-byte words (the int8 of each chunk's two blocks) and
 // K/32 float2 (the two blocks' scales).
@@ -100,122 +136,278 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
   const int kt = p.K / 64;
   uint4* aq_s = gemv_smem;  // [TT][2][nchunks]
   float2* sa_s = reinterpret_cast<float2*>(gemv_smem + 2 * TT * nchunks);  // [TT][nchunks]
-  for (int i = threadIdx.x; i < p.T * nchunks; i += blockDim.x) {
-    const int t = i / nchunks;
-    const int c = i - t * nchunks;
-    uint32_t q[8];
-    decode_chunk(__ldg(reinterpret_cast<const uint4*>(p.A + int64_t(t) * kh) + c), q);
-    aq_s[(t * 2) * nchunks + c] = make_uint4(q[0], q[1], q[2], q[3]);
-    aq_s[(t * 2 + 1) * nchunks + c] = make_uint4(q[4], q[5], q[6], q[7]);
-    sa_s[t * nchunks + c] = e4m3x2_to_float2(__ldg(reinterpret_cast<const unsigned short*>(
-        p.sfA + gemv_sf_row_offset(t, kt) + (c >> 1) * 512 + (c & 1) * 2)));
+  __shared__ float red_s[4];
+  __shared__ float amax_s[kGemvMaxCluster];
+  float g_act = 0.f;
+  if (p.X) {
+    // The operator form, launched in clusters of ncta CTAs: CTA `rank`
+    // takes every ncta-th share of X.  (1) Each CTA's share
+    // maximum goes to every CTA of the cluster; after a cluster barrier all
+    // of them hold the same global scale.  (2) Each CTA encodes its share
+    // of the 32-element chunks exactly as the block quantizer does, decodes
+    // them, and stores the int8 planes and block scales into the shared
+    // memory of every CTA of the cluster; a second barrier publishes them.
+    // A cluster spans the whole of X, so each cluster quantizes X once.
+    const uint32_t rank = cluster_ctarank();
+    const int ncta = int(cluster_nctarank());
+    {
+      // Start the warp's first two weight rows (contiguous) on their way
+      // into L2 while the activations are quantized.
+      const int pair0 = blockIdx.x * 4 + (threadIdx.x >> 5);
+      if (pair0 * 2 < p.N) {
+        const uint8_t* rows = p.W + int64_t(pair0) * 2 * kh;
+        for (int off = lane * 128; off < 2 * kh; off += 32 * 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rows + off));
+      }
+    }
+    const uint4* xv = reinterpret_cast<const uint4*>(p.X);
+    const int nvec = p.T * (p.K / 8);
+    float a = 0.f;
+    for (int i = int(rank) * blockDim.x + threadIdx.x; i < nvec; i += ncta * blockDim.x)
+      a = fmaxf(a, bf16x8_amax(__ldg(xv + i)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) red_s[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (int(threadIdx.x) < ncta) {
+      const float m = fmaxf(fmaxf(red_s[0], red_s[1]), fmaxf(red_s[2], red_s[3]));
+      st_cluster_u32(mapa_shared(smem_u32(&amax_s[rank]), threadIdx.x), __float_as_uint(m));
+    }
+    cluster_sync();
+    float m = 0.f;
+    for (int r = 0; r < ncta; ++r) m = fmaxf(m, amax_s[r]);
+    g_act = nvfp4_global_from_amax(m);
+    const uint32_t aq_base = smem_u32(aq_s), sa_base = smem_u32(sa_s);
+    for (int i = int(rank) + ncta * int(threadIdx.x); i < p.T * nchunks;
+         i += ncta * blockDim.x) {
+      const int t = i / nchunks;
+      const int c = i - t * nchunks;
+      const uint4* src = xv + (int64_t(t) * p.K + int64_t(c) * 32) / 8;
+      uint4 codes;
+      float2 sa;
+      nvfp4_encode_block(__ldg(src), __ldg(src + 1), g_act, codes.x, codes.y, &sa.x);
+      nvfp4_encode_block(__ldg(src + 2), __ldg(src + 3), g_act, codes.z, codes.w, &sa.y);
+      uint32_t q[8];
+      decode_chunk(codes, q);
+      const uint32_t o0 = aq_base + uint32_t((t * 2) * nchunks + c) * 16u;
+      const uint32_t o1 = aq_base + uint32_t((t * 2 + 1) * nchunks + c) * 16u;
+      const uint32_t os = sa_base + uint32_t(t * nchunks + c) * 8u;
+      for (int r = 0; r < ncta; ++r) {
+        st_cluster_v4(mapa_shared(o0, r), q[0], q[1], q[2], q[3]);
+        st_cluster_v4(mapa_shared(o1, r), q[4], q[5], q[6], q[7]);
+        st_cluster_v2(mapa_shared(os, r), __float_as_uint(sa.x), __float_as_uint(sa.y));
+      }
+    }
+    cluster_sync();
+  } else {
+    for (int i = threadIdx.x; i < p.T * nchunks; i += blockDim.x) {
+      const int t = i / nchunks;
+      const int c = i - t * nchunks;
+      uint32_t q[8];
+      decode_chunk(__ldg(reinterpret_cast<const uint4*>(p.A + int64_t(t) * kh) + c), q);
+      aq_s[(t * 2) * nchunks + c] = make_uint4(q[0], q[1], q[2], q[3]);
+      aq_s[(t * 2 + 1) * nchunks + c] = make_uint4(q[4], q[5], q[6], q[7]);
+      sa_s[t * nchunks + c] = e4m3x2_to_float2(__ldg(reinterpret_cast<const unsigned short*>(
+          p.sfA + gemv_sf_row_offset(t, kt) + (c >> 1) * 512 + (c & 1) * 2)));
+    }
   }
   __syncthreads();
 
-  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (pair * 2 >= p.N) return;  // warp-uniform, after the CTA's only barrier
-  const int n0 = pair * 2;
-  const uint4* w0 = reinterpret_cast<const uint4*>(p.W + int64_t(n0) * kh);
-  const uint4* w1 = reinterpret_cast<const uint4*>(p.W + int64_t(n0 + 1) * kh);
-  const int sw0 = gemv_sf_row_offset(n0, kt);
-  const int sw1 = gemv_sf_row_offset(n0 + 1, kt);
-  float acc[2][TT];
+  // One weight-row pair per warp.  In the operator form the grid is one
+  // resident wave and the warps stride over the pairs, so the in-kernel
+  // quantization is paid once per CTA; otherwise the loop runs once.
+  for (int pair = blockIdx.x * 4 + (threadIdx.x >> 5); pair * 2 < p.N; pair += gridDim.x * 4) {
+    const int n0 = pair * 2;
+    const uint4* w0 = reinterpret_cast<const uint4*>(p.W + int64_t(n0) * kh);
+    const uint4* w1 = reinterpret_cast<const uint4*>(p.W + int64_t(n0 + 1) * kh);
+    const int sw0 = gemv_sf_row_offset(n0, kt);
+    const int sw1 = gemv_sf_row_offset(n0 + 1, kt);
+    float acc[2][TT];
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-    for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
+      for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
 
-  for (int c0 = lane; c0 < nchunks; c0 += 32 * kUnroll) {
-    // The weight stream of kUnroll chunks first (read once: evict-first).
-    uint4 wv[kUnroll][2];
-    uint16_t ws[kUnroll][2];
+    for (int c0 = lane; c0 < nchunks; c0 += 32 * kUnroll) {
+      // The weight stream of kUnroll chunks first (read once: evict-first).
+      uint4 wv[kUnroll][2];
+      uint16_t ws[kUnroll][2];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int c = c0 + 32 * u;
-      if (c < nchunks) {
-        const int so = (c >> 1) * 512 + (c & 1) * 2;
-        wv[u][0] = __ldcs(w0 + c);
-        wv[u][1] = __ldcs(w1 + c);
-        ws[u][0] = __ldg(reinterpret_cast<const unsigned short*>(p.sfW + sw0 + so));
-        ws[u][1] = __ldg(reinterpret_cast<const unsigned short*>(p.sfW + sw1 + so));
-      } else {
-        wv[u][0] = wv[u][1] = make_uint4(0u, 0u, 0u, 0u);
-        ws[u][0] = ws[u][1] = 0;
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < nchunks) {
+          const int so = (c >> 1) * 512 + (c & 1) * 2;
+          wv[u][0] = __ldcs(w0 + c);
+          wv[u][1] = __ldcs(w1 + c);
+          ws[u][0] = __ldg(reinterpret_cast<const unsigned short*>(p.sfW + sw0 + so));
+          ws[u][1] = __ldg(reinterpret_cast<const unsigned short*>(p.sfW + sw1 + so));
+        } else {
+          wv[u][0] = wv[u][1] = make_uint4(0u, 0u, 0u, 0u);
+          ws[u][0] = ws[u][1] = 0;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= nchunks) break;
+        uint32_t wq[2][8];
+        decode_chunk(wv[u][0], wq[0]);
+        decode_chunk(wv[u][1], wq[1]);
+        const float2 sw[2] = {e4m3x2_to_float2(ws[u][0]), e4m3x2_to_float2(ws[u][1])};
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          if (t >= p.T) break;
+          const uint4 a0 = aq_s[(t * 2) * nchunks + c];
+          const uint4 a1 = aq_s[(t * 2 + 1) * nchunks + c];
+          const float2 sa = sa_s[t * nchunks + c];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            int d0 = __dp4a(int(a0.x), int(wq[r][0]), 0);
+            d0 = __dp4a(int(a0.y), int(wq[r][1]), d0);
+            d0 = __dp4a(int(a0.z), int(wq[r][2]), d0);
+            d0 = __dp4a(int(a0.w), int(wq[r][3]), d0);
+            int d1 = __dp4a(int(a1.x), int(wq[r][4]), 0);
+            d1 = __dp4a(int(a1.y), int(wq[r][5]), d1);
+            d1 = __dp4a(int(a1.z), int(wq[r][6]), d1);
+            d1 = __dp4a(int(a1.w), int(wq[r][7]), d1);
+            acc[r][t] = fmaf(float(d0), sa.x * sw[r].x, acc[r][t]);
+            acc[r][t] = fmaf(float(d1), sa.y * sw[r].y, acc[r][t]);
+          }
+        }
       }
     }
+
+    // Sum over the lanes (every lane ends with the totals).
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int c = c0 + 32 * u;
-      if (c >= nchunks) break;
-      uint32_t wq[2][8];
-      decode_chunk(wv[u][0], wq[0]);
-      decode_chunk(wv[u][1], wq[1]);
-      const float2 sw[2] = {e4m3x2_to_float2(ws[u][0]), e4m3x2_to_float2(ws[u][1])};
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
+
+    const float s = (p.X ? g_act : __ldg(p.gA)) * __ldg(p.gW);
+    if constexpr (EPI == SPG_EPI_SWIGLU) {
+      // rows n0 (gate) and n0 + 1 (up) give output column n0 / 2
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
-        if (t >= p.T) break;
-        const uint4 a0 = aq_s[(t * 2) * nchunks + c];
-        const uint4 a1 = aq_s[(t * 2 + 1) * nchunks + c];
-        const float2 sa = sa_s[t * nchunks + c];
+        if (lane == t && t < p.T) {
+          float gate = (acc[0][t] * 0.25f) * s;
+          float up = (acc[1][t] * 0.25f) * s;
+          if (p.bias_kind) {
+            gate += gemv_bias(p, n0);
+            up += gemv_bias(p, n0 + 1);
+          }
+          const float o = __fdividef(gate, 1.f + __expf(-gate)) * up;
+          p.Y[int64_t(t) * p.n_out + pair] = __float2bfloat16_rn(o);
+        }
+      }
+    } else {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          int d0 = __dp4a(int(a0.x), int(wq[r][0]), 0);
-          d0 = __dp4a(int(a0.y), int(wq[r][1]), d0);
-          d0 = __dp4a(int(a0.z), int(wq[r][2]), d0);
-          d0 = __dp4a(int(a0.w), int(wq[r][3]), d0);
-          int d1 = __dp4a(int(a1.x), int(wq[r][4]), 0);
-          d1 = __dp4a(int(a1.y), int(wq[r][5]), d1);
-          d1 = __dp4a(int(a1.z), int(wq[r][6]), d1);
-          d1 = __dp4a(int(a1.w), int(wq[r][7]), d1);
-          acc[r][t] = fmaf(float(d0), sa.x * sw[r].x, acc[r][t]);
-          acc[r][t] = fmaf(float(d1), sa.y * sw[r].y, acc[r][t]);
+      for (int r = 0; r < 2; ++r) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          if (lane == r * TT + t && t < p.T) {
+            const int n = n0 + r;
+            float v = (acc[r][t] * 0.25f) * s;
+            if (p.bias_kind) v += gemv_bias(p, n);
+            if constexpr (EPI == SPG_EPI_ADD)
+              v += __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(
+                                                      p.residual) +
+                                                  int64_t(t) * p.N + n))
+                                   << 16);
+            p.Y[int64_t(t) * p.n_out + n] = __float2bfloat16_rn(v);
+          }
         }
       }
     }
   }
+}
 
-  // Sum over the lanes (every lane ends with the totals).
-#pragma unroll
-  for (int r = 0; r < 2; ++r)
-#pragma unroll
-    for (int t = 0; t < TT; ++t)
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
+// Clusters of the operator form that fit on the device at once for this
+// launch configuration (0 if the query fails), cached per kernel and
+// shared-memory size.
+template <typename Kern>
+int gemv_cluster_wave(Kern kern, const cudaLaunchConfig_t& cfg) {
+  static std::mutex mu;
+  static std::map<std::pair<int, size_t>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_pair(dev, cfg.dynamicSmemBytes);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
 
-  const float s = __ldg(p.gA) * __ldg(p.gW);
-  if constexpr (EPI == SPG_EPI_SWIGLU) {
-    // rows n0 (gate) and n0 + 1 (up) give output column n0 / 2
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      if (lane == t && t < p.T) {
-        float gate = (acc[0][t] * 0.25f) * s;
-        float up = (acc[1][t] * 0.25f) * s;
-        if (p.bias_kind) {
-          gate += gemv_bias(p, n0);
-          up += gemv_bias(p, n0 + 1);
-        }
-        const float o = __fdividef(gate, 1.f + __expf(-gate)) * up;
-        p.Y[int64_t(t) * p.n_out + pair] = __float2bfloat16_rn(o);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        if (lane == r * TT + t && t < p.T) {
-          const int n = n0 + r;
-          float v = (acc[r][t] * 0.25f) * s;
-          if (p.bias_kind) v += gemv_bias(p, n);
-          if constexpr (EPI == SPG_EPI_ADD)
-            v += __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(
-                                                    p.residual) +
-                                                int64_t(t) * p.N + n))
-                                 << 16);
-          p.Y[int64_t(t) * p.n_out + n] = __float2bfloat16_rn(v);
-        }
-      }
-    }
+// Launch: one warp per weight-row pair, 4 warps per CTA; the dynamic shared
+// memory limit is raised once per device.
+template <int EPI, int TT>
+spg_status launch_gemv(const GemvParams& p, cudaStream_t s) {
+  int grid = (p.N / 2 + 3) / 4;
+  const int64_t smem = gemv_smem_bytes(TT, p.K);  // <= 200 KB (the route checks)
+  auto kern = gemv_nvfp4_kernel<EPI, TT>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024),
+                    "cudaFuncSetAttribute") != SPG_OK)
+      return SPG_ERR_CUDA;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  if (!p.X) {
+    kern<<<grid, 128, static_cast<size_t>(smem), s>>>(p);
+    return launch_status();
+  }
+  // Operator form: clusters of kGemvCluster CTAs, at most one resident wave
+  // of them (the warps stride over the row pairs).  CTAs without a row pair
+  // only take their share of the quantization.
+  grid = (grid + kGemvCluster - 1) / kGemvCluster * kGemvCluster;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kGemvCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // More CTAs than one wave holds: take R = ceil(CTAs / wave) rounds of
+  // pairs per warp and just enough CTAs for them (fewer CTAs also quantize
+  // X fewer times).
+  const int wave = gemv_cluster_wave(kern, cfg) * kGemvCluster;
+  if (wave > 0 && grid > wave) {
+    const int pairs = p.N / 2;
+    const int rounds = (grid + wave - 1) / wave;
+    const int ctas = ((pairs + rounds - 1) / rounds + 3) / 4;
+    cfg.gridDim = dim3((ctas + kGemvCluster - 1) / kGemvCluster * kGemvCluster);
+  }
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, p), "cudaLaunchKernelEx");
+}
+
+template <int EPI>
+spg_status launch_gemv_tokens(const GemvParams& p, cudaStream_t s) {
+  if (p.T == 1) return launch_gemv<EPI, 1>(p, s);
+  if (p.T == 2) return launch_gemv<EPI, 2>(p, s);
+  return launch_gemv<EPI, 4>(p, s);
+}
+
+inline spg_status launch_gemv_epilogue(const GemvParams& p, int epilogue, cudaStream_t s) {
+  switch (epilogue) {
+    case SPG_EPI_LINEAR: return launch_gemv_tokens<SPG_EPI_LINEAR>(p, s);
+    case SPG_EPI_ADD: return launch_gemv_tokens<SPG_EPI_ADD>(p, s);
+    default: return launch_gemv_tokens<SPG_EPI_SWIGLU>(p, s);
   }
 }
 

@@ -211,14 +211,15 @@ void tmap_cache_stats(uint64_t* hits, uint64_t* misses) {
 }
 
 // ------------------------------------------------------------ forced routes
-// SPG_FORCE_VARIANT / SPG_FORCE_TAIL pin a tile shape or a tail split for
-// A/B runs and tests.  They are read from the environment once, on first
+// SPG_FORCE_VARIANT / SPG_FORCE_TAIL pin a tile shape or a tail split, and
+// SPG_FORCE_GROUP_M the rasterization group, for A/B runs and tests.  They are read from the environment once, on first
 // use, and again only when spg_debug_reload_env() is called, so the
 // selector does no environment lookup per call.
 namespace {
 struct ForcedRoute {
   char variant[32];
   char tail[16];
+  int group_m;  // SPG_FORCE_GROUP_M: m-blocks per rasterization group (0: the default)
 };
 std::mutex g_forced_mu;
 ForcedRoute g_forced;
@@ -238,6 +239,9 @@ ForcedRoute forced_route() {
   if (!g_forced_loaded) {
     copy_env(g_forced.variant, sizeof g_forced.variant, "SPG_FORCE_VARIANT");
     copy_env(g_forced.tail, sizeof g_forced.tail, "SPG_FORCE_TAIL");
+    const char* gm = std::getenv("SPG_FORCE_GROUP_M");
+    g_forced.group_m = gm ? std::atoi(gm) : 0;
+    if (g_forced.group_m < 0 || g_forced.group_m > 4096) g_forced.group_m = 0;
     g_forced_loaded = true;
   }
   return g_forced;
@@ -288,6 +292,10 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   r.kind = kind;
   r.acc_buffers = 2;
   r.group_m = 16;
+  {
+    const ForcedRoute f = forced_route();
+    if (f.group_m > 0) r.group_m = f.group_m;
+  }
   const int sms = num_sms();
   const int pairs = sms / 2;
   const int64_t nb = batch > 0 ? batch : 1;

@@ -1,0 +1,63 @@
+// NVFP4 encoding of bf16 values, shared by the block quantizer and by the
+// GEMV that quantizes its activations itself.
+//
+// ninfer PR #160 "The NVFP4 TMA route reads activation scales as one tile"
+// (E2M1 codes, one E4M3 scale per 16 elements, activations quantized too),
+// with the two-level scale the global scale g adds: per 16-element block
+//   sf   = E4M3_rne_satfinite((amax_b / 6) / g)      two IEEE divisions
+//   d    = dec(sf) * g                                 one IEEE multiply
+//   code = E2M1_rne_satfinite(x / d)                   0 when d == 0
+// and g = amax / (448 * 6) over the whole tensor (1 when amax == 0).  Every
+// fp32 step is one IEEE-rounded operation, so the codes and scales are bit
+// for bit those of the plain definition.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace spg {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max |x| over eight bf16 values.
+__device__ __forceinline__ float bf16x8_amax(const uint4& v) {
+  float a = 0.f;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  return a;
+}
+
+// The global scale from the tensor's amax.
+__device__ __forceinline__ float nvfp4_global_from_amax(float amax) {
+  return (amax == 0.f) ? 1.f : __fdiv_rn(amax, 2688.f);
+}
+
+// One 16-element block (v0: elements 0-7, v1: 8-15) with global scale g:
+// its eight code bytes (element i in nibble i of the 64 bits, low word
+// first) and its E4M3 scale byte; *dec receives the scale's exact value.
+__device__ __forceinline__ uint32_t nvfp4_encode_block(const uint4& v0, const uint4& v1, float g,
+                                                       uint32_t& code_lo, uint32_t& code_hi,
+                                                       float* dec) {
+  const float amax_b = fmaxf(bf16x8_amax(v0), bf16x8_amax(v1));
+  const float t = __fdiv_rn(__fdiv_rn(amax_b, 6.f), g);
+  const uint32_t sfc = cvt_e4m3x2(t, t) & 0xFFu;
+  const float2 dd = e4m3x2_to_float2(static_cast<uint16_t>(sfc));  // one byte is zero
+  const float sv = fmaxf(dd.x, dd.y);
+  const float d = __fmul_rn(sv, g);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
+    q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
+  }
+  code_lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
+  code_hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));
+  *dec = sv;
+  return sfc;
+}
+
+}  // namespace spg

@@ -16,21 +16,13 @@
 #include <mutex>
 
 #include "common.h"
+#include "nvfp4_encode.cuh"
 #include "ptx.cuh"
 
 namespace spg {
 namespace {
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ float vec_amax(const uint4& v) {
-  float a = 0.f;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-  return a;
-}
+__device__ __forceinline__ float vec_amax(const uint4& v) { return bf16x8_amax(v); }
 
 // Eight bf16 divided by s (IEEE) -> eight E4M3 codes.
 __device__ __forceinline__ uint2 vec_encode_e4m3(const uint4& v, float s) {
@@ -132,8 +124,7 @@ __global__ void __launch_bounds__(256) encode_fp8_tensor_kernel(const uint4* __r
 
 // g = amax / (448 * 6), 1 when amax = 0.
 __global__ void nvfp4_global_finalize_kernel(const float* __restrict__ amax, float* __restrict__ g) {
-  const float a = *amax;
-  *g = (a == 0.f) ? 1.f : __fdiv_rn(a, 2688.f);
+  *g = nvfp4_global_from_amax(*amax);
 }
 
 // NVFP4 block quantizer.  One thread per 64 consecutive elements of a row
@@ -159,24 +150,10 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
   uint32_t* ow = reinterpret_cast<uint32_t*>(out);
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const uint4 v0 = __ldg(xp + 2 * b), v1 = __ldg(xp + 2 * b + 1);
-    const float amax_b = fmaxf(vec_amax(v0), vec_amax(v1));
-    const float t = __fdiv_rn(__fdiv_rn(amax_b, 6.f), g);
-    const uint32_t sfc = cvt_e4m3x2(t, t) & 0xFFu;
+    float dec;
+    const uint32_t sfc = nvfp4_encode_block(__ldg(xp + 2 * b), __ldg(xp + 2 * b + 1), g,
+                                            ow[2 * b], ow[2 * b + 1], &dec);
     sf_bytes |= sfc << (8 * b);
-    const float2 dec = e4m3x2_to_float2(static_cast<uint16_t>(sfc));  // one byte is zero
-    const float d = __fmul_rn(fmaxf(dec.x, dec.y), g);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float q[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
-      q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
-    }
-    const float(&q0)[8] = *reinterpret_cast<const float(*)[8]>(&q[0]);
-    const float(&q1)[8] = *reinterpret_cast<const float(*)[8]>(&q[8]);
-    ow[2 * b] = cvt_e2m1x8(q0);
-    ow[2 * b + 1] = cvt_e2m1x8(q1);
   }
   uint4* cp = codes + (r * (K / 2) + cb * 32) / 16;
   cp[0] = out[0];

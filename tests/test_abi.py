@@ -127,6 +127,33 @@ def test_route_selector_gemv(lib, monkeypatch):
     assert spg.select_route("nvfp4", 5, 5120, 17408, "add")["variant"] != 4
 
 
+def test_act_workspace_sizes(lib, monkeypatch):
+    """The activation operators' workspace: none for the fused NVFP4 decode
+    kernel; otherwise the activation codes and scales (256-byte aligned
+    pieces) followed by the GEMM's own K-split workspace."""
+    for v in ("SPG_FORCE_VARIANT", "SPG_FORCE_TAIL", "SPG_FORCE_GROUP_M"):
+        monkeypatch.delenv(v, raising=False)
+    up = lambda v: (v + 255) // 256 * 256
+    # the fused decode kernel: wide N at T <= 4, or one token with K <= 8192
+    for T in (1, 2, 3, 4):
+        assert spg.act_workspace_bytes("nvfp4", T, 34816, 5120, "swiglu") == 0
+    assert spg.act_workspace_bytes("nvfp4", 1, 5120, 6144, "add") == 0
+    for T, N, K, epi in [(1, 5120, 17408, "add"), (2, 5120, 6144, "add"),
+                         (5, 5120, 17408, "add"), (64, 5120, 6144, "add"),
+                         (8192, 34816, 5120, "swiglu")]:
+        need = 256 + up(T * K // 2) + up(spg.nvfp4_sf_bytes(T, K))
+        assert spg.act_workspace_bytes("nvfp4", T, N, K, epi) == \
+            need + spg.gemm_workspace_bytes("nvfp4", T, N, K, epi)
+    for T, N, K, epi in [(1, 5120, 17408, "add"), (1024, 5120, 17408, "add"),
+                         (4096, 34816, 5120, "swiglu")]:
+        need = up(T * K) + up(4 * T)
+        assert spg.act_workspace_bytes("fp8_rowscaled", T, N, K, epi) == \
+            need + spg.gemm_workspace_bytes("fp8_rowscaled", T, N, K, epi)
+    assert lib.spg_act_workspace_bytes(2, 64, 64, 64, 0) == 0      # per-tensor: no operator
+    assert lib.spg_act_workspace_bytes(1, 64, 64, 96, 0) == 0      # NVFP4 K % 64
+    assert lib.spg_act_workspace_bytes(0, 0, 64, 64, 0) == 0
+
+
 def test_route_selector_swap(lib, monkeypatch):
     """The swapped narrow-T tile: FP8 row-scaled, one problem, linear or
     linear_add, T <= 128; token tile 64 or 128 wide, weights in 256-row tiles."""

@@ -86,10 +86,10 @@ def test_nvfp4_explicit_global_scale():
 
 
 # ---------------------------------------------------------------------------
-# The quantizers take each code from x * fl(1/s) and fall back to the exact
-# quotient only near a point where the code's rounding changes.  These cases
-# put quotients exactly on and around those points, in the subnormal E4M3
-# range, and behind a subnormal scale (whose reciprocal overflows).
+# Quotients x / s placed exactly on and around the points where a code's
+# rounding changes (ties to even), in the subnormal E4M3 range, and behind a
+# subnormal scale: any encoder that forms the quotient other than as one
+# IEEE-rounded division fails here first.
 
 def _bf16_rows(rows_f32):
     return f32_to_bf16_bits(np.asarray(rows_f32, np.float32))
