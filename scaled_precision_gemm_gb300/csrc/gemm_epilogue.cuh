@@ -165,13 +165,29 @@ __device__ __forceinline__ uint32_t split_piece_finish(const GemmParams& p, uint
 // kernels only, cta_rank: this CTA's rank in the pair) go through
 // split_piece_finish first and then run the epilogue on the chunks whose
 // total they hold.
-template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty>
+// RES_TMA (linear_add): the residual of each 32 x 32 output block comes by a
+// TMA copy (tmR, 32 x 32 boxes, the output's swizzle) into the warp's
+// staging buffer, one chunk ahead -- the first chunk's before the
+// accumulator is ready -- and the output is computed in place and stored
+// from the same buffer (res_bars: two mbarriers per epilogue warp, one per
+// buffer).  Without it each thread loads its row's residual with 16-byte
+// loads, 32 rows apart across the warp.  On the CTA's last item nothing
+// follows to hide the chunk-by-chunk copies behind, so once that item's
+// accumulator is full (every MMA, hence every read of the operand ring, is
+// done, and no load into the ring remains) all of its residual blocks are
+// requested at once into the idle ring (idle_ring: BN/32 x 2 KB per warp)
+// and waited for together: one memory round trip instead of one per chunk.
+template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty, bool RES_TMA = false>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtensorMap* tmY,
                                               uint32_t tmem_base, uint64_t* acc_full,
                                               ArriveEmpty arrive_empty, uint8_t* epi_smem,
                                               int item_begin, int item_end, int item_step,
-                                              ItemFn item_fn, const WaitCtl& ctl, int cta_rank) {
+                                              ItemFn item_fn, const WaitCtl& ctl, int cta_rank,
+                                              const CUtensorMap* tmR = nullptr,
+                                              uint64_t* res_bars = nullptr,
+                                              uint8_t* idle_ring = nullptr) {
   using E = EpilogueCfg<EPI, SCALE, BN>;
+  constexpr bool kResTma = RES_TMA && EPI == SPG_EPI_ADD;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int e = warp - 2;
@@ -181,8 +197,22 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
   int chunk_ctr = 0;
   float scalar = 1.f;
   if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
+  // TMA residual: buffer of the copy in flight (-1: none) and the parity
+  // each buffer's barrier completes next.
+  int res_inflight = -1;
+  uint32_t res_ph = 0;
+  auto res_load = [&](int buf, int x, int y, int b) {
+    if (lane == 0) {
+      uint64_t* bar = &res_bars[e * 2 + buf];
+      mbar_arrive_expect_tx(bar, E::kBufBytes);
+      tma_load_3d(stage0 + buf * E::kBufBytes, tmR, bar, x, y, b);
+    }
+    res_inflight = buf;
+    __syncwarp();
+  };
+  bool aborted = false;
 
-  for (int item = item_begin; item < item_end; item += item_step, ++it) {
+  for (int item = item_begin; item < item_end && !aborted; item += item_step, ++it) {
     const int buf = it & 1;
     const uint32_t acc_ph = (it >> 1) & 1;
     const WorkItem tc = item_fn(item);
@@ -216,23 +246,41 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
     // Epilogue operands, requested before the accumulator is ready.
     float row_s = scalar;
     if constexpr (SCALE == kScaleRow) row_s = row_ok ? __ldg(p.row_scale + m) : 0.f;
-    float swr[E::kSwRegs];
-    if constexpr (SCALE == kScaleRow) {
-#pragma unroll
-      for (int j = 0; j < E::kSwRegs; ++j) {
-        const int n = n0 + 32 * j + lane;
-        swr[j] = (32 * j < tc.width && n < p.N) ? __ldg(p.col_scale + n) : 0.f;
-      }
-    }
-    float biasr[E::kSwRegs];
+    // Column scales and bias of one chunk per lane (lane j: column 32 i + j
+    // of the chunk's i-th 32 columns), the next chunk's requested while the
+    // current one is processed.  The chunk loop stays rolled: unrolled over
+    // all chunks its code outgrew the instruction cache, and with every CTA
+    // of a wave in the same chunk at once the refetches serialized.
+    constexpr int kCw = E::kAccColsPerChunk / 32;
     const bool has_bias = p.bias_kind != 0;
-    if (has_bias) {
+    auto chunk_cols = [&](int c, float (&sw)[kCw], float (&bi)[kCw]) {
 #pragma unroll
-      for (int j = 0; j < E::kSwRegs; ++j)
-        biasr[j] = 32 * j < tc.width ? load_bias(p, n0 + 32 * j + lane) : 0.f;
+      for (int j = 0; j < kCw; ++j) {
+        const int col = c * E::kAccColsPerChunk + 32 * j;  // inside the item
+        const int n = n0 + col + lane;
+        sw[j] = 1.f;
+        if constexpr (SCALE == kScaleRow) sw[j] = (col < tc.width && n < p.N) ? __ldg(p.col_scale + n) : 0.f;
+        bi[j] = (has_bias && col < tc.width) ? load_bias(p, n) : 0.f;
+      }
+    };
+    float swc[kCw], biasc[kCw];
+    {
+      const int c_first = own_mask == 0xffffffffu ? 0 : __ffs(own_mask) - 1;
+      chunk_cols(c_first, swc, biasc);
     }
     uint4 res_cur[4];
-    if constexpr (EPI == SPG_EPI_ADD) {
+    // The last item's residual comes whole into the idle operand ring.
+    const bool res_bulk = kResTma && !split_item && idle_ring != nullptr &&
+                          item + item_step >= item_end;
+    uint8_t* ring_w = idle_ring + e * (E::kChunks * E::kBufBytes);
+    if constexpr (kResTma) {
+      // The first chunk's block, into the buffer whose store of two chunks
+      // back must have been read.
+      if (!split_item && !res_bulk) {
+        if (lane == 0) bulk_wait_read<1>();
+        res_load(chunk_ctr & 1, n0, m0 + q * 32, tc.b);
+      }
+    } else if constexpr (EPI == SPG_EPI_ADD) {
       if (!split_item) load_residual_chunk(p, m, n0, row_ok, res_cur);
     }
 
@@ -240,12 +288,32 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
       tc_fence_after();
     }
+    if constexpr (kResTma) {
+      if (res_bulk) {
+        if (lane == 0) {
+          uint64_t* bar = &res_bars[e * 2];
+          mbar_arrive_expect_tx(bar, uint32_t(nch * E::kBufBytes));
+          for (int c = 0; c < nch; ++c)
+            tma_load_3d(ring_w + c * E::kBufBytes, tmR, bar, n0 + 32 * c, m0 + q * 32, tc.b);
+        }
+        res_inflight = 0;
+        __syncwarp();
+        if (!mbar_wait(&res_bars[e * 2], res_ph & 1u, ctl, kErrWaitFull)) break;
+        res_ph ^= 1u;
+        res_inflight = -1;
+      }
+    }
 
-#pragma unroll
+#pragma unroll 1
     for (int c = 0; c < E::kChunks; ++c) {
       if (c >= nch) break;
       if (!((own_mask >> c) & 1u)) continue;
       const int acc_c0 = c * E::kAccColsPerChunk;
+      // The next chunk this warp finishes: its column scales and bias now.
+      float swn[kCw], biasn[kCw];
+      const uint32_t later = (c + 1 < 32) ? (own_mask >> (c + 1)) : 0u;
+      const int c_next = later ? c + __ffs(later) : -1;
+      if (c_next >= 0 && c_next < nch) chunk_cols(c_next, swn, biasn);
       if constexpr (EPI == SPG_EPI_ADD) {
         // A K-split piece finishes scattered chunks: load each one's residual.
         if (split_item) load_residual_chunk(p, m, n0 + acc_c0, row_ok, res_cur);
@@ -260,7 +328,32 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         for (int i = 0; i < E::kAccColsPerChunk; ++i) raw[i] = 0u;
       }
       uint4 res_next[4];
-      if constexpr (EPI == SPG_EPI_ADD) {
+      if constexpr (kResTma) {
+        if (res_bulk) {
+          const uint8_t* rbuf = ring_w + c * E::kBufBytes + lane * 64;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            res_cur[g] = *reinterpret_cast<const uint4*>(rbuf + ((g ^ ((lane >> 1) & 3)) * 16));
+        } else if (!split_item) {
+          // This chunk's block, then the next one into the other buffer once
+          // that buffer's store has been read.
+          const int rb = chunk_ctr & 1;
+          if (!mbar_wait(&res_bars[e * 2 + rb], (res_ph >> rb) & 1u, ctl, kErrWaitFull)) {
+            aborted = true;
+            break;
+          }
+          res_ph ^= 1u << rb;
+          res_inflight = -1;
+          if (c + 1 < nch) {
+            if (lane == 0) bulk_wait_read<0>();
+            res_load(rb ^ 1, n0 + acc_c0 + 32, m0 + q * 32, tc.b);
+          }
+          const uint8_t* rbuf = stage0 + rb * E::kBufBytes + lane * 64;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            res_cur[g] = *reinterpret_cast<const uint4*>(rbuf + ((g ^ ((lane >> 1) & 3)) * 16));
+        }
+      } else if constexpr (EPI == SPG_EPI_ADD) {
         if (!split_item && c + 1 < nch) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
       }
       if (have_k) tmem_wait_ld();
@@ -276,7 +369,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         float s = row_s;
         if constexpr (SCALE == kScaleRow) {
           const int col = acc_c0 + i;  // column inside the tile
-          s = row_s * __shfl_sync(0xffffffffu, swr[col >> 5], col & 31);
+          s = row_s * __shfl_sync(0xffffffffu, swc[(col - acc_c0) >> 5], col & 31);
         }
         v[i] = __uint_as_float(raw[i]) * s;
       }
@@ -284,7 +377,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
 #pragma unroll
         for (int i = 0; i < E::kAccColsPerChunk; ++i) {
           const int col = acc_c0 + i;
-          v[i] += __shfl_sync(0xffffffffu, biasr[col >> 5], col & 31);
+          v[i] += __shfl_sync(0xffffffffu, biasc[(col - acc_c0) >> 5], col & 31);
         }
       }
       float o[32];
@@ -307,14 +400,20 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
               o[g * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xFFFF0000u);
             }
           }
+          if constexpr (!kResTma) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) res_cur[g] = res_next[g];
+            for (int g = 0; g < 4; ++g) res_cur[g] = res_next[g];
+          }
         }
       }
       // Stage the 32 x 32 bf16 block (64-byte swizzle) and TMA-store it.
+      // The buffer's store of two chunks back must have been read (the TMA
+      // residual path waited for that before loading this chunk's block).
       uint8_t* sbuf = stage0 + (chunk_ctr & 1) * E::kBufBytes;
       ++chunk_ctr;
-      if (lane == 0) bulk_wait_read<1>();
+      if (!kResTma || split_item || res_bulk) {
+        if (lane == 0) bulk_wait_read<1>();
+      }
       __syncwarp();
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
@@ -334,7 +433,20 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         if (out_y < p.M && out_x < p.n_out) tma_store_3d(tmY, sbuf, out_x, out_y, tc.b);
         bulk_commit();
       }
+      if (c_next >= 0 && c_next < nch) {
+#pragma unroll
+        for (int j = 0; j < kCw; ++j) {
+          swc[j] = swn[j];
+          biasc[j] = biasn[j];
+        }
+      }
     }
+  }
+  if constexpr (kResTma) {
+    // No residual copy may still be writing the staging buffers at exit.
+    if (res_inflight >= 0 && lane == 0)
+      mbar_wait_drain(&res_bars[e * 2 + res_inflight], (res_ph >> res_inflight) & 1u, p.drain_ns,
+                      p.err);
   }
   if (lane == 0) bulk_wait<0>();
   __syncwarp();

@@ -74,6 +74,7 @@ spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, c
     } else {
       maps.b_narrow = maps.b;
     }
+    maps.r = maps.y;  // unused by the swapped tile
     GemmParams p;
     fill_common_params(p, r, N, T, K, K, N, 1);
     if (!p.err) return SPG_ERR_CUDA;
@@ -94,6 +95,10 @@ spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, c
   if (!make_tmap_3d(&maps.a, A, false, K, T, 1, K, K * T, 128, 128, 128) ||
       !make_tmap_3d(&maps.b, W, false, K, N, 1, K, K * N, 128, b_rows, 128) ||
       !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
+    return SPG_ERR_CUDA;
+  maps.r = maps.y;
+  if (r.block_m == 256 && epilogue == SPG_EPI_ADD &&
+      !make_tmap_3d(&maps.r, residual, true, N, T, 1, N * 2, N * 2 * T, 32, 32, 64))
     return SPG_ERR_CUDA;
   GemmParams p;
   fill_common_params(p, r, T, N, K, K, n_out, 1);

@@ -62,8 +62,14 @@ struct Gemm2smCfg {
   static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  // barriers, tmem slot + abort flag, residual barriers, stall barrier, PairExit
-  static_assert((2 * STAGES + 7 + kEpiWarps) * 8 + sizeof(PairExit) <= kBarBytes,
+  // linear_add residual by TMA into the epilogue staging buffers (the last
+  // item's whole into the idle operand ring)
+  static constexpr bool kResTma = !SWAP && EPI == SPG_EPI_ADD;
+  static_assert(!kResTma || kEpiWarps * (BN / 32) * 32 * 64 <= STAGES * kStageBytes,
+                "the last item's residual blocks must fit the operand ring");
+  // barriers, tmem slot + abort flag, residual barriers (two per epilogue
+  // warp), stall barrier, PairExit
+  static_assert((2 * STAGES + 7 + 2 * kEpiWarps) * 8 + sizeof(PairExit) <= kBarBytes,
                 "barrier area too small");
 
   // kind::f8f6f4, E4M3 x E4M3 -> f32, M = 256 (pair), N = BN.
@@ -77,7 +83,8 @@ template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWA
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmY,
-                    const __grid_constant__ CUtensorMap tmBnarrow, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmBnarrow,
+                    const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
   using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -93,8 +100,10 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  uint64_t* res_bars = drain + 2;  // swapped linear_add: one per epilogue warp
-  uint64_t* stall = res_bars + Cfg::kEpiWarps;  // test hook: nothing arrives on it
+  // linear_add residual copies: one per epilogue warp (swapped tile) or two
+  // (one per staging buffer)
+  uint64_t* res_bars = drain + 2;
+  uint64_t* stall = res_bars + 2 * Cfg::kEpiWarps;  // test hook: nothing arrives on it
   PairExit* pexit = reinterpret_cast<PairExit*>(stall + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -113,8 +122,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&acc_empty[b], 2 * Cfg::kEpiWarps);
     }
     mbar_init(drain, 1);
-    if constexpr (Cfg::kResBytes != 0)
-      for (int w = 0; w < Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
+    if constexpr (Cfg::kResBytes != 0 || Cfg::kResTma)
+      for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     mbar_init(stall, 1);
     mbar_init(&pexit->bar, 1);
     *abort_flag = 0;
@@ -125,6 +134,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmY);
     if (p.split_ways > 1 || Cfg::kResBytes != 0) prefetch_tmap(&tmBnarrow);
+    if constexpr (Cfg::kResTma) prefetch_tmap(&tmR);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
@@ -256,8 +266,9 @@ __global__ void __launch_bounds__(192, 1)
                                   p.total_items, num_pairs, item_fn, ctl, int(rank), &tmBnarrow,
                                   res_bars, res_smem);
     else
-      epilogue_loop<EPI, SCALE, BN>(p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair,
-                                    p.total_items, num_pairs, item_fn, ctl, int(rank));
+      epilogue_loop<EPI, SCALE, BN, decltype(item_fn), decltype(arrive_fn), Cfg::kResTma>(
+          p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, p.total_items, num_pairs, item_fn,
+          ctl, int(rank), &tmR, res_bars, ring);
   }
 
   tc_fence_before();

@@ -17,7 +17,7 @@ struct GemmMaps {
   CUtensorMap a, b, y;
   CUtensorMap sfa, sfb;  // NVFP4 two-SM kernel only
   CUtensorMap b_narrow;  // two-SM FP8 kernel: B box of a tail-split item
-  CUtensorMap r;         // NVFP4 warp-scale kernel, linear_add: residual, 32 x 32 boxes
+  CUtensorMap r;         // linear_add residual, 32 x 32 boxes (two-SM kernels; else a copy of y)
 };
 
 template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
@@ -69,7 +69,7 @@ spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cuda_status(cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, maps.b_narrow, p),
+  if (cuda_status(cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, maps.b_narrow, maps.r, p),
                   "cudaLaunchKernelEx") != SPG_OK)
     return SPG_ERR_CUDA;
   return launch_status();

@@ -80,6 +80,7 @@ spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_
     ok = make_tmap_3d(&maps.y, C, true, N, M, batch, N * 2, (batch > 1 ? strideC : M * N) * 2, 32,
                       32, 64);
   if (!ok) return SPG_ERR_CUDA;
+  maps.r = maps.y;  // no residual in the per-tensor GEMM
   GemmParams p;
   fill_common_params(p, r, M, N, K, K, N, batch);
   if (!p.err) return SPG_ERR_CUDA;
