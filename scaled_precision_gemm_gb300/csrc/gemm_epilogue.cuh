@@ -357,8 +357,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         if (!split_item && c + 1 < nch) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
       }
       if (have_k) tmem_wait_ld();
-      if (c == last_c) {
-        // Every column of this accumulator buffer has been read: hand it back.
+      if (c == last_c && item + item_step < item_end) {
+        // Every column of this accumulator buffer has been read: hand it back
+        // (after the CTA's last item no MMA waits for it, and the cluster-
+        // scope arrival would only delay the last stores).
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_empty(buf);
@@ -585,8 +587,10 @@ __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CU
               rb + j * 64 + (((lane >> 3) ^ ((j >> 1) & 3)) * 16));
       }
       if (have_k) tmem_wait_ld();
-      if (c == last_c) {
-        // Every column of this accumulator buffer has been read: hand it back.
+      if (c == last_c && item + item_step < item_end) {
+        // Every column of this accumulator buffer has been read: hand it back
+        // (after the CTA's last item no MMA waits for it, and the cluster-
+        // scope arrival would only delay the last stores).
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_empty(buf);
@@ -785,9 +789,13 @@ __device__ __forceinline__ void epilogue_loop_regdrain(const GemmParams& p, cons
 #pragma unroll
       for (int i = 0; i < kCols; ++i) acc[i] = 0u;
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) arrive_empty(0);
+    if (item + item_step < p.total_items) {
+      // Released at once (the next item's main loop overlaps the math and
+      // stores below); after the CTA's last item no MMA waits for it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_empty(0);
+    }
 
 #pragma unroll
     for (int c = 0; c < kOutChunks; ++c) {
