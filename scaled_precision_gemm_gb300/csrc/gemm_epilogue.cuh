@@ -471,7 +471,7 @@ namespace spg {
 // is ready and completing on res_bars[warp].  p.M = weight rows (N of the
 // layer), p.N = tokens (T).  K-split pieces go through split_piece_finish
 // like the unswapped tile.
-template <int EPI, int BN, typename ItemFn, typename ArriveEmpty>
+template <int EPI, int BN, typename ItemFn, typename ArriveEmpty, int SCALE = kScaleRow>
 __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CUtensorMap* tmY,
                                                    uint32_t tmem_base, uint64_t* acc_full,
                                                    ArriveEmpty arrive_empty, uint8_t* epi_smem,
@@ -495,6 +495,10 @@ __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CU
   int chunk_ctr = 0;
   const int n_w = p.M;  // weight rows = output columns
   const int n_t = p.N;  // tokens = output rows
+  // Per-tensor scales (kScaleScalar): the product sA * sB stands in for the
+  // weight row's scale and every token scale is 1.
+  float scalar = 1.f;
+  if constexpr (SCALE == kScaleScalar) scalar = __ldg(p.scalar_a) * __ldg(p.scalar_b);
 
   for (int item = item_begin; item < item_end; item += item_step, ++it) {
     const int buf = it & 1;
@@ -510,7 +514,8 @@ __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CU
     // Epilogue operands, requested before the accumulator is ready: the
     // weight scale and bias of this thread's row, the token scales (token
     // t0 + 32 c + lane in sar[c]) and the residual of the first chunk.
-    const float sw = n_ok ? __ldg(p.row_scale + n) : 0.f;
+    float sw = 0.f;
+    if (n_ok) sw = SCALE == kScaleRow ? __ldg(p.row_scale + n) : scalar;
     float bias = 0.f;
     if (p.bias_kind != 0 && n_ok) {
       if (p.bias_kind == 1) {
@@ -525,7 +530,7 @@ __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CU
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
       const int t = t0 + c * 32 + lane;
-      sar[c] = t < n_t ? __ldg(p.col_scale + t) : 0.f;
+      sar[c] = t < n_t ? (SCALE == kScaleRow ? __ldg(p.col_scale + t) : 1.f) : 0.f;
     }
     if constexpr (EPI == SPG_EPI_ADD) {
       if (live) {

@@ -56,8 +56,10 @@ struct Gemm2smCfg {
   static_assert(SWAP ? (BN == 32 || BN == 64 || BN == 128)
                      : (BN == 128 || BN == 160 || BN == 192 || BN == 256),
                 "pair tiles are 256 x {128, 160, 192, 256} (256 x {32, 64, 128} swapped)");
-  static_assert(!SWAP || (EPI != SPG_EPI_SWIGLU && !A_MN && !B_MN && SCALE == kScaleRow),
-                "the swapped tile serves row-scaled linear / linear_add with K-major operands");
+  static_assert(!SWAP || (EPI != SPG_EPI_SWIGLU && !A_MN && !B_MN &&
+                          (SCALE == kScaleRow || EPI == SPG_EPI_LINEAR)),
+                "the swapped tile serves row-scaled linear / linear_add and per-tensor linear, "
+                "with K-major operands");
   static_assert(EPI != SPG_EPI_SWIGLU || BN % 64 == 0, "SwiGLU tiles hold whole 64-column chunks");
   static_assert(!B_MN || BN == 256, "an N-major B half must be one 128-byte swizzle row");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned");
@@ -262,9 +264,9 @@ __global__ void __launch_bounds__(192, 1)
       return w;
     };
     if constexpr (SWAP)
-      epilogue_loop_swap<EPI, BN>(p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair,
-                                  p.total_items, num_pairs, item_fn, ctl, int(rank), &tmBnarrow,
-                                  res_bars, res_smem);
+      epilogue_loop_swap<EPI, BN, decltype(item_fn), decltype(arrive_fn), SCALE>(
+          p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, p.total_items, num_pairs, item_fn,
+          ctl, int(rank), &tmBnarrow, res_bars, res_smem);
     else
       epilogue_loop<EPI, SCALE, BN, decltype(item_fn), decltype(arrive_fn), Cfg::kResTma>(
           p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, p.total_items, num_pairs, item_fn,

@@ -267,10 +267,12 @@ inline void plan_items(GemmParams& p, const spg_route& r, int units, void* works
 // Route of a GEMM entry point: with a workspace the last partial wave may be
 // split along K, if the workspace is large enough for the plan.
 inline spg_route route_for(int kind, int64_t T, int64_t N, int64_t K, int epilogue, int64_t batch,
-                           bool b_mn, const void* workspace, int64_t workspace_bytes) {
-  spg_route r = select_route_internal(kind, T, N, K, epilogue, batch, b_mn, workspace != nullptr);
+                           bool b_mn, const void* workspace, int64_t workspace_bytes,
+                           bool allow_swap = true) {
+  spg_route r = select_route_internal(kind, T, N, K, epilogue, batch, b_mn, workspace != nullptr,
+                                      allow_swap);
   if (r.workspace_bytes > workspace_bytes)
-    r = select_route_internal(kind, T, N, K, epilogue, batch, b_mn, false);
+    r = select_route_internal(kind, T, N, K, epilogue, batch, b_mn, false, allow_swap);
   return r;
 }
 

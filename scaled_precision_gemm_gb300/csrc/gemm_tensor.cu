@@ -57,8 +57,37 @@ spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_
       !aligned16(workspace))
     return SPG_ERR_MISALIGNED;
 
+  // The swapped narrow-M tile reads both operands K-major ("NT" only).
   const spg_route r = route_for(SPG_KIND_FP8_TENSOR, M, N, K, SPG_EPI_LINEAR, batch, b_mn,
-                                workspace, workspace_bytes);
+                                workspace, workspace_bytes, !a_mn);
+  if (r.swap_ab) {
+    // Swapped tile (M <= 128, one matrix): the MMA's 256-row side takes B's
+    // rows (the output columns), its N side M rows of A; the epilogue writes
+    // C [M, N] transposed from the accumulator, scaled by sA * sB.
+    GemmMaps maps;
+    const uint32_t t_rows = static_cast<uint32_t>(r.block_n / 2);
+    if (!make_tmap_3d(&maps.a, B, false, K, N, 1, K, K * N, 128, 128, 128) ||
+        !make_tmap_3d(&maps.b, A, false, K, M, 1, K, K * M, 128, t_rows, 128) ||
+        !make_tmap_3d(&maps.y, C, true, N, M, 1, N * 2, N * 2 * M, 32, 32, 64))
+      return SPG_ERR_CUDA;
+    maps.b_narrow = maps.b;  // the swapped tile never splits along N
+    maps.r = maps.y;         // no residual
+    GemmParams p;
+    fill_common_params(p, r, N, M, K, K, N, 1);
+    if (!p.err) return SPG_ERR_CUDA;
+    if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
+    const int pairs = num_sms() / 2;
+    plan_items(p, r, pairs, workspace);
+    spg_route rr = r;
+    rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+    p.scalar_a = sA;
+    p.scalar_b = sB;
+    if (r.block_n == 64)
+      return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 64, 10, false, false, kScaleScalar, true>(
+          maps, p, rr.grid, stream);
+    return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 128, 8, false, false, kScaleScalar, true>(
+        maps, p, rr.grid, stream);
+  }
   const int b_rows = r.block_m == 256 ? r.block_n / 2 : r.block_n;  // B rows staged per CTA
   const bool a_batched = batch > 1 && strideA != 0;
   const bool b_batched = batch > 1 && strideB != 0;

@@ -286,7 +286,8 @@ struct Candidate {
 }  // namespace
 
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
-                                int64_t batch, bool b_mn_major, bool allow_ksplit) {
+                                int64_t batch, bool b_mn_major, bool allow_ksplit,
+                                bool allow_swap) {
   spg_route r;
   std::memset(&r, 0, sizeof r);
   r.kind = kind;
@@ -315,14 +316,16 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const double fixed = 6.0;  // per-tile fixed cost in 128-byte-deep K blocks
   KSplit best_ks;
   int best_ways = 1;
-  // Swapped pair tile for narrow T (FP8 row-scaled, one problem, linear /
-  // linear_add): the weight rows fill the MMA's 256-row M side and the
-  // tokens its N side (64 or 128 wide), so every staged byte but the small
-  // token tile is weight stream, where the unswapped tile stages a 256-row
-  // activation tile that is mostly out-of-range padding.  SPG_FORCE_VARIANT
-  // = swap pins it; any other forced variant disables it.
-  const bool swap_ok = kind == SPG_KIND_FP8_ROWSCALED && nb == 1 && epilogue != SPG_EPI_SWIGLU &&
-                       !b_mn_major && T >= 1 && T <= 128;
+  // Swapped pair tile for narrow T (FP8 row-scaled linear / linear_add, and
+  // the per-tensor GEMM with both operands K-major; one problem): the weight
+  // rows fill the MMA's 256-row M side and the tokens its N side (64 or 128
+  // wide), so every staged byte but the small token tile is weight stream,
+  // where the unswapped tile stages a 256-row activation tile that is mostly
+  // out-of-range padding.  SPG_FORCE_VARIANT = swap pins it; any other
+  // forced variant disables it.
+  const bool swap_ok = (kind == SPG_KIND_FP8_ROWSCALED || kind == SPG_KIND_FP8_TENSOR) &&
+                       allow_swap && nb == 1 && epilogue != SPG_EPI_SWIGLU && !b_mn_major &&
+                       T >= 1 && T <= 128;
   const bool swap = swap_ok && (forced_name ? std::strcmp(forced_name, "swap") == 0
                                             : swap_default(T, N, pairs));
   if (swap) {
@@ -612,7 +615,11 @@ extern "C" int64_t spg_gemm_workspace_bytes(int kind, int64_t T, int64_t N, int6
     return 0;
   const int64_t b = select_route_internal(kind, T, N, K, epilogue, batch, false, true).workspace_bytes;
   if (kind != SPG_KIND_FP8_TENSOR) return b;
-  // Per-tensor GEMM: enough for either B layout (an N-major B takes other tiles).
+  // Per-tensor GEMM: enough for either B layout and for an M-major A (which
+  // never takes the swapped tile).
   const int64_t n = select_route_internal(kind, T, N, K, epilogue, batch, true, true).workspace_bytes;
-  return b > n ? b : n;
+  const int64_t u =
+      select_route_internal(kind, T, N, K, epilogue, batch, false, true, false).workspace_bytes;
+  const int64_t m = b > n ? b : n;
+  return m > u ? m : u;
 }

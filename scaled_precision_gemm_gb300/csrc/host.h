@@ -101,8 +101,10 @@ inline double ksplit_piece_time(const KSplit& k, int bn) {
 // The selector behind spg_select_route (no validation).
 // b_mn_major: the B operand is N-major (per-tensor GEMM with layout_b 'N').
 // allow_ksplit: the caller provides a workspace, so the last partial wave may
-// be split along K.
+// be split along K.  allow_swap: the swapped narrow-T tile may be taken (the
+// per-tensor GEMM clears it for an M-major A, which that tile cannot read).
 spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
-                                int64_t batch, bool b_mn_major, bool allow_ksplit);
+                                int64_t batch, bool b_mn_major, bool allow_ksplit,
+                                bool allow_swap = true);
 
 }  // namespace spg

@@ -8,8 +8,8 @@ kernels rely on when the route is launched.
 * a K split has 2-4 pieces, none empty, each at least 4 K blocks, and the
   workspace query returns exactly the plan's bytes (the per-tensor GEMM:
   at least, it covers both B layouts); plain routes never split K;
-* the swapped tile is FP8 row-scaled, linear / linear_add, T <= 128, one
-  problem; the GEMV is NVFP4 with T <= 4.
+* the swapped tile is FP8 (row-scaled linear / linear_add, or per-tensor),
+  T <= 128, one problem; the GEMV is NVFP4 with T <= 4.
 """
 import itertools
 
@@ -58,7 +58,7 @@ def test_route_invariants(kind, epi):
             else:
                 assert r["grid"] <= 2 * PAIRS, tag
             if r["swap_ab"]:
-                assert kind == "fp8_rowscaled" and epi != "swiglu" and T <= 128, tag
+                assert kind in ("fp8_rowscaled", "fp8_tensor") and epi != "swiglu" and T <= 128, tag
                 assert r["block_n"] == (64 if T <= 64 else 128), tag
             if not ws:
                 assert r["split_k"] == 1 and r["workspace_bytes"] == 0, tag

@@ -1,4 +1,5 @@
-"""Swapped narrow-T tile of the FP8 row-scaled GEMM against the CPU oracle.
+"""Swapped narrow-T tile of the FP8 row-scaled GEMM (and of the per-tensor
+GEMM at narrow M, layout NT) against the CPU oracle.
 
 For T <= 128 the weights can take the MMA's 256-row side and the tokens its
 N side (the accumulator is Y transposed; the epilogue writes it back as
@@ -141,3 +142,70 @@ def test_swap_full_size_sampled(T, swap):
     rows = np.unique(np.array([0, 1, 15, 31, 32, 63, 64, 100, 127]) % T).astype(np.int64)
     ref = oracle.fp8_rowscaled_gemm(A, sa, W, sw, res, "add", rows=rows)
     assert_within_tol(to_f64(y[torch.from_numpy(rows).to(DEV)]), ref, f"fp8 swap T={T} add")
+
+
+# ------------------------------------------------------------ per-tensor
+def tensor_run(layout, A, sA, B, sB, M, N, K, ws=None, bias=None, bias_scale=None):
+    y = spg.fp8_tensor_gemm(layout, cuda(A), torch.tensor([sA], dtype=torch.float32, device=DEV),
+                            cuda(B), torch.tensor([sB], dtype=torch.float32, device=DEV), M, N, K,
+                            workspace=ws, bias=bias, bias_scale=bias_scale)
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    return to_f64(y).reshape(M, N)
+
+
+def tensor_operands(layout, M, N, K, seed):
+    a = normal_bf16((K, M) if layout[0] == "T" else (M, K), seed=seed)
+    b = normal_bf16((K, N) if layout[1] == "N" else (N, K), seed=seed + 1)
+    A, sA = oracle.quantize_fp8_tensor(a)
+    B, sB = oracle.quantize_fp8_tensor(b)
+    return A.reshape(-1), sA, B.reshape(-1), sB
+
+
+@pytest.mark.parametrize("M", [1, 16, 33, 64, 100, 128])
+@pytest.mark.parametrize("N,K", [(136, 256), (1040, 2064), (8192, 2048)])
+@pytest.mark.parametrize("with_ws", [False, True])
+def test_tensor_swap_nt(M, N, K, with_ws, swap):
+    """Per-tensor NT at narrow M takes the swapped tile (B's rows on the MMA's
+    256-row side, scaled by sA * sB)."""
+    A, sA, B, sB = tensor_operands("NT", M, N, K, seed=M * 3 + N + K)
+    r = spg.select_route("fp8_tensor", M, N, K, "linear", workspace=with_ws)
+    assert r["swap_ab"] == 1 and r["block_n"] == (64 if M <= 64 else 128)
+    if with_ws:
+        buf, ws, r = workspace_for("fp8_tensor", M, N, K, exact=False)
+        y = tensor_run("NT", A, sA, B, sB, M, N, K, ws)
+        check_workspace(buf, ws.numel(), r)
+    else:
+        y = tensor_run("NT", A, sA, B, sB, M, N, K)
+    ref = oracle.fp8_tensor_gemm("NT", A, sA, B, sB, M, N, K).reshape(M, N)
+    assert_within_tol(y, ref, f"tensor swap NT {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+def test_tensor_swap_bias(kind, swap):
+    M, N, K = 48, 784, 1024
+    A, sA, B, sB = tensor_operands("NT", M, N, K, seed=91)
+    if kind == "bf16":
+        b = normal_bf16((N,), seed=92, std=2.0)
+        bs, bt, bst = None, cuda_bf16(b), None
+    else:
+        b = random_codes((N,), seed=92, exclude=(0x7F, 0xFF))
+        bs = np.float32(0.125)
+        bt, bst = cuda(b), torch.tensor([bs], dtype=torch.float32, device=DEV)
+    y = tensor_run("NT", A, sA, B, sB, M, N, K, bias=bt, bias_scale=bst)
+    ref = oracle.fp8_tensor_gemm("NT", A, sA, B, sB, M, N, K, bias=b, bias_scale=bs).reshape(M, N)
+    assert_within_tol(y, ref, f"tensor swap bias {kind}")
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN", "TT"])
+def test_tensor_narrow_other_layouts(layout):
+    """Narrow M with an M-major A or an N-major B: the unswapped tiles."""
+    M, N, K = 64, 528, 1024
+    A, sA, B, sB = tensor_operands(layout, M, N, K, seed=95)
+    y = tensor_run(layout, A, sA, B, sB, M, N, K)
+    if layout == "TT":
+        Bt = B.reshape(N, K).T.reshape(-1)
+        ref = oracle.fp8_tensor_gemm("TN", A, sA, Bt, sB, M, N, K)
+    else:
+        ref = oracle.fp8_tensor_gemm(layout, A, sA, B, sB, M, N, K)
+    assert_within_tol(y, ref.reshape(M, N), f"tensor narrow {layout}")
