@@ -21,6 +21,40 @@ namespace spg {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// x / s correctly rounded for many x and one s, from a reciprocal taken
+// once: Markstein's correction step.  With y = RN(1/s) and the faithful
+// q0 = RN(x * y), the remainder x - q0 * s is exact (one FMA) and
+// RN(q0 + (x - q0 * s) * y) = RN(x / s) -- a quotient of two floats is never
+// a tie.  The remainder is formed as q0 * s - x and subtracted, which keeps
+// x = -0 giving -0 as the division does.  1/s loses precision for huge
+// divisors and the remainder may underflow for tiny ones, so divisors
+// outside [2^-90, 2^100] take the IEEE division (`fast` false).  With
+// s >= 2^-90 a remainder can underflow only for |x| < 2^-100, where the
+// quotient is below 2^-10 and every code it can round to is zero.  Checked
+// against double-precision division on 2e8 random (bf16, float) pairs:
+// equal wherever a code could differ.
+struct ExactDivisor {
+  float s, y;
+  bool fast;
+  __device__ __forceinline__ explicit ExactDivisor(float s_) : s(s_) {
+    fast = s_ >= 0x1p-90f && s_ <= 0x1p100f;  // false for NaN too
+    y = fast ? __frcp_rn(s_) : 0.f;
+  }
+  // Requires `fast` and a finite quotient below 2^126.
+  __device__ __forceinline__ float div_fast(float x) const {
+    const float q0 = __fmul_rn(x, y);
+    return __fmaf_rn(-__fmaf_rn(q0, s, -x), y, q0);
+  }
+  // Any x: quotients of 2^126 and beyond (and NaN) come back as x * y, every
+  // code saturating there as it does for the division's result.
+  __device__ __forceinline__ float div(float x) const {
+    if (!fast) return __fdiv_rn(x, s);
+    const float q0 = __fmul_rn(x, y);
+    if (!(fabsf(q0) < 0x1p126f)) return q0;
+    return __fmaf_rn(-__fmaf_rn(q0, s, -x), y, q0);
+  }
+};
+
 // max |x| over eight bf16 values.
 __device__ __forceinline__ float bf16x8_amax(const uint4& v) {
   float a = 0.f;
@@ -48,11 +82,22 @@ __device__ __forceinline__ uint32_t nvfp4_encode_block(const uint4& v0, const ui
   const float sv = fmaxf(dd.x, dd.y);
   const float d = __fmul_rn(sv, g);
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  // |x| <= amax_b and d >= dec(sf) * g with sf the rounded (amax_b / 6) / g,
+  // so the quotients stay below 2^126.
+  const ExactDivisor dv(d);
   float q[16];
+  if (dv.fast) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
-    q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
+    for (int i = 0; i < 8; ++i) {
+      q[2 * i] = dv.div_fast(bf16_lo(w[i]));
+      q[2 * i + 1] = dv.div_fast(bf16_hi(w[i]));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
+      q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
+    }
   }
   code_lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
   code_hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));

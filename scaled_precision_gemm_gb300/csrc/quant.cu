@@ -2,15 +2,15 @@
 // scales, and bf16 -> NVFP4 (E2M1 codes, E4M3 block-16 scales in the blocked
 // tile layout, fp32 global scale).
 //
-// All of them are HBM-bound streaming kernels: 16-byte vector loads of the
-// bf16 input, every fp32 step as one IEEE-rounded operation (__fdiv_rn,
-// __fmul_rn) so that codes and scales are bit-for-bit those of the plain
-// definition, and hardware cvt.rn.satfinite conversions for the codes.  The
-// per-element IEEE division makes them partly ALU-bound (measured on GB300:
-// the FP8 row quantizer takes 88 us at T = 8192, K = 17408, and 63.5 us --
-// the HBM copy rate -- with the division replaced by a multiply, which is
-// not bit-exact; a reciprocal multiply with an exact fallback near the
-// rounding points measured slower than the division itself).
+// All of them are streaming kernels: 16-byte vector loads of the bf16
+// input, every fp32 step one correctly rounded operation so that codes and
+// scales are bit-for-bit those of the plain definition, and hardware
+// cvt.rn.satfinite conversions for the codes.  The per-element quotient
+// x / s is the correctly rounded one, formed from a reciprocal taken once
+// per scale with Markstein's correction step (ExactDivisor): an IEEE
+// division per element made them instruction-bound (measured on GB300: the
+// FP8 row quantizer took 88 us at T = 8192, K = 17408, against 63.5 us --
+// the HBM copy rate -- with an inexact plain multiply).
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -24,13 +24,23 @@ namespace {
 
 __device__ __forceinline__ float vec_amax(const uint4& v) { return bf16x8_amax(v); }
 
-// Eight bf16 divided by s (IEEE) -> eight E4M3 codes.
-__device__ __forceinline__ uint2 vec_encode_e4m3(const uint4& v, float s) {
+// Eight bf16 divided by s (correctly rounded) -> eight E4M3 codes.  MODE 0:
+// any s and x (the delayed scale may be stale); 1: s.fast and |x| <= 448 s
+// (a scale taken from this data's amax); 2: the IEEE division.
+template <int MODE>
+__device__ __forceinline__ uint2 vec_encode_e4m3(const uint4& v, const ExactDivisor& s) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t c[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    c[i] = cvt_e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+  for (int i = 0; i < 4; ++i) {
+    const float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+    if constexpr (MODE == 1)
+      c[i] = cvt_e4m3x2(s.div_fast(lo), s.div_fast(hi));
+    else if constexpr (MODE == 2)
+      c[i] = cvt_e4m3x2(__fdiv_rn(lo, s.s), __fdiv_rn(hi, s.s));
+    else
+      c[i] = cvt_e4m3x2(s.div(lo), s.div(hi));
+  }
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
@@ -83,13 +93,25 @@ __global__ void __launch_bounds__(THREADS) quantize_fp8_rows_kernel(
     amax = fmaxf(amax, vec_amax(__ldg(xr + i)));
   amax = block_max<THREADS>(amax, red);
   const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+  const ExactDivisor sd(s);
+  // The branch is uniform over the CTA (one row, one scale).
+  if (sd.fast) {
 #pragma unroll
-  for (int j = 0; j < VECS; ++j) {
-    const int64_t i = threadIdx.x + static_cast<int64_t>(j) * THREADS;
-    if (i < nvec) cr[i] = vec_encode_e4m3(cache[j], s);
+    for (int j = 0; j < VECS; ++j) {
+      const int64_t i = threadIdx.x + static_cast<int64_t>(j) * THREADS;
+      if (i < nvec) cr[i] = vec_encode_e4m3<1>(cache[j], sd);
+    }
+    for (int64_t i = threadIdx.x + int64_t(VECS) * THREADS; i < nvec; i += THREADS)
+      cr[i] = vec_encode_e4m3<1>(__ldg(xr + i), sd);
+  } else {
+#pragma unroll
+    for (int j = 0; j < VECS; ++j) {
+      const int64_t i = threadIdx.x + static_cast<int64_t>(j) * THREADS;
+      if (i < nvec) cr[i] = vec_encode_e4m3<2>(cache[j], sd);
+    }
+    for (int64_t i = threadIdx.x + int64_t(VECS) * THREADS; i < nvec; i += THREADS)
+      cr[i] = vec_encode_e4m3<2>(__ldg(xr + i), sd);
   }
-  for (int64_t i = threadIdx.x + int64_t(VECS) * THREADS; i < nvec; i += THREADS)
-    cr[i] = vec_encode_e4m3(__ldg(xr + i), s);
   if (threadIdx.x == 0) scales[row] = s;
 }
 
@@ -116,9 +138,16 @@ __global__ void __launch_bounds__(256) encode_fp8_tensor_kernel(const uint4* __r
                                                                 float* __restrict__ scale) {
   const float a = *amax;
   const float s = (a == 0.f) ? 1.f : __fdiv_rn(a, 448.f);
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
-       i += int64_t(gridDim.x) * blockDim.x)
-    codes[i] = vec_encode_e4m3(__ldg(x + i), s);
+  const ExactDivisor sd(s);
+  if (sd.fast) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
+         i += int64_t(gridDim.x) * blockDim.x)
+      codes[i] = vec_encode_e4m3<1>(__ldg(x + i), sd);
+  } else {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
+         i += int64_t(gridDim.x) * blockDim.x)
+      codes[i] = vec_encode_e4m3<2>(__ldg(x + i), sd);
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
 }
 
@@ -212,12 +241,13 @@ __global__ void __launch_bounds__(256) quantize_fp8_delayed_kernel(const uint4* 
   __shared__ float red[8];
   __shared__ bool last;
   const float s = *reinterpret_cast<volatile float*>(ring + history);
+  const ExactDivisor sd(s);
   float a = 0.f;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nvec;
        i += int64_t(gridDim.x) * blockDim.x) {
     const uint4 v = __ldg(x + i);
     a = fmaxf(a, vec_amax(v));
-    codes[i] = vec_encode_e4m3(v, s);
+    codes[i] = vec_encode_e4m3<0>(v, sd);
   }
   a = block_max<256>(a, red);
   unsigned int* amax_bits = reinterpret_cast<unsigned int*>(ring + history + 1);
