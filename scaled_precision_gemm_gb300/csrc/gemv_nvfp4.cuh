@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
     for (int r = 0; r < ncta; ++r) m = fmaxf(m, amax_s[r]);
     g_act = nvfp4_global_from_amax(m);
     const uint32_t aq_base = smem_u32(aq_s), sa_base = smem_u32(sa_s);
+    const Nvfp4BlockEncoder enc(g_act);
     for (int i = int(rank) + ncta * int(threadIdx.x); i < p.T * nchunks;
          i += ncta * blockDim.x) {
       const int t = i / nchunks;
@@ -185,8 +186,8 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
       const uint4* src = xv + (int64_t(t) * p.K + int64_t(c) * 32) / 8;
       uint4 codes;
       float2 sa;
-      nvfp4_encode_block(__ldg(src), __ldg(src + 1), g_act, codes.x, codes.y, &sa.x);
-      nvfp4_encode_block(__ldg(src + 2), __ldg(src + 3), g_act, codes.z, codes.w, &sa.y);
+      enc.block(__ldg(src), __ldg(src + 1), codes.x, codes.y, &sa.x);
+      enc.block(__ldg(src + 2), __ldg(src + 3), codes.z, codes.w, &sa.y);
       uint32_t q[8];
       decode_chunk(codes, q);
       const uint32_t o0 = aq_base + uint32_t((t * 2) * nchunks + c) * 16u;

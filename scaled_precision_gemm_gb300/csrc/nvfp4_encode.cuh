@@ -69,40 +69,46 @@ __device__ __forceinline__ float nvfp4_global_from_amax(float amax) {
   return (amax == 0.f) ? 1.f : __fdiv_rn(amax, 2688.f);
 }
 
-// One 16-element block (v0: elements 0-7, v1: 8-15) with global scale g:
-// its eight code bytes (element i in nibble i of the 64 bits, low word
-// first) and its E4M3 scale byte; *dec receives the scale's exact value.
-__device__ __forceinline__ uint32_t nvfp4_encode_block(const uint4& v0, const uint4& v1, float g,
-                                                       uint32_t& code_lo, uint32_t& code_hi,
-                                                       float* dec) {
-  const float amax_b = fmaxf(bf16x8_amax(v0), bf16x8_amax(v1));
-  const float t = __fdiv_rn(__fdiv_rn(amax_b, 6.f), g);
-  const uint32_t sfc = cvt_e4m3x2(t, t) & 0xFFu;
-  const float2 dd = e4m3x2_to_float2(static_cast<uint16_t>(sfc));  // one byte is zero
-  const float sv = fmaxf(dd.x, dd.y);
-  const float d = __fmul_rn(sv, g);
-  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  // |x| <= amax_b and d >= dec(sf) * g with sf the rounded (amax_b / 6) / g,
-  // so the quotients stay below 2^126.
-  const ExactDivisor dv(d);
-  float q[16];
-  if (dv.fast) {
+// The block encoder for one global scale g, its divisors prepared once.
+// One 16-element block (v0: elements 0-7, v1: 8-15): its eight code bytes
+// (element i in nibble i of the 64 bits, low word first) and its E4M3 scale
+// byte; *dec receives the scale's exact value.  (amax_b / 6) / g stays two
+// IEEE divisions per block (with the reciprocal form measured no faster).
+struct Nvfp4BlockEncoder {
+  float g;
+  __device__ __forceinline__ explicit Nvfp4BlockEncoder(float g_) : g(g_) {}
+
+  __device__ __forceinline__ uint32_t block(const uint4& v0, const uint4& v1, uint32_t& code_lo,
+                                            uint32_t& code_hi, float* dec) const {
+    const float amax_b = fmaxf(bf16x8_amax(v0), bf16x8_amax(v1));
+    const float t = __fdiv_rn(__fdiv_rn(amax_b, 6.f), g);
+    const uint32_t sfc = cvt_e4m3x2(t, t) & 0xFFu;
+    const float2 dd = e4m3x2_to_float2(static_cast<uint16_t>(sfc));  // one byte is zero
+    const float sv = fmaxf(dd.x, dd.y);
+    const float d = __fmul_rn(sv, g);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    // |x| <= amax_b and d >= dec(sf) * g with sf the rounded (amax_b / 6) / g,
+    // so the quotients stay below 2^126.
+    const ExactDivisor dv(d);
+    float q[16];
+    if (dv.fast) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      q[2 * i] = dv.div_fast(bf16_lo(w[i]));
-      q[2 * i + 1] = dv.div_fast(bf16_hi(w[i]));
-    }
-  } else {
+      for (int i = 0; i < 8; ++i) {
+        q[2 * i] = dv.div_fast(bf16_lo(w[i]));
+        q[2 * i + 1] = dv.div_fast(bf16_hi(w[i]));
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
-      q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
+      for (int i = 0; i < 8; ++i) {
+        q[2 * i] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_lo(w[i]), d);
+        q[2 * i + 1] = (d == 0.f) ? 0.f : __fdiv_rn(bf16_hi(w[i]), d);
+      }
     }
+    code_lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
+    code_hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));
+    *dec = sv;
+    return sfc;
   }
-  code_lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
-  code_hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));
-  *dec = sv;
-  return sfc;
-}
+};
 
 }  // namespace spg
