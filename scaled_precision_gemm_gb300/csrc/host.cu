@@ -292,7 +292,11 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   std::memset(&r, 0, sizeof r);
   r.kind = kind;
   r.acc_buffers = 2;
-  r.group_m = 16;
+  // Raster group (256-row blocks per group of the tile order), swept on
+  // GB300 at T = 8192 over 4..32: 16 within ~1% of the best for FP8 and the
+  // NVFP4 linear_add widths; the 34816-wide NVFP4 SwiGLU ran 680 us at 32
+  // against 688 at 16 (its wide rows re-read A less in taller groups).
+  r.group_m = (kind == SPG_KIND_NVFP4 && N >= 16384) ? 32 : 16;
   {
     const ForcedRoute f = forced_route();
     if (f.group_m > 0) r.group_m = f.group_m;
