@@ -384,14 +384,15 @@ def run_gpu(args):
             gA = torch.empty((1,), dtype=torch.float32, device=dev)
 
             def quant(x, res, A=A, sfA=sfA, gA=gA, k=k):
-                spg.nvfp4_global_scale(x, gA, scratch)
-                spg.quantize_nvfp4(x, gA, A, sfA)
+                spg.quantize_nvfp4_act(x, gA, A, sfA, scratch)
                 k.res_dev = res
             k.quant = quant
             k.gemm = lambda A=A, sfA=sfA, gA=gA, Wc=Wc, sfW=sfW, gW=gW, k=k, epi=c["epi"]: \
                 spg.nvfp4_gemm(A, sfA, gA, Wc, sfW, gW, residual=k.res_dev, epilogue=epi,
                                out=k.out, workspace=k.ws)
-            k.launches = 4     # amax + finalize + quantize + GEMM (plus one memset)
+            # one quantizer kernel for small activations, else amax + finalize +
+            # quantize (plus one memset); then the GEMM
+            k.launches = 2 if T * K <= 72 * 1024 else 4
         prepared.append(k)
 
     # Warm the library (first-call set-up: shared-memory limits, device error

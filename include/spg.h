@@ -88,8 +88,10 @@ typedef struct {
                         /* 0-3 pair tiles 256/192/160/128 wide, 4-5 one-CTA  */
                         /* 256/128, 6 swapped pair tile; NVFP4: 0 pair tile  */
                         /* with copied scales, 2 one-CTA, 3 pair tile with   */
-                        /* warp-stored scales, 4 CUDA-core GEMV for T <= 4:  */
-                        /* block_m 1, block_n 2 weight rows per warp)        */
+                        /* warp-stored scales, 4 CUDA-core GEMV for T <= 4   */
+                        /* (block_m 1, block_n 2 weight rows per warp), 5    */
+                        /* cluster of two one-CTA tiles sharing B by TMA     */
+                        /* multicast)                                        */
   int32_t split_n;      /* last partial wave: tiles split along N this many ways */
   int32_t split_k;      /* last partial wave: tiles split along K this many ways */
   int64_t workspace_bytes; /* workspace the K split needs (0 without one)     */
@@ -239,6 +241,17 @@ SPG_API spg_status spg_nvfp4_global_scale(const void* x, int64_t numel, float* g
 SPG_API spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K, const float* g,
                               uint8_t* codes, uint8_t* sf, spg_stream_t stream);
 
+/* The activations' NVFP4 quantization in one call: spg_nvfp4_global_scale
+ * (x -> g) followed by spg_quantize_nvfp4 (x, g -> codes, sf), bit for bit.
+ * Tensors of at most 73,728 elements (decode widths) take a single kernel
+ * (one CTA finds the maximum and encodes every block) instead of the four
+ * launches of the two calls (GB300: 10.8 against 21.0 us at 1 x 17408, 14.9
+ * against 16.9 at 4 x 17408; 18.9 against 14.9 at 7 x 17408).  Arguments, layouts and errors as for the two
+ * calls (amax_scratch: one fp32 of caller-owned scratch). */
+SPG_API spg_status spg_quantize_nvfp4_act(const void* x, int64_t rows, int64_t K, float* g,
+                                          float* amax_scratch, uint8_t* codes, uint8_t* sf,
+                                          spg_stream_t stream);
+
 /* Bytes of the blocked NVFP4 scale layout for a [rows, K] operand:
  * ceil(rows/128)*128 * ceil(K/64)*4.  Layout: the [rows, K/16] scale matrix
  * is cut into tiles of 128 rows x 4 scales (512 bytes), stored tile row by
@@ -380,7 +393,8 @@ SPG_API spg_status fp8_tensor_gemm_ws(char layout_a, char layout_b, int64_t batc
  *   fp8_rowscaled_linear_bf16 = spg_quantize_fp8_rows(X) -> (A, sa), then
  *     fp8_rowscaled_gemm_ws(A, sa, W, sw, ...);
  *   nvfp4_linear_bf16 = spg_nvfp4_global_scale(X) -> gA,
- *     spg_quantize_nvfp4(X, gA) -> (A, sfA), then nvfp4_gemm_ws(A, sfA, gA, ...).
+ *     spg_quantize_nvfp4(X, gA) -> (A, sfA) (as spg_quantize_nvfp4_act does
+ *     them), then nvfp4_gemm_ws(A, sfA, gA, ...).
  * The codes, scales and result are exactly those of that sequence.  At
  * NVFP4 decode widths (T <= 4, the GEMV route) the whole operator is one
  * kernel: each CTA of the GEMV quantizes X into its shared memory itself and

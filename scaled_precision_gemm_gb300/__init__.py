@@ -19,7 +19,7 @@ __all__ = [
     "SpgError", "EPILOGUES", "load_library", "library_path",
     "quantize_fp8_rows", "quantize_fp8_tensor", "quantize_fp8_tensor_noalloc",
     "fp8_scale_ring", "quantize_fp8_tensor_delayed",
-    "nvfp4_global_scale", "quantize_nvfp4",
+    "nvfp4_global_scale", "quantize_nvfp4", "quantize_nvfp4_act",
     "nvfp4_sf_bytes", "nvfp4_sf_offset", "fp8_rowscaled_gemm", "nvfp4_gemm", "fp8_tensor_gemm",
     "act_workspace_bytes", "act_workspace", "fp8_rowscaled_linear_bf16", "nvfp4_linear_bf16",
     "select_route", "last_device_error", "set_wait_timeout_ns", "status_string",
@@ -88,6 +88,7 @@ def load_library():
             "spg_fp8_scale_ring_init": (st, [vp, i32, ctypes.c_float, vp]),
             "spg_quantize_fp8_tensor_delayed": (st, [vp, i64, vp, vp, vp, i32, vp]),
             "spg_quantize_nvfp4": (st, [vp, i64, i64, vp, vp, vp, vp]),
+            "spg_quantize_nvfp4_act": (st, [vp, i64, i64, vp, vp, vp, vp, vp]),
             "spg_nvfp4_sf_bytes": (ctypes.c_size_t, [i64, i64]),
             "spg_nvfp4_sf_offset": (i64, [i64, i64, i64]),
             "fp8_rowscaled_gemm": (st, [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]),
@@ -325,6 +326,25 @@ def quantize_nvfp4(x: torch.Tensor, g: torch.Tensor, codes=None, sf=None):
 
 
 # ------------------------------------------------------------------ GEMMs
+def quantize_nvfp4_act(x: torch.Tensor, g=None, codes=None, sf=None, amax_scratch=None):
+    """bf16 [R, K] -> (packed E2M1 codes [R, K/2], blocked E4M3 scales, fp32 [1] g):
+    the global scale and the block quantizer in one call (one kernel for small x)."""
+    _need(x, "x", torch.bfloat16, 2)
+    R, K = x.shape
+    g = torch.empty((1,), dtype=torch.float32, device=x.device) if g is None else g
+    codes = (torch.empty((R, K // 2), dtype=torch.uint8, device=x.device)
+             if codes is None else codes)
+    sf = (torch.empty((nvfp4_sf_bytes(R, K),), dtype=torch.uint8, device=x.device)
+          if sf is None else sf)
+    scratch = (torch.empty((4,), dtype=torch.float32, device=x.device)
+               if amax_scratch is None else amax_scratch)
+    _need(g, "g", torch.float32)
+    _check(load_library().spg_quantize_nvfp4_act(_ptr(x), R, K, _ptr(g), _ptr(scratch),
+                                                 _ptr(codes), _ptr(sf), _stream(x)),
+           "spg_quantize_nvfp4_act")
+    return codes, sf, g
+
+
 def _epi(epilogue) -> int:
     return EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
 

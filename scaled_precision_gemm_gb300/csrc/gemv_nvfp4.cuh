@@ -111,19 +111,19 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b)
-               : "memory");
-}
-
 // Shared-memory bytes of the decoded activations of one CTA: per token two
 // planes of K/32 16-byte words (the int8 of each chunk's two blocks) and
-// K/32 float2 (the two blocks' scales).
+// K/32 pairs of E4M3 scale codes (decoded where they are used: kept as
+// codes, four tokens at K = 17408 fit three CTAs per SM instead of two).
 __host__ __device__ constexpr int64_t gemv_smem_bytes(int tt, int64_t K) {
-  return int64_t(tt) * (K / 32) * 40;
+  return int64_t(tt) * (K / 32) * 34;
 }
 
-// TT: tokens the instantiation holds (1, 2 or 4); p.T <= TT.  Grid: one
+__device__ __forceinline__ void st_cluster_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// TT: tokens the instantiation holds (1 to 4); p.T <= TT.  Grid: one
 // warp per pair of weight rows, 4 warps per CTA.  The CTA first decodes the
 // activations once into shared memory (they are read by every row).
 template <int EPI, int TT>
@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
   const int nchunks = p.K / 32;
   const int kt = p.K / 64;
   uint4* aq_s = gemv_smem;  // [TT][2][nchunks]
-  float2* sa_s = reinterpret_cast<float2*>(gemv_smem + 2 * TT * nchunks);  // [TT][nchunks]
+  // [TT][nchunks] pairs of E4M3 scale codes (low byte: the chunk's first block)
+  uint16_t* sa_s = reinterpret_cast<uint16_t*>(gemv_smem + 2 * TT * nchunks);
   __shared__ float red_s[4];
   __shared__ float amax_s[kGemvMaxCluster];
   float g_act = 0.f;
@@ -185,18 +186,19 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
       const int c = i - t * nchunks;
       const uint4* src = xv + (int64_t(t) * p.K + int64_t(c) * 32) / 8;
       uint4 codes;
-      float2 sa;
-      enc.block(__ldg(src), __ldg(src + 1), codes.x, codes.y, &sa.x);
-      enc.block(__ldg(src + 2), __ldg(src + 3), codes.z, codes.w, &sa.y);
+      float dec;
+      const uint32_t sf0 = enc.block(__ldg(src), __ldg(src + 1), codes.x, codes.y, &dec);
+      const uint32_t sf1 = enc.block(__ldg(src + 2), __ldg(src + 3), codes.z, codes.w, &dec);
+      const uint16_t sa = static_cast<uint16_t>(sf0 | (sf1 << 8));
       uint32_t q[8];
       decode_chunk(codes, q);
       const uint32_t o0 = aq_base + uint32_t((t * 2) * nchunks + c) * 16u;
       const uint32_t o1 = aq_base + uint32_t((t * 2 + 1) * nchunks + c) * 16u;
-      const uint32_t os = sa_base + uint32_t(t * nchunks + c) * 8u;
+      const uint32_t os = sa_base + uint32_t(t * nchunks + c) * 2u;
       for (int r = 0; r < ncta; ++r) {
         st_cluster_v4(mapa_shared(o0, r), q[0], q[1], q[2], q[3]);
         st_cluster_v4(mapa_shared(o1, r), q[4], q[5], q[6], q[7]);
-        st_cluster_v2(mapa_shared(os, r), __float_as_uint(sa.x), __float_as_uint(sa.y));
+        st_cluster_u16(mapa_shared(os, r), sa);
       }
     }
     cluster_sync();
@@ -208,8 +210,8 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
       decode_chunk(__ldg(reinterpret_cast<const uint4*>(p.A + int64_t(t) * kh) + c), q);
       aq_s[(t * 2) * nchunks + c] = make_uint4(q[0], q[1], q[2], q[3]);
       aq_s[(t * 2 + 1) * nchunks + c] = make_uint4(q[4], q[5], q[6], q[7]);
-      sa_s[t * nchunks + c] = e4m3x2_to_float2(__ldg(reinterpret_cast<const unsigned short*>(
-          p.sfA + gemv_sf_row_offset(t, kt) + (c >> 1) * 512 + (c & 1) * 2)));
+      sa_s[t * nchunks + c] = __ldg(reinterpret_cast<const unsigned short*>(
+          p.sfA + gemv_sf_row_offset(t, kt) + (c >> 1) * 512 + (c & 1) * 2));
     }
   }
   __syncthreads();
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(128, 5) gemv_nvfp4_kernel(const GemvParams p) 
           if (t >= p.T) break;
           const uint4 a0 = aq_s[(t * 2) * nchunks + c];
           const uint4 a1 = aq_s[(t * 2 + 1) * nchunks + c];
-          const float2 sa = sa_s[t * nchunks + c];
+          const float2 sa = e4m3x2_to_float2(sa_s[t * nchunks + c]);
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             int d0 = __dp4a(int(a0.x), int(wq[r][0]), 0);
@@ -401,6 +403,7 @@ template <int EPI>
 spg_status launch_gemv_tokens(const GemvParams& p, cudaStream_t s) {
   if (p.T == 1) return launch_gemv<EPI, 1>(p, s);
   if (p.T == 2) return launch_gemv<EPI, 2>(p, s);
+  if (p.T == 3) return launch_gemv<EPI, 3>(p, s);
   return launch_gemv<EPI, 4>(p, s);
 }
 

@@ -359,18 +359,19 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     return r;
   }
   // NVFP4 at decode-sized T (1-4 tokens): the CUDA-core GEMV (variant 4;
-  // two weight rows per warp, 4 warps per CTA; no workspace).  Measured on
-  // GB300 against the best tile route: linear_add N = 5120, K = 17408:
-  // 24.6 / 30.7 / 36.9 us at T = 1 / 2 / 4 against 41.0 / 36.9 / 38.9;
-  // K = 6144: 14.3 / 14.3 / 20.5 against 20.5; the 34816-wide SwiGLU ties
-  // (36.9-38.9 us).  SPG_FORCE_VARIANT=gemv pins it, any other forced
-  // variant disables it.  Its CTAs hold the decoded activations in shared
-  // memory (40 bytes per token slot and 32 K elements; 1, 2 or 4 slots), so
-  // K is bounded.
-  const int64_t gemv_tt = T == 1 ? 1 : (T == 2 ? 2 : 4);
+  // two weight rows per warp, 4 warps per CTA; no workspace) where it
+  // measured faster than the tile routes on GB300 (us, GEMV / best tile):
+  // linear_add N = 5120, K = 17408: T = 1 / 2 24.6 / 36.9, 28.7 / 36.9, but
+  // T = 3 / 4 41.0 / 36.9, 47.2 / 34.8; K = 6144: T = 3 / 4 16.4 / 22.5,
+  // 18.5 / 22.5; the 34816-wide SwiGLU 39-59 against 37-39.  Hence: N up to
+  // 16384, and T <= 2 or K <= 8192.  SPG_FORCE_VARIANT=gemv pins it, any
+  // other forced variant disables it.  Its CTAs hold the decoded activations
+  // in shared memory (34 bytes per token and 32 K elements), so K is bounded.
+  const bool gemv_pays = N <= 16384 && (T <= 2 || K <= 8192);
+  const int64_t gemv_tt = T;  // token slots of the instance (1 to 4)
   if (kind == SPG_KIND_NVFP4 && nb == 1 && T >= 1 && T <= 4 &&
-      gemv_tt * (K / 32) * 40 <= 200 * 1024 &&
-      (!forced_name || std::strcmp(forced_name, "gemv") == 0)) {
+      gemv_tt * (K / 32) * 34 <= 200 * 1024 &&
+      (forced_name ? std::strcmp(forced_name, "gemv") == 0 : gemv_pays)) {
     r.block_m = 1;
     r.block_n = 2;
     r.block_k = 32;
@@ -381,7 +382,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     r.grid = static_cast<int>((N / 2 + 3) / 4);
     r.split_n = 1;
     r.split_k = 1;
-    r.smem_bytes = static_cast<int32_t>(gemv_tt * (K / 32) * 40);
+    r.smem_bytes = static_cast<int32_t>(gemv_tt * (K / 32) * 34);
     return r;
   }
   if (kind == SPG_KIND_NVFP4) {

@@ -34,20 +34,19 @@ struct ActLayout {
   bool fused = false;    // NVFP4 decode: one GEMV kernel, no workspace
 };
 
-// The fused decode kernel where it measured faster than the quantizer
-// kernels followed by the GEMV (GB300, graph-replayed, L2 flushed; us):
-//   SwiGLU N = 34816, K = 5120, T = 1..4:  47.6 / 51.7 / 57.9 / 64.0
-//                                  against 49.7 / 55.8 / 62.0 / 70.1
-//   linear_add N = 5120, K = 6144, T = 1:  21.0 against 25.1
-// and not elsewhere (N = 5120, K = 17408, T = 1 / 2: 39.4 / 49.6 against
-// 35.3 / 41.4; the other N = 5120 shapes within one timer step or slower):
+// The fused decode kernel (the GEMV in its operator form) where it measured
+// faster than the quantizer kernels followed by the plain route (GB300,
+// graph-replayed, L2 flushed; us):
+//   SwiGLU N = 34816, K = 5120, T = 1 / 2:  47.6 / 51.7 against 52-56
+//   linear_add N = 5120, K = 6144, T = 1:   21.0 against 25.1
+// and not elsewhere (SwiGLU T = 3 / 4 57.9 / 64.0 against ~53 on the tile
+// route; N = 5120, K = 17408, T = 1 / 2: 39.4 / 49.6 against 35.3 / 41.4):
 // the kernel pays off where the weight stream is long against the
-// per-cluster quantization (wide N, several row pairs per warp) or X is
-// one short row.
+// per-cluster quantization (wide N) or X is one short row.
 bool nvfp4_fused_route(int64_t T, int64_t N, int64_t K, int epilogue) {
-  if (select_route_internal(SPG_KIND_NVFP4, T, N, K, epilogue, 1, false, false).variant != 4)
-    return false;
-  return N >= 16384 || (T == 1 && K <= 8192);
+  if (T < 1 || T > 4 || epilogue < 0 || epilogue > 2) return false;
+  if (T * (K / 32) * 34 > 200 * 1024) return false;  // the GEMV's shared memory
+  return (T <= 2 && N >= 16384) || (T == 1 && K <= 8192);
 }
 
 ActLayout act_layout(int kind, int64_t T, int64_t N, int64_t K, int epilogue) {
@@ -165,9 +164,7 @@ extern "C" spg_status nvfp4_linear_bf16(const void* X, const uint8_t* W, const u
   float* gA = reinterpret_cast<float*>(ws + l.scratch + 16);
   uint8_t* A = ws + l.codes;
   uint8_t* sfA = ws + l.scales;
-  spg_status s = spg_nvfp4_global_scale(X, T * K, gA, amax, stream);
-  if (s != SPG_OK) return s;
-  s = spg_quantize_nvfp4(X, T, K, gA, A, sfA, stream);
+  const spg_status s = spg_quantize_nvfp4_act(X, T, K, gA, amax, A, sfA, stream);
   if (s != SPG_OK) return s;
   return nvfp4_gemm_ws(A, sfA, gA, W, sfW, gW, bias, bias_scale, residual, Y, T, N, K, epilogue,
                        ws + l.gemm, workspace_bytes - l.gemm, stream);

@@ -214,6 +214,61 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
   }
 }
 
+// Global scale and block quantizer in one CTA, for tensors small enough
+// that one SM streams them faster than four launches (memset, amax,
+// finalize, encode) take to start: the CTA's maximum gives g (written to
+// *g_out), then each lane encodes 16-element blocks as the block quantizer
+// does (consecutive lanes on consecutive blocks, so a group's four scale
+// bytes sit in lanes 4j .. 4j+3).
+constexpr int kNvSmallThreads = 1024;
+constexpr int64_t kNvSmallMaxElems = 72 * 1024;  // measured: one CTA wins up to ~70K elements
+
+__global__ void __launch_bounds__(kNvSmallThreads) quantize_nvfp4_small_kernel(
+    const uint4* __restrict__ x, uint32_t rows, uint32_t rows_pad, uint32_t upr,
+    float* __restrict__ g_out, uint2* __restrict__ codes, uint32_t* __restrict__ sf) {
+  __shared__ float red[kNvSmallThreads / 32];
+  const uint32_t nblk = rows * upr * 4;
+  const uint32_t nvec = nblk * 2;
+  if (rows_pad != rows) {
+    // Zero the scale tiles of the last row block whole (16-byte stores): its
+    // padding rows stay zero, its real rows are written below, after the
+    // barriers of the block maximum.  (One word per padding row and scale
+    // column, each with its own index arithmetic, took ~20 us at K = 17408.)
+    uint4* t = reinterpret_cast<uint4*>(sf) + ((rows_pad >> 7) - 1) * upr * 32;
+    for (uint32_t i = threadIdx.x; i < upr * 32; i += kNvSmallThreads)
+      t[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  float a = 0.f;
+  for (uint32_t i = threadIdx.x; i < nvec; i += kNvSmallThreads) a = fmaxf(a, vec_amax(__ldg(x + i)));
+  const float g = nvfp4_global_from_amax(block_max<kNvSmallThreads>(a, red));
+  if (threadIdx.x == 0) *g_out = g;
+  const Nvfp4BlockEncoder enc(g);
+  const int lane = threadIdx.x & 31;
+  // every lane of a warp takes the same number of trips (the shuffles)
+  for (uint32_t base = threadIdx.x - lane; base < nblk; base += kNvSmallThreads) {
+    const uint32_t blk = base + lane;
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    if (blk < nblk) {
+      v0 = __ldg(x + 2 * blk);
+      v1 = __ldg(x + 2 * blk + 1);
+    }
+    uint2 c;
+    float dec;
+    const uint32_t sfc = enc.block(v0, v1, c.x, c.y, &dec);
+    uint32_t w = sfc << (8 * (lane & 3));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    if (blk < nblk) {
+      codes[blk] = c;
+      if ((lane & 3) == 0) {
+        const uint32_t grp = blk >> 2;
+        const uint32_t r = grp / upr, cb = grp - r * upr;
+        sf[(r >> 7) * upr * 128 + cb * 128 + (r & 31) * 4 + ((r >> 5) & 3)] = w;
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------
 // Allocation-free variant of the per-tensor quantizer.  Its amax scratch is
 // this file-scope device array instead of a caller-provided buffer: slots
@@ -395,6 +450,29 @@ extern "C" spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K,
       static_cast<uint32_t>(upr), g, reinterpret_cast<uint2*>(codes),
       reinterpret_cast<uint32_t*>(sf));
   return launch_status();
+}
+
+extern "C" spg_status spg_quantize_nvfp4_act(const void* x, int64_t rows, int64_t K, float* g,
+                                             float* amax_scratch, uint8_t* codes, uint8_t* sf,
+                                             spg_stream_t stream) {
+  if (rows < 0 || K < 0) return SPG_ERR_INVALID_ARG;
+  if (rows == 0) return SPG_OK;
+  if (!x || !g || !amax_scratch || !codes || !sf) return SPG_ERR_INVALID_ARG;
+  if (K == 0 || K % 64 != 0) return SPG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || !aligned16(g) ||
+      !aligned16(amax_scratch))
+    return SPG_ERR_MISALIGNED;
+  if (rows * K <= kNvSmallMaxElems) {
+    const int64_t rows_pad = (rows + 127) / 128 * 128;
+    quantize_nvfp4_small_kernel<<<1, kNvSmallThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), static_cast<uint32_t>(rows),
+        static_cast<uint32_t>(rows_pad), static_cast<uint32_t>(K / 64), g,
+        reinterpret_cast<uint2*>(codes), reinterpret_cast<uint32_t*>(sf));
+    return launch_status();
+  }
+  const spg_status st = spg_nvfp4_global_scale(x, rows * K, g, amax_scratch, stream);
+  if (st != SPG_OK) return st;
+  return spg_quantize_nvfp4(x, rows, K, g, codes, sf, stream);
 }
 
 extern "C" size_t spg_nvfp4_sf_bytes(int64_t rows, int64_t K) {

@@ -105,25 +105,29 @@ def test_route_selector_forced_variants(lib, monkeypatch):
 
 def test_route_selector_gemv(lib, monkeypatch):
     """NVFP4 at T <= 4 takes the CUDA-core GEMV (variant 4: two weight rows
-    per warp, four warps per CTA, no workspace); a forced tile variant or
-    T > 4 does not."""
+    per warp, four warps per CTA, no workspace) for N up to 16384 and T <= 2
+    or K <= 8192; a forced tile variant, wider N or T > 4 does not."""
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
     monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
-    for T, slots in [(1, 1), (2, 2), (3, 4), (4, 4)]:
+    for T, K in [(1, 17408), (2, 17408), (3, 6144), (4, 6144)]:
         for epi in ("linear", "add", "swiglu"):
-            r = spg.select_route("nvfp4", T, 5120, 17408, epi, workspace=True)
+            r = spg.select_route("nvfp4", T, 5120, K, epi, workspace=True)
             assert r["variant"] == 4 and r["block_n"] == 2 and r["grid"] == 640
             assert r["split_k"] == 1 and r["workspace_bytes"] == 0
-            assert r["smem_bytes"] == slots * (17408 // 32) * 40  # decoded activations
+            assert r["smem_bytes"] == T * (K // 32) * 34  # decoded activations
     assert spg.gemm_workspace_bytes("nvfp4", 1, 5120, 17408, "add") == 0
-    assert spg.select_route("nvfp4", 1, 34816, 5120, "swiglu")["variant"] == 4
+    for T in (3, 4):
+        assert spg.select_route("nvfp4", T, 5120, 17408, "add")["variant"] != 4
+    assert spg.select_route("nvfp4", 1, 34816, 5120, "swiglu")["variant"] != 4
     assert spg.select_route("fp8_rowscaled", 1, 5120, 17408, "add")["variant"] != 4
     monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
     assert spg.select_route("nvfp4", 1, 5120, 17408, "add")["variant"] == 3
     monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv")
+    assert spg.select_route("nvfp4", 4, 5120, 17408, "add")["variant"] == 4
+    assert spg.select_route("nvfp4", 1, 34816, 5120, "swiglu")["variant"] == 4
     # the decoded activations must fit the CTA's shared memory
-    assert spg.select_route("nvfp4", 4, 256, 40960, "add")["variant"] == 4
-    assert spg.select_route("nvfp4", 4, 256, 41216, "add")["variant"] != 4
+    assert spg.select_route("nvfp4", 4, 256, 48128, "add")["variant"] == 4
+    assert spg.select_route("nvfp4", 4, 256, 48384, "add")["variant"] != 4
     assert spg.select_route("nvfp4", 5, 5120, 17408, "add")["variant"] != 4
 
 
@@ -134,11 +138,12 @@ def test_act_workspace_sizes(lib, monkeypatch):
     for v in ("SPG_FORCE_VARIANT", "SPG_FORCE_TAIL", "SPG_FORCE_GROUP_M"):
         monkeypatch.delenv(v, raising=False)
     up = lambda v: (v + 255) // 256 * 256
-    # the fused decode kernel: wide N at T <= 4, or one token with K <= 8192
-    for T in (1, 2, 3, 4):
+    # the fused decode kernel: wide N at T <= 2, or one token with K <= 8192
+    for T in (1, 2):
         assert spg.act_workspace_bytes("nvfp4", T, 34816, 5120, "swiglu") == 0
     assert spg.act_workspace_bytes("nvfp4", 1, 5120, 6144, "add") == 0
     for T, N, K, epi in [(1, 5120, 17408, "add"), (2, 5120, 6144, "add"),
+                         (3, 34816, 5120, "swiglu"), (4, 34816, 5120, "swiglu"),
                          (5, 5120, 17408, "add"), (64, 5120, 6144, "add"),
                          (8192, 34816, 5120, "swiglu")]:
         need = 256 + up(T * K // 2) + up(spg.nvfp4_sf_bytes(T, K))

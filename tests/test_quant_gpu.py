@@ -181,3 +181,29 @@ def test_nvfp4_many_blocks_bit_exact():
     bad = np.argwhere(codes.cpu().numpy() != oc)
     assert bad.size == 0, f"{len(bad)} code bytes differ, first {bad[:5].tolist()}"
     assert np.array_equal(sf_blocked_to_rowmajor(sf.cpu().numpy(), rows, K), osf)
+
+
+@pytest.mark.parametrize("rows,K", [(1, 64), (3, 1024), (4, 17408), (7, 5120), (64, 2048),
+                                    (129, 5120)])
+def test_nvfp4_act_quantizer(rows, K):
+    """Global scale + block quantizer in one call: one kernel up to 73,728
+    elements, the two-pass kernels beyond; bit-exact against the oracle and
+    identical to the two calls, padding scale rows zero."""
+    x = normal_bf16((rows, K), seed=rows * 5 + K)
+    xf = bf16_bits_to_f32(x).copy()
+    xf[0, :16] = 0.0                           # an all-zero block
+    if rows > 1:
+        xf[1, 16:32] *= 1e-7                   # a block whose scale underflows
+    x = f32_to_bf16_bits(xf)
+    xd = cuda_bf16(x)
+    codes, sf, g = spg.quantize_nvfp4_act(xd)
+    og = oracle.nvfp4_global_scale(x)
+    assert g.item() == float(og)
+    oc, osf = oracle.quantize_nvfp4(x, og)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    blocked = sf.cpu().numpy()
+    assert np.array_equal(sf_blocked_to_rowmajor(blocked, rows, K), osf)
+    g2 = spg.nvfp4_global_scale(xd)
+    c2, s2 = spg.quantize_nvfp4(xd, g2)
+    assert torch.equal(codes, c2) and torch.equal(sf, s2)
+    assert spg.last_device_error() == 0
