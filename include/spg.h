@@ -395,12 +395,12 @@ SPG_API spg_status fp8_tensor_gemm_ws(char layout_a, char layout_b, int64_t batc
  *   nvfp4_linear_bf16 = spg_nvfp4_global_scale(X) -> gA,
  *     spg_quantize_nvfp4(X, gA) -> (A, sfA) (as spg_quantize_nvfp4_act does
  *     them), then nvfp4_gemm_ws(A, sfA, gA, ...).
- * The codes, scales and result are exactly those of that sequence.  At
- * NVFP4 decode widths (T <= 4, the GEMV route) the whole operator is one
- * kernel: each CTA of the GEMV quantizes X into its shared memory itself and
- * nothing but Y is written (no workspace is needed).  Otherwise the
+ * The codes, scales and result are exactly those of that sequence.  The
  * quantizer and the GEMM run back to back on `stream`, the codes and scales
- * held in the workspace.
+ * held in the workspace.  With SPG_FORCE_VARIANT=gemv_fused the NVFP4
+ * operator at T <= 4 is instead one kernel (each CTA cluster of the GEMV
+ * quantizes X into its shared memory; nothing but Y is written and no
+ * workspace is needed) -- measured slower than the two kernels.
  * workspace: device memory, 16-byte aligned, owned by the caller, at least
  *   spg_act_workspace_bytes(kind, T, N, K, epilogue) bytes for the full
  *   route (activation codes and scales, then the GEMM's K-split workspace);

@@ -458,8 +458,8 @@ _ACT_KINDS = {"fp8_rowscaled": 0, "nvfp4": 1}
 
 def act_workspace_bytes(kind, T, N, K, epilogue="linear") -> int:
     """Bytes of workspace the activation operators take (0: none needed)."""
-    return int(load_library().spg_act_workspace_bytes(_ACT_KINDS[kind], T, N, K,
-                                                      _epi(epilogue)))
+    return int(_lib_for_call().spg_act_workspace_bytes(_ACT_KINDS[kind], T, N, K,
+                                                       _epi(epilogue)))
 
 
 def act_workspace(kind, T, N, K, epilogue="linear", device="cuda"):

@@ -253,6 +253,11 @@ void reload_forced_route() {
   g_forced_loaded = false;
 }
 
+bool forced_variant_is(const char* name) {
+  const ForcedRoute f = forced_route();
+  return std::strcmp(f.variant, name) == 0;
+}
+
 // ---------------------------------------------------------------- routes
 // Per-shape selection.  The cost compared is the one the ninfer FP8 route
 // model uses ("Routing": waves needed times the work one SM carries through

@@ -30,6 +30,9 @@ void set_tmap_cache(bool on);
 // its next call.
 void reload_forced_route();
 
+// Whether SPG_FORCE_VARIANT (as last read) names this variant.
+bool forced_variant_is(const char* name);
+
 // Tail split of a two-SM schedule along N (see plan_items): with `units` CTA
 // pairs and `tiles` tiles of width bn, the tiles of the last partial wave
 // are split into `ways` (1, 2 or 4) narrower items, each a whole number of

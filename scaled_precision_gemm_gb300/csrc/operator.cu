@@ -5,12 +5,14 @@
 // "The fp8 A8 GEMM stages its operands through TMA": the A8 call sites
 // quantize their activations per row at run time).
 //
-// NVFP4 at decode widths (the GEMV route, T <= 4) is one kernel: every CTA
-// of the GEMV computes the activations' global scale, block scales and
-// codes itself, in the order and precision of the block quantizer, into the
-// shared planes it multiplies from.  Elsewhere the quantizer and the GEMM
-// run back to back on the caller's stream, the codes and scales passing
-// through the caller's workspace.
+// The quantizer and the GEMM run back to back on the caller's stream, the
+// codes and scales passing through the caller's workspace (NVFP4 at decode
+// widths: the one-CTA global-scale-and-encode kernel, then the GEMV).  The
+// library also has a single-kernel form for NVFP4 decode widths -- each CTA
+// cluster of the GEMV quantizes the activations itself, in the order and
+// precision of the block quantizer, into the shared planes it multiplies
+// from -- pinned with SPG_FORCE_VARIANT=gemv_fused (measured slower than the
+// two kernels; see nvfp4_fused_route).
 #include <cuda_bf16.h>
 
 #include "common.h"
@@ -34,19 +36,20 @@ struct ActLayout {
   bool fused = false;    // NVFP4 decode: one GEMV kernel, no workspace
 };
 
-// The fused decode kernel (the GEMV in its operator form) where it measured
-// faster than the quantizer kernels followed by the plain route (GB300,
-// graph-replayed, L2 flushed; us):
-//   SwiGLU N = 34816, K = 5120, T = 1 / 2:  47.6 / 51.7 against 52-56
-//   linear_add N = 5120, K = 6144, T = 1:   21.0 against 25.1
-// and not elsewhere (SwiGLU T = 3 / 4 57.9 / 64.0 against ~53 on the tile
-// route; N = 5120, K = 17408, T = 1 / 2: 39.4 / 49.6 against 35.3 / 41.4):
-// the kernel pays off where the weight stream is long against the
-// per-cluster quantization (wide N) or X is one short row.
+// The fused decode kernel (the GEMV in its operator form) runs when
+// SPG_FORCE_VARIANT=gemv_fused pins it.  It measured faster than the
+// four-launch quantizer followed by the GEMV (SwiGLU N = 34816, T = 1 / 2:
+// 47.6 / 51.7 against 52-56 us; linear_add N = 5120, K = 6144, T = 1: 21.0
+// against 25.1), but not than the one-CTA quantizer (spg_quantize_nvfp4_act)
+// followed by the plain route, which the operator now uses (45.5 / 49.6
+// against 41.4 / 45.5; 20.9 against 18.9; GB300, graph-replayed, L2
+// flushed): the cluster's quantization plus its two cluster barriers cost
+// more than a one-CTA kernel whose latency overlaps the GEMV's start.
 bool nvfp4_fused_route(int64_t T, int64_t N, int64_t K, int epilogue) {
+  (void)N;
   if (T < 1 || T > 4 || epilogue < 0 || epilogue > 2) return false;
   if (T * (K / 32) * 34 > 200 * 1024) return false;  // the GEMV's shared memory
-  return (T <= 2 && N >= 16384) || (T == 1 && K <= 8192);
+  return forced_variant_is("gemv_fused");
 }
 
 ActLayout act_layout(int kind, int64_t T, int64_t N, int64_t K, int epilogue) {

@@ -138,12 +138,14 @@ def test_act_workspace_sizes(lib, monkeypatch):
     for v in ("SPG_FORCE_VARIANT", "SPG_FORCE_TAIL", "SPG_FORCE_GROUP_M"):
         monkeypatch.delenv(v, raising=False)
     up = lambda v: (v + 255) // 256 * 256
-    # the fused decode kernel: wide N at T <= 2, or one token with K <= 8192
-    for T in (1, 2):
+    # the fused decode kernel only where pinned (T <= 4, its shared memory)
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv_fused")
+    for T in (1, 2, 3, 4):
         assert spg.act_workspace_bytes("nvfp4", T, 34816, 5120, "swiglu") == 0
-    assert spg.act_workspace_bytes("nvfp4", 1, 5120, 6144, "add") == 0
-    for T, N, K, epi in [(1, 5120, 17408, "add"), (2, 5120, 6144, "add"),
-                         (3, 34816, 5120, "swiglu"), (4, 34816, 5120, "swiglu"),
+    assert spg.act_workspace_bytes("nvfp4", 5, 5120, 6144, "add") > 0
+    monkeypatch.delenv("SPG_FORCE_VARIANT")
+    for T, N, K, epi in [(1, 5120, 17408, "add"), (2, 5120, 6144, "add"), (1, 5120, 6144, "add"),
+                         (1, 34816, 5120, "swiglu"), (4, 34816, 5120, "swiglu"),
                          (5, 5120, 17408, "add"), (64, 5120, 6144, "add"),
                          (8192, 34816, 5120, "swiglu")]:
         need = 256 + up(T * K // 2) + up(spg.nvfp4_sf_bytes(T, K))

@@ -6,10 +6,9 @@ scales, codes; FP8: row scales, codes) and multiplies them with the
 oracle-quantized weights; the operator's output must meet the element-wise
 tolerance of the GEMM tests.  The operator's codes are by definition those
 of the library's quantizers, so its output must also equal, bit for bit,
-the library's own quantize-then-GEMM sequence on the same route -- for the
-NVFP4 decode widths that compares the single fused kernel (each CTA
-quantizes the activations itself) with the quantizer kernels followed by
-the GEMV.  Output buffers are NaN-filled with NaN guard bands.
+the library's own quantize-then-GEMM sequence on the same route -- and the
+single fused NVFP4 decode kernel (pinned; each CTA cluster quantizes the
+activations itself) against the quantizer kernels followed by the GEMV.  Output buffers are NaN-filled with NaN guard bands.
 """
 import numpy as np
 import pytest
@@ -31,6 +30,15 @@ def default_route(monkeypatch):
         monkeypatch.delenv(v, raising=False)
 
 
+@pytest.fixture(params=["sequence", "fused"])
+def nv_form(request, monkeypatch):
+    """The NVFP4 operator as two kernels (the default) or, at T <= 4, as the
+    single fused decode kernel (pinned)."""
+    if request.param == "fused":
+        monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv_fused")
+    return request.param
+
+
 def nv_weights(N, K, seed):
     w = normal_bf16((N, K), seed=seed)
     gW = oracle.nvfp4_global_scale(w)
@@ -50,13 +58,20 @@ def nv_reference(x, W, sfW, gW, res, epi, rows=None, bias=None, bias_scale=None)
                              bias_scale=bias_scale)
 
 
-def nv_library_sequence(xd, Wd, sfWd, gWd, resd, epi, T, N, K, bias=None, bias_scale=None):
-    """The library's quantizers, then its GEMM with the operator's workspace."""
+def nv_library_sequence(xd, Wd, sfWd, gWd, resd, epi, T, N, K, fused, monkeypatch,
+                        bias=None, bias_scale=None):
+    """The library's quantizers, then its GEMM with the operator's workspace
+    (for the fused kernel: the GEMV, whose sums it shares)."""
     gA = spg.nvfp4_global_scale(xd)
     A, sfA = spg.quantize_nvfp4(xd, gA)
-    return spg.nvfp4_gemm(A, sfA, gA, Wd, sfWd, gWd, residual=resd, epilogue=epi, bias=bias,
-                          bias_scale=bias_scale,
-                          workspace=spg.gemm_workspace("nvfp4", T, N, K, epi, device=DEV))
+    if fused:
+        monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv")
+    y = spg.nvfp4_gemm(A, sfA, gA, Wd, sfWd, gWd, residual=resd, epilogue=epi, bias=bias,
+                       bias_scale=bias_scale,
+                       workspace=spg.gemm_workspace("nvfp4", T, N, K, epi, device=DEV))
+    if fused:
+        monkeypatch.setenv("SPG_FORCE_VARIANT", "gemv_fused")
+    return y
 
 
 def run_nv_operator(xd, Wd, sfWd, gWd, resd, epi, T, N, bias=None, bias_scale=None):
@@ -70,16 +85,11 @@ def run_nv_operator(xd, Wd, sfWd, gWd, resd, epi, T, N, bias=None, bias_scale=No
     return y
 
 
-def fused_expected(T, N, K):
-    """Where the library takes the single fused decode kernel."""
-    return (T <= 2 and N >= 16384) or (T == 1 and K <= 8192)
-
-
 @pytest.mark.parametrize("epi", ["linear", "add", "swiglu"])
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 64, 200])
 @pytest.mark.parametrize("N,K", [(144, 768), (1040, 4352), (16400, 512)])
-def test_nvfp4_operator(T, N, K, epi):
-    fused = fused_expected(T, N, K)
+def test_nvfp4_operator(T, N, K, epi, nv_form, monkeypatch):
+    fused = nv_form == "fused" and T <= 4
     assert (spg.act_workspace_bytes("nvfp4", T, N, K, epi) == 0) == fused
     x = normal_bf16((T, K), seed=T * 7 + N + K)
     W, sfW, gW = nv_weights(N, K, seed=N + 1)
@@ -90,7 +100,7 @@ def test_nvfp4_operator(T, N, K, epi):
     y = run_nv_operator(xd, Wd, sfWd, gWd, resd, epi, T, N)
     assert_within_tol(to_f64(y), nv_reference(x, W, sfW, gW, res, epi),
                       f"nvfp4 operator {epi} {T}x{N}x{K}")
-    seq = nv_library_sequence(xd, Wd, sfWd, gWd, resd, epi, T, N, K)
+    seq = nv_library_sequence(xd, Wd, sfWd, gWd, resd, epi, T, N, K, fused, monkeypatch)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), seq.view(torch.int16))
 
@@ -98,7 +108,7 @@ def test_nvfp4_operator(T, N, K, epi):
 @pytest.mark.parametrize("kind", ["bf16", "fp8"])
 @pytest.mark.parametrize("epi", ["linear", "add", "swiglu"])
 @pytest.mark.parametrize("T,N,K", [(2, 16400, 512), (64, 272, 1024)])
-def test_nvfp4_operator_bias(T, N, K, epi, kind):
+def test_nvfp4_operator_bias(T, N, K, epi, kind, nv_form):
     x = normal_bf16((T, K), seed=11)
     W, sfW, gW = nv_weights(N, K, seed=12)
     if kind == "bf16":
@@ -117,11 +127,11 @@ def test_nvfp4_operator_bias(T, N, K, epi, kind):
     assert_within_tol(to_f64(y), ref, f"nvfp4 operator bias {kind} {epi}")
 
 
-def test_nvfp4_operator_special_activations():
+def test_nvfp4_operator_special_activations(nv_form, monkeypatch):
     """Activations with an all-zero block, a block whose scale underflows to
     zero, an all-zero token and an all-zero tensor (global scale 1)."""
-    T, N, K = 2, 16400, 1024          # the fused decode kernel
-    assert fused_expected(T, N, K)
+    T, N, K = 2, 16400, 1024
+    fused = nv_form == "fused"
     x = normal_bf16((T, K), seed=21).view(np.uint16).copy()
     x[0, 16:32] = 0                                  # zero block
     xf = (x[0].astype(np.uint32) << 16).view(np.float32) * np.float32(1e-7)
@@ -134,7 +144,8 @@ def test_nvfp4_operator_special_activations():
         y = run_nv_operator(xd, Wd, sfWd, gWd, None, "linear", T, N)
         assert_within_tol(to_f64(y), nv_reference(xx, W, sfW, gW, None, "linear"),
                           "nvfp4 operator special blocks")
-        seq = nv_library_sequence(xd, Wd, sfWd, gWd, None, "linear", T, N, K)
+        seq = nv_library_sequence(xd, Wd, sfWd, gWd, None, "linear", T, N, K, fused,
+                                  monkeypatch)
         torch.cuda.synchronize()
         assert torch.equal(y.view(torch.int16), seq.view(torch.int16))
 
@@ -142,7 +153,7 @@ def test_nvfp4_operator_special_activations():
 @pytest.mark.parametrize("T,K,N,epi", [(1, 17408, 5120, "add"), (1, 6144, 5120, "add"),
                                        (4, 6144, 5120, "add"), (2, 5120, 34816, "swiglu"),
                                        (4, 5120, 34816, "swiglu"), (64, 17408, 5120, "add")])
-def test_nvfp4_operator_full_size(T, K, N, epi):
+def test_nvfp4_operator_full_size(T, K, N, epi, nv_form):
     x = normal_bf16((T, K), seed=31)
     W, sfW, gW = nv_weights(N, K, seed=32)
     res = normal_bf16((T, N), seed=33) if epi == "add" else None
