@@ -110,11 +110,12 @@ def workload_cases(name):
     if name == "decode":
         # Narrow T (decode and small batches) at the linear_add widths: the
         # weights stream once, so these are HBM-bound (swapped FP8 tile with
-        # the K split, the NVFP4 GEMV at T <= 4).
+        # the K split; NVFP4: the GEMV at T <= 2 or K <= 8192, else one-CTA
+        # tiles with the K split inside clusters).
         cases = [dict(kind="fp8", T=T, K=K, N=5120, epi="add", w_std=0.02)
                  for T in (1, 16, 64, 128) for K in (17408, 6144)]
         cases += [dict(kind="nvfp4", T=T, K=K, N=5120, epi="add")
-                  for T in (1, 2, 4) for K in (17408, 6144)]
+                  for T in (1, 2, 4, 16, 64, 128) for K in (17408, 6144)]
         return cases
     if name == "fp8_tensor":
         return [dict(kind="tensor", layout=l, M=M, N=N, K=K, batch=b) for (l, M, N, K, b) in [

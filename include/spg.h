@@ -91,9 +91,12 @@ typedef struct {
                         /* warp-stored scales, 4 CUDA-core GEMV for T <= 4   */
                         /* (block_m 1, block_n 2 weight rows per warp), 5    */
                         /* cluster of two one-CTA tiles sharing B by TMA     */
-                        /* multicast)                                        */
+                        /* multicast, 7 one-CTA tiles whose K is split over  */
+                        /* the split_k CTAs of a cluster and reduced through */
+                        /* distributed shared memory: no workspace)          */
   int32_t split_n;      /* last partial wave: tiles split along N this many ways */
   int32_t split_k;      /* last partial wave: tiles split along K this many ways */
+                        /* (variant 7: every tile, one piece per cluster CTA) */
   int64_t workspace_bytes; /* workspace the K split needs (0 without one)     */
   int32_t swap_ab;      /* 1: operands exchanged (weights on the M side, the   */
                         /* T tokens on the N side; block_n covers tokens)     */

@@ -25,6 +25,14 @@ uint32_t next_split_epoch();
 // Streaming multiprocessors of the current device (queried once per device).
 int num_sms();
 
+// Shared-memory bytes each CTA of a cluster K split receives (one-CTA tiles
+// bn columns wide, epilogue chunks of cw columns, split_k pieces): per chunk
+// it finishes (chunk i goes to the CTA of rank i mod split_k), per 32-column
+// sub-block, source piece and TMEM lane quarter one 4 KB block.
+__host__ __device__ constexpr int cluster_recv_bytes(int bn, int cw, int split_k) {
+  return ((bn / cw) + split_k - 1) / split_k * (cw / 32) * split_k * 4 * 4096;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Map a CUDA error to a status; with SPG_DEBUG set in the environment the

@@ -158,13 +158,140 @@ __device__ __forceinline__ uint32_t split_piece_finish(const GemmParams& p, uint
   return mask;
 }
 
+// K split inside a thread-block cluster (one-CTA kernel): the split_k
+// pieces of a tile run as the CTAs of one cluster, cluster rank = piece, and
+// are reduced through distributed shared memory instead of a global
+// workspace.  Each CTA runs exactly one piece, so once its accumulator is
+// full its operand ring is idle; chunk i of the tile is finished by the CTA
+// of rank i mod split_k, whose ring receives every piece's partial sums of
+// that chunk.
+//   free:  one arrival per epilogue warp of the cluster once its CTA's
+//          accumulator is full (its ring is idle and may receive)
+//   ready: one arrival per epilogue warp of the cluster once its partial
+//          sums are written to their owners (or it gave up); a CTA leaves
+//          only after its ready phase completed, so no write into it is
+//          still in flight
+// Every warp gives both arrivals exactly once (cluster_piece_finish, or the
+// kernel's exit path for a warp that never got there), so neither phase
+// waits on a warp that has left.
+struct ClusterSplit {
+  uint64_t* free_bar;
+  uint64_t* ready;
+  uint8_t* ring;     // this CTA's operand ring (receive area)
+  bool arrived;      // this warp has given its free and ready arrivals
+};
+
+// One epilogue warp's share of the cluster reduction of a K-split piece.
+// The warp owns TMEM lane quarter q (t_row: column 0 of the accumulator in
+// that quarter).  Once every CTA of the cluster has a full accumulator
+// (free), it writes its rows' partial sums of every chunk into the chunk's
+// owner (st.shared::cluster, its own CTA included; two TMEM blocks loaded
+// per wait), arrives on every CTA's ready barrier and waits for its own;
+// then, for each chunk this CTA owns, it adds the pieces in split order
+// (piece 0 first) and writes the total back to TMEM.
+// Returns the mask of chunks whose total this warp now holds (bit i: chunk
+// i), 0 after a time-out.  An empty K range (have_k false) contributes
+// zeros.
+template <int BN, int CW>
+__device__ __forceinline__ uint32_t cluster_piece_finish(const GemmParams& p, uint32_t t_row,
+                                                         const WorkItem& tc, int q,
+                                                         ClusterSplit& cs, const WaitCtl& ctl) {
+  static_assert(CW == 32 || CW == 64, "epilogue chunks are 32 or 64 columns");
+  constexpr int kSub = CW / 32;
+  constexpr int kChunks = BN / CW;
+  constexpr int kBlocks = BN / 32;
+  const int lane = threadIdx.x & 31;
+  const int S = p.split_k;
+  const int rank = tc.split;
+  const bool have_k = tc.kb_end > tc.kb_begin;
+  // Receive area (cluster_recv_bytes): per owned chunk (li: its index among
+  // the owner's chunks), 32-column sub-block sb, source piece src and lane
+  // quarter q one 4 KB block of 32 rows x 32 fp32, 16-byte groups
+  // XOR-swizzled by row so a quarter-warp's accesses fall in distinct banks.
+  // Byte offset of group g of this lane's row:
+  auto slot = [&](int li, int sb, int src, int g) {
+    return uint32_t((((li * kSub + sb) * S + src) * 4 + q) * 4096 + lane * 128 +
+                    ((g ^ (lane & 7)) * 16));
+  };
+  auto load_block = [&](int b, uint32_t (&r)[32]) {
+    if (have_k) {
+      tmem_ld_32x32b_x32(t_row + b * 32, r);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+    }
+  };
+  const uint32_t ring_base = smem_u32(cs.ring);
+  auto send_block = [&](int b, const uint32_t (&r)[32]) {
+    const int i = b / kSub;
+    const uint32_t dst = mapa_shared(ring_base, uint32_t(i % S));
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      st_cluster_v4(dst + slot(i / S, b % kSub, rank, g), r[4 * g], r[4 * g + 1], r[4 * g + 2],
+                    r[4 * g + 3]);
+  };
+  __syncwarp();
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) mbar_arrive_cluster(mapa_shared(smem_u32(cs.free_bar), uint32_t(s)));
+  const bool can_send =
+      __all_sync(0xffffffffu, mbar_wait_cluster(cs.free_bar, 0, ctl, kErrWaitFull));
+  if (can_send) {
+    static_assert(kBlocks % 2 == 0, "blocks go out in pairs");
+#pragma unroll 1
+    for (int b = 0; b < kBlocks; b += 2) {
+      uint32_t r0[32], r1[32];
+      load_block(b, r0);
+      load_block(b + 1, r1);
+      if (have_k) tmem_wait_ld();
+      send_block(b, r0);
+      send_block(b + 1, r1);
+    }
+  }
+  fence_acq_rel_cluster();
+  __syncwarp();
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) mbar_arrive_cluster(mapa_shared(smem_u32(cs.ready), uint32_t(s)));
+  cs.arrived = true;
+  const bool ok = can_send &&
+                  __all_sync(0xffffffffu, mbar_wait_cluster(cs.ready, 0, ctl, kErrWaitFull));
+  if (!ok) return 0u;
+  uint32_t mask = 0u;
+#pragma unroll 1
+  for (int i = rank; i < kChunks; i += S) {
+    mask |= 1u << i;
+#pragma unroll 1
+    for (int sb = 0; sb < kSub; ++sb) {
+      float t[32];
+#pragma unroll 1
+      for (int src = 0; src < S; ++src) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float4 v = *reinterpret_cast<const float4*>(cs.ring + slot(i / S, sb, src, g));
+          if (src == 0) {
+            t[4 * g] = v.x; t[4 * g + 1] = v.y; t[4 * g + 2] = v.z; t[4 * g + 3] = v.w;
+          } else {
+            t[4 * g] += v.x; t[4 * g + 1] += v.y; t[4 * g + 2] += v.z; t[4 * g + 3] += v.w;
+          }
+        }
+      }
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(t[j]);
+      tmem_st_32x32b_x32(t_row + (i * kSub + sb) * 32, r);
+    }
+  }
+  tmem_wait_st();
+  return mask;
+}
+
 // ItemFn(item) -> WorkItem with mb already offset for this CTA's rows (a
 // whole tile has n_off = 0, width = BN); the loop runs over items
 // [item_begin, item_end) with stride item_step.  ArriveEmpty(buf) releases
-// accumulator buffer `buf` to the MMA issuer.  K-split pieces (two-SM
-// kernels only, cta_rank: this CTA's rank in the pair) go through
-// split_piece_finish first and then run the epilogue on the chunks whose
-// total they hold.
+// accumulator buffer `buf` to the MMA issuer.  K-split pieces go through
+// split_piece_finish (two-SM kernels, global workspace; cta_rank: this CTA's
+// rank in the pair) or, with CLUSTER_SPLIT (one-CTA kernel, one piece per
+// CTA of a cluster), cluster_piece_finish with *csplit, and then run the
+// epilogue on the chunks whose total they hold.
 // RES_TMA (linear_add): the residual of each 32 x 32 output block comes by a
 // TMA copy (tmR, 32 x 32 boxes, the output's swizzle) into the warp's
 // staging buffer, one chunk ahead -- the first chunk's before the
@@ -177,7 +304,8 @@ __device__ __forceinline__ uint32_t split_piece_finish(const GemmParams& p, uint
 // done, and no load into the ring remains) all of its residual blocks are
 // requested at once into the idle ring (idle_ring: BN/32 x 2 KB per warp)
 // and waited for together: one memory round trip instead of one per chunk.
-template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty, bool RES_TMA = false>
+template <int EPI, int SCALE, int BN, typename ItemFn, typename ArriveEmpty, bool RES_TMA = false,
+          bool CLUSTER_SPLIT = false>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtensorMap* tmY,
                                               uint32_t tmem_base, uint64_t* acc_full,
                                               ArriveEmpty arrive_empty, uint8_t* epi_smem,
@@ -185,7 +313,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
                                               ItemFn item_fn, const WaitCtl& ctl, int cta_rank,
                                               const CUtensorMap* tmR = nullptr,
                                               uint64_t* res_bars = nullptr,
-                                              uint8_t* idle_ring = nullptr) {
+                                              uint8_t* idle_ring = nullptr,
+                                              ClusterSplit* csplit = nullptr) {
   using E = EpilogueCfg<EPI, SCALE, BN>;
   constexpr bool kResTma = RES_TMA && EPI == SPG_EPI_ADD;
   const int warp = threadIdx.x >> 5;
@@ -220,7 +349,12 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
     // Chunks this warp finishes: all of them, or those whose K-split total
     // it holds.
     uint32_t own_mask = 0xffffffffu;
-    if (tc.split >= 0) {
+    if (tc.split >= 0 && CLUSTER_SPLIT) {
+      // The chunks of rank tc.split: known before the reduction, which runs
+      // below, after this item's epilogue operands have been requested.
+      own_mask = 0u;
+      for (int i = tc.split; i < 32; i += p.split_k) own_mask |= 1u << i;
+    } else if (tc.split >= 0) {
       if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
       tc_fence_after();
       own_mask = split_piece_finish<BN, E::kAccColsPerChunk, 8>(
@@ -233,6 +367,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       }
     }
     const bool split_item = tc.split >= 0;
+    // A chunk's residual is loaded one chunk ahead (the first before the
+    // accumulator is ready) unless a global-workspace K split decides the
+    // chunks only after its reduction.
+    const bool res_ahead = !split_item || CLUSTER_SPLIT;
     // After a K-split reduction TMEM holds the total of all pieces.
     const bool have_k = tc.split >= 0 || tc.kb_end > tc.kb_begin;
     const int m0 = tc.mb * 128;
@@ -264,10 +402,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       }
     };
     float swc[kCw], biasc[kCw];
-    {
-      const int c_first = own_mask == 0xffffffffu ? 0 : __ffs(own_mask) - 1;
-      chunk_cols(c_first, swc, biasc);
-    }
+    const int c_first = own_mask == 0xffffffffu ? 0 : __ffs(own_mask) - 1;
+    if (c_first >= 0 && c_first < nch) chunk_cols(c_first, swc, biasc);
     uint4 res_cur[4];
     // The last item's residual comes whole into the idle operand ring.
     const bool res_bulk = kResTma && !split_item && idle_ring != nullptr &&
@@ -281,12 +417,21 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
         res_load(chunk_ctr & 1, n0, m0 + q * 32, tc.b);
       }
     } else if constexpr (EPI == SPG_EPI_ADD) {
-      if (!split_item) load_residual_chunk(p, m, n0, row_ok, res_cur);
+      if (res_ahead && c_first >= 0 && c_first < nch)
+        load_residual_chunk(p, m, n0 + c_first * 32, row_ok, res_cur);
     }
 
-    if (tc.split < 0) {
+    if (tc.split < 0 || CLUSTER_SPLIT) {
       if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
       tc_fence_after();
+    }
+    if constexpr (CLUSTER_SPLIT) {
+      // Every CTA of the cluster takes part, including one that finishes no
+      // chunk; 0 back means the reduction timed out.
+      if (split_item &&
+          cluster_piece_finish<BN, E::kAccColsPerChunk>(p, t_row, tc, q, *csplit, ctl) == 0u &&
+          own_mask != 0u)
+        break;
     }
     if constexpr (kResTma) {
       if (res_bulk) {
@@ -315,8 +460,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
       const int c_next = later ? c + __ffs(later) : -1;
       if (c_next >= 0 && c_next < nch) chunk_cols(c_next, swn, biasn);
       if constexpr (EPI == SPG_EPI_ADD) {
-        // A K-split piece finishes scattered chunks: load each one's residual.
-        if (split_item) load_residual_chunk(p, m, n0 + acc_c0, row_ok, res_cur);
+        // A global-workspace K-split piece finishes scattered chunks: load
+        // each one's residual.
+        if (!res_ahead) load_residual_chunk(p, m, n0 + acc_c0, row_ok, res_cur);
       }
       uint32_t raw[E::kAccColsPerChunk];
       if (have_k) {
@@ -354,7 +500,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const CUtenso
             res_cur[g] = *reinterpret_cast<const uint4*>(rbuf + ((g ^ ((lane >> 1) & 3)) * 16));
         }
       } else if constexpr (EPI == SPG_EPI_ADD) {
-        if (!split_item && c + 1 < nch) load_residual_chunk(p, m, n0 + acc_c0 + 32, row_ok, res_next);
+        if (res_ahead && c_next >= 0 && c_next < nch)
+          load_residual_chunk(p, m, n0 + c_next * 32, row_ok, res_next);
       }
       if (have_k) tmem_wait_ld();
       if (c == last_c && item + item_step < item_end) {

@@ -29,7 +29,9 @@
 
 namespace spg {
 
-template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+// ACC_BUFS: TMEM accumulator buffers (2: the epilogue of one tile overlaps
+// the next tile's main loop; 1 when every CTA runs one work item).
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, int ACC_BUFS = 2>
 struct GemmCfg {
   static constexpr int kBM = 128;
   static constexpr int kBKBytes = 128;  // K bytes per stage (one 128-byte swizzle row)
@@ -41,7 +43,7 @@ struct GemmCfg {
   static constexpr int kSfbBytes = KIND == kKindNvfp4 ? kNHalves * 4 * 512 : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kMmaN = KIND == kKindNvfp4 ? 128 : BN;
-  static constexpr int kAccBufs = 2;
+  static constexpr int kAccBufs = ACC_BUFS;
   static constexpr int kSfColsPerKStep = KIND == kKindNvfp4 ? 4 + 4 * kNHalves : 0;
   static constexpr int kSfColsPerStage = kKSteps * kSfColsPerKStep;
   static constexpr int kTmemUsed = kAccBufs * BN + STAGES * kSfColsPerStage;
@@ -62,7 +64,7 @@ struct GemmCfg {
   static_assert(kTmemUsed <= 512, "TMEM budget exceeded");
   static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-byte aligned (128B swizzle)");
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static_assert(2 * STAGES + 6 <= kBarBytes / 8 - 2, "barrier area too small");
+  static_assert(2 * STAGES + 8 <= kBarBytes / 8 - 2, "barrier area too small");
   static_assert(!(KIND == kKindNvfp4 && (A_MN || B_MN)), "NVFP4 operands are K-major");
 
   // Instruction descriptor.
@@ -81,11 +83,16 @@ struct GemmCfg {
   }
 };
 
-template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+// CSPLIT: launched in clusters of p.split_k CTAs, one work item per CTA:
+// the K-split pieces of a tile (cluster rank = piece) reduced through
+// distributed shared memory into the idle operand rings
+// (cluster_piece_finish); no workspace.
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE,
+          bool CSPLIT = false>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
-  using Cfg = GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE>;
+  using Cfg = GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE, CSPLIT ? 1 : 2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -98,7 +105,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint64_t* stall = drain + 1;  // test hook: never arrived on
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall + 1);
+  uint64_t* cs_free = stall + 1;  // CSPLIT: cluster reduction barriers
+  uint64_t* cs_ready = stall + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall + 3);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -115,6 +124,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(drain, 1);
     mbar_init(stall, 1);
+    if constexpr (CSPLIT) {
+      mbar_init(cs_free, uint32_t(Cfg::kEpiWarps * p.split_k));
+      mbar_init(cs_ready, uint32_t(Cfg::kEpiWarps * p.split_k));
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -128,7 +141,12 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // The peers arrive on this CTA's reduction barriers: their initialisation
+  // must be visible across the cluster first.
+  if constexpr (CSPLIT)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl ctl{p.timeout_ns, p.err, abort_flag};
@@ -140,13 +158,13 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-        const TileCoord tc = tile_coord(tile, p);
+      for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
+        const WorkItem tc = work_item(item, p, BN);
         const int m0 = tc.mb * Cfg::kBM;
         const int n0 = tc.nb * BN;
         const int za = tc.b * p.a_batch_mul;
         const int zb = tc.b * p.b_batch_mul;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = tc.kb_begin; kb < tc.kb_end; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, ctl, kErrWaitEmpty)) {
             ok = false;
             break;
@@ -201,13 +219,15 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+      for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x, ++it) {
+        const WorkItem w = work_item(item, p, BN);
         const int buf = it & 1;
         const uint32_t acc_ph = (it >> 1) & 1;
         if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, ctl, kErrWaitAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          const bool acc = kb != w.kb_begin;
           if (!mbar_wait(&full[s], ph, ctl, kErrWaitFull)) {
             ok = false;
             break;
@@ -238,7 +258,7 @@ __global__ void __launch_bounds__(192, 1)
                 const uint64_t bdesc =
                     smem_desc(sb + h * 128 * Cfg::kBKBytes + j * 32, 16, 1024, kSwizzle128B);
                 mma_nvf4(d_tmem + h * 128, adesc, bdesc, kIdesc, col, col + 4 + 4 * h,
-                         (kb | j) != 0);
+                         acc || j != 0);
               }
             }
           } else {
@@ -253,7 +273,7 @@ __global__ void __launch_bounds__(192, 1)
                 bdesc = smem_desc(sb + j * 32 * 128, 128 * Cfg::kBKBytes, 1024, kSwizzle128B);
               else
                 bdesc = smem_desc(sb + j * 32, 16, 1024, kSwizzle128B);
-              mma_f8f6f4(d_tmem, adesc, bdesc, kIdesc, (kb | j) != 0);
+              mma_f8f6f4(d_tmem, adesc, bdesc, kIdesc, acc || j != 0);
             }
           }
           tc_commit(&empty[s]);
@@ -271,19 +291,34 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    ClusterSplit cs{cs_free, cs_ready, ring, false};
+    auto arrive_fn = [&](int b) { mbar_arrive(&acc_empty[b]); };
+    auto item_fn = [&](int item) { return work_item(item, p, BN); };
     // Test hook: wait on a barrier nothing arrives on, so the bounded wait
     // runs out, the CTA aborts and every role drains and returns.
     if (p.debug_stall && !mbar_wait(stall, 0, ctl, kErrInjectedStall)) {
       // aborted: skip the tiles; the other roles see the abort flag
-    } else
-    epilogue_loop<EPI, SCALE, BN>(
-        p, &tmY, tmem_base, acc_full, [&](int b) { mbar_arrive(&acc_empty[b]); }, epi, blockIdx.x,
-        p.total_tiles, gridDim.x,
-        [&](int tile) {
-          const TileCoord tc = tile_coord(tile, p);
-          return WorkItem{tc.b, tc.mb, tc.nb, 0, BN, 0, p.num_k_blocks, -1, 0};
-        },
-        ctl, 0);
+    } else {
+      epilogue_loop<EPI, SCALE, BN, decltype(item_fn), decltype(arrive_fn), false, CSPLIT>(
+          p, &tmY, tmem_base, acc_full, arrive_fn, epi, blockIdx.x, p.total_items, gridDim.x,
+          item_fn, ctl, 0, nullptr, nullptr, nullptr, &cs);
+    }
+    if constexpr (CSPLIT) {
+      // Leave only once every epilogue warp of the cluster has finished
+      // writing into this CTA (a warp that never reached the reduction gives
+      // its arrivals here).
+      if (!cs.arrived) {
+        __syncwarp();
+        if (lane == 0) {
+          for (int s = 0; s < p.split_k; ++s)
+            mbar_arrive_cluster(mapa_shared(smem_u32(cs_free), uint32_t(s)));
+          for (int s = 0; s < p.split_k; ++s)
+            mbar_arrive_cluster(mapa_shared(smem_u32(cs_ready), uint32_t(s)));
+        }
+      }
+      if (lane == 0) mbar_wait_drain_cluster(cs_ready, 0, p.drain_ns, p.err);
+      __syncwarp();
+    }
   }
 
   tc_fence_before();

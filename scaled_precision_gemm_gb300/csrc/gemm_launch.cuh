@@ -40,6 +40,58 @@ spg_status launch_gemm_variant(const GemmMaps& maps, const GemmParams& p, int gr
   return launch_status();
 }
 
+// One-CTA variant with the K split inside clusters: clusters of p.split_k
+// CTAs, grid = p.total_items (one piece per CTA).
+template <int KIND, int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE>
+spg_status launch_gemm_csplit_variant(const GemmMaps& maps, const GemmParams& p,
+                                      cudaStream_t stream) {
+  using Cfg = GemmCfg<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE, 1>;
+  auto kern = gemm_kernel<KIND, EPI, BN, STAGES, A_MN, B_MN, SCALE, true>;
+  if (p.split_k < 2 || p.split_k > kMaxClusterSplit || p.split_full != 0 ||
+      p.total_items != p.total_tiles * p.split_k ||
+      cluster_recv_bytes(BN, Cfg::kAccColsPerChunk, p.split_k) > STAGES * Cfg::kStageBytes)
+    return SPG_ERR_INVALID_ARG;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes),
+                    "cudaFuncSetAttribute") != SPG_OK)
+      return SPG_ERR_CUDA;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.total_items), 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.split_k);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.y, p),
+                  "cudaLaunchKernelEx") != SPG_OK)
+    return SPG_ERR_CUDA;
+  return launch_status();
+}
+
+// K split of every tile inside clusters (route variant 7): the plan the
+// selector made for this shape.
+inline void plan_cluster_items(GemmParams& p, const spg_route& r, int ring_bytes, int cw) {
+  const KSplit k = csplit_plan(p.total_tiles, num_sms(), p.num_k_blocks, 8, r.block_n, cw,
+                               ring_bytes);
+  if (k.split_k != r.split_k) return;  // leaves an unsplit plan: the launcher refuses it
+  p.split_k = k.split_k;
+  p.kb_per_split = k.kb_per_split;
+  p.split_full = 0;
+  p.total_items = p.total_tiles * k.split_k;
+}
+
 // Two-SM variant: clusters of 2 CTAs, grid = 2 x pairs.
 template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
 spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, int grid,

@@ -22,6 +22,11 @@ spg_status launch(const spg_route& r, const GemmMaps& m, const GemmParams& p, cu
     if (p.bias_kind) return launch_nvfp4_2sm_variant<EPI, 5, true>(m, p, r.grid, s);
     return launch_nvfp4_2sm_variant<EPI, 5, false>(m, p, r.grid, s);
   }
+  if (r.variant == 7) {
+    if (r.block_n == 256)
+      return launch_gemm_csplit_variant<kKindNvfp4, EPI, 256, 3, false, false, kScaleScalar>(m, p, s);
+    return launch_gemm_csplit_variant<kKindNvfp4, EPI, 128, 5, false, false, kScaleScalar>(m, p, s);
+  }
   return launch_gemm_variant<kKindNvfp4, EPI, 128, 5, false, false, kScaleScalar>(m, p, r.grid, s);
 }
 
@@ -79,8 +84,11 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
   const int64_t kh = K / 2;
   const int64_t n_out = epilogue == SPG_EPI_SWIGLU ? N / 2 : N;
   GemmMaps maps;
+  // B box: the rows one CTA stages per stage (a pair tile's CTA stages half
+  // of its 256 rows; a one-CTA tile all of block_n).
+  const uint32_t b_rows = r.block_m == 256 ? 128u : static_cast<uint32_t>(r.block_n);
   if (!make_tmap_3d(&maps.a, A, false, kh, T, 1, kh, kh * T, 128, 128, 128) ||
-      !make_tmap_3d(&maps.b, W, false, kh, N, 1, kh, kh * N, 128, 128, 128) ||
+      !make_tmap_3d(&maps.b, W, false, kh, N, 1, kh, kh * N, 128, b_rows, 128) ||
       !make_tmap_3d(&maps.y, Y, true, n_out, T, 1, n_out * 2, n_out * 2 * T, 32, 32, 64))
     return SPG_ERR_CUDA;
   if (r.block_m == 256) {
@@ -113,6 +121,9 @@ spg_status nvfp4_impl(const uint8_t* A, const uint8_t* sfA, const float* gA, con
     const int pairs = num_sms() / 2;
     plan_items(p, r, pairs, workspace);
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
+  } else if (r.variant == 7) {
+    const int ring = r.stages * (128 * 128 + r.block_n * 128 + 2048 + (r.block_n / 128) * 2048);
+    plan_cluster_items(p, r, ring, epilogue == SPG_EPI_SWIGLU ? 64 : 32);
   }
   switch (epilogue) {
     case SPG_EPI_LINEAR: return launch<SPG_EPI_LINEAR>(rr, maps, p, stream);

@@ -98,19 +98,6 @@ __device__ __forceinline__ float gemv_bias(const GemvParams& p, int n) {
 constexpr int kGemvCluster = 4;  // measured against 8 on GB300: equal or faster on every decode shape
 constexpr int kGemvMaxCluster = 8;
 
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
-
 // Shared-memory bytes of the decoded activations of one CTA: per token two
 // planes of K/32 16-byte words (the int8 of each chunk's two blocks) and
 // K/32 pairs of E4M3 scale codes (decoded where they are used: kept as

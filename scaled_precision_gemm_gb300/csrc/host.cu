@@ -310,7 +310,9 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const int pairs = sms / 2;
   const int64_t nb = batch > 0 ? batch : 1;
   // SPG_FORCE_VARIANT pins the tile shape for A/B runs and tests:
-  // 2sm | 2sm192 | 2sm160 | 2sm128 (pair tiles), 1sm256 | 1sm128 (one CTA).
+  // 2sm | 2sm192 | 2sm160 | 2sm128 (pair tiles), 1sm256 | 1sm128 (one CTA);
+  // NVFP4 also 2sm_st | 2sm_cp | 2sm_mc (pair tiles), 1sm_cks | 1sm256_cks
+  // (one-CTA tiles, K split inside clusters), gemv, gemv_fused.
   // SPG_FORCE_TAIL = none | n | k pins how the last partial wave is split.
   const ForcedRoute forced = forced_route();
   const char* forced_name = forced.variant[0] ? forced.variant : nullptr;
@@ -325,6 +327,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   const double fixed = 6.0;  // per-tile fixed cost in 128-byte-deep K blocks
   KSplit best_ks;
   int best_ways = 1;
+  int cluster_split = 1;  // variant 7: CTAs per cluster (K pieces per tile)
   // Swapped pair tile for narrow T (FP8 row-scaled linear / linear_add, and
   // the per-tensor GEMM with both operands K-major; one problem): the weight
   // rows fill the MMA's 256-row M side and the tokens its N side (64 or 128
@@ -430,6 +433,33 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     const bool mc = forced_name && std::strcmp(forced_name, "2sm_mc") == 0;
     r.variant = one_cta ? 2 : (mc ? 5 : (st_scales ? 3 : 0));
     if (r.variant == 5) r.stages = 3;
+    // One-CTA tiles whose K is split over the CTAs of a cluster (variant 7,
+    // reduced through distributed shared memory, no workspace): 1sm_cks
+    // (128 x 128 tiles) or 1sm256_cks (128 x 256).  The 128 x 128 form is
+    // the default wherever every tile gets at least two pieces in one wave;
+    // measured on GB300 (us, linear_add N = 5120, L2 flushed; against the
+    // best other tile route): K = 17408 T = 16-64 26.6 / 36.9-38.9, T = 128
+    // 26.7-28.7 / 43.0; K = 6144 T = 64-128 20.5 / 22.5.  The 128 x 256 form
+    // measured slower wherever both apply (34.8 / 26.6 at T = 64).
+    const bool cks128 = forced_name ? !std::strcmp(forced_name, "1sm_cks") : nb == 1;
+    const bool cks256 = forced_name && !std::strcmp(forced_name, "1sm256_cks");
+    if (cks128 || cks256) {
+      const int bn = cks256 ? 256 : 128;
+      const int stages = bn == 256 ? 3 : 5;
+      const int ring = stages * (128 * 128 + bn * 128 + 2048 + (bn / 128) * 2048);
+      const int64_t tiles1 = ((T + 127) / 128) * ((N + bn - 1) / bn) * nb;
+      const KSplit cs =
+          csplit_plan(tiles1, sms, nkb, 8, bn, epilogue == SPG_EPI_SWIGLU ? 64 : 32, ring);
+      if (cs.split_k > 1) {
+        r.block_m = 128;
+        r.block_n = bn;
+        r.stages = stages;
+        r.acc_buffers = 1;
+        r.variant = 7;
+        cluster_split = cs.split_k;
+        best_ks = KSplit();
+      }
+    }
   } else {
     // Pair tiles first (widths 256/192/160/128), then one-CTA tiles.  The
     // efficiencies are steady-state tensor-pipe fractions measured on GB300
@@ -512,6 +542,9 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   } else if (r.block_m == 256 && best_ways > 1) {
     r.split_n = best_ways;
     items = tiles - tiles % units + (tiles % units) * best_ways;
+  } else if (cluster_split > 1) {
+    r.split_k = cluster_split;
+    items = tiles * cluster_split;  // one wave: items <= units
   }
   const int64_t g = items < units ? items : units;
   r.grid = static_cast<int>((g < 1 ? 1 : g) * (r.block_m == 256 ? 2 : 1));
@@ -521,7 +554,7 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     stage_bytes = 128 * 128 + (r.variant == 5 ? 2 : 1) * 128 * 128 + 2048 + 4096;
     epi_warps = 8;
   } else if (kind == SPG_KIND_NVFP4) {
-    stage_bytes = 128 * 128 + 128 * 128 + 2048 + 2048;
+    stage_bytes = 128 * 128 + r.block_n * 128 + 2048 + (r.block_n / 128) * 2048;
   } else {
     stage_bytes = 128 * 128 + (r.block_m == 256 ? r.block_n / 2 : r.block_n) * 128;
     if (r.block_m == 256) epi_warps = 4;

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include "common.h"
 #include "spg.h"
 
 namespace spg {
@@ -77,6 +78,33 @@ inline KSplit ksplit_plan(int64_t tiles, int64_t units, int64_t nkb) {
   k.split_k = static_cast<int>(s);
   k.kb_per_split = static_cast<int>(kbps);
   k.tail_tiles = rem;
+  return k;
+}
+
+// K split of one-CTA tiles inside thread-block clusters: with fewer tiles
+// than SMs every tile is reduced by split_k CTAs of one cluster, as many as
+// the SMs allow (one wave, one piece per CTA), at most kMaxClusterSplit,
+// each piece at least min_kb K blocks deep and none empty, and the partial
+// sums each CTA receives (cluster_recv_bytes for tiles bn wide with
+// epilogue chunks of cw columns) within its ring_bytes of operand ring.
+// The pieces are summed through distributed shared memory: no workspace.
+constexpr int kMaxClusterSplit = 4;
+inline KSplit csplit_plan(int64_t tiles, int64_t sms, int64_t nkb, int64_t min_kb, int bn,
+                          int cw, int ring_bytes) {
+  KSplit k;
+  if (tiles <= 0 || nkb <= 0 || sms <= 0) return k;
+  int64_t s = sms / tiles;
+  if (s > kMaxClusterSplit) s = kMaxClusterSplit;
+  while (s > 1 && ((nkb + s - 1) / s < min_kb ||
+                   cluster_recv_bytes(bn, cw, static_cast<int>(s)) > ring_bytes))
+    --s;
+  if (s < 2) return k;
+  const int64_t kbps = (nkb + s - 1) / s;
+  s = (nkb + kbps - 1) / kbps;  // no empty piece
+  if (s < 2) return k;
+  k.split_k = static_cast<int>(s);
+  k.kb_per_split = static_cast<int>(kbps);
+  k.tail_tiles = tiles;
   return k;
 }
 

@@ -193,6 +193,37 @@ def test_route_selector_swap(lib, monkeypatch):
     assert spg.select_route("nvfp4", 64, 5120, 17408, "add")["swap_ab"] == 0
 
 
+def test_route_selector_cluster_split(lib, monkeypatch):
+    """NVFP4 with few tiles: one-CTA 128 x 128 tiles whose K is split over
+    the CTAs of a cluster (variant 7) wherever every tile gets two to four
+    pieces of at least 8 K blocks in one wave, with or without a workspace
+    (it needs none); the GEMV keeps decode widths, wide problems keep the
+    pair tiles."""
+    monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+    monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
+    for T, N, K, epi, S in [(3, 5120, 17408, "add", 3), (128, 5120, 17408, "linear", 3),
+                            (64, 5120, 6144, "swiglu", 3), (512, 512, 4096, "add", 2),
+                            (200, 1024, 8192, "add", 4)]:
+        for ws in (False, True):
+            r = spg.select_route("nvfp4", T, N, K, epi, workspace=ws)
+            tiles = -(-T // 128) * -(-N // 128)
+            assert (r["variant"], r["block_m"], r["block_n"], r["split_k"]) == (7, 128, 128, S), r
+            assert r["grid"] == tiles * S <= 152 and r["workspace_bytes"] == 0, r
+            nkb = K // 256
+            kbps = -(-nkb // S)
+            assert kbps >= 8 and (S - 1) * kbps < nkb  # no empty piece
+        assert spg.gemm_workspace_bytes("nvfp4", T, N, K, epi) == 0
+    assert spg.select_route("nvfp4", 1, 5120, 17408, "add")["variant"] == 4   # GEMV
+    assert spg.select_route("nvfp4", 256, 5120, 17408, "add")["variant"] == 2  # 80 tiles
+    assert spg.select_route("nvfp4", 1024, 5120, 17408, "add")["variant"] == 3
+    assert spg.select_route("nvfp4", 64, 5120, 2048, "add")["variant"] != 7   # 8 K blocks
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "1sm256_cks")
+    r = spg.select_route("nvfp4", 256, 5120, 17408, "add")
+    assert (r["variant"], r["block_n"], r["split_k"], r["grid"]) == (7, 256, 3, 120), r
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
+    assert spg.select_route("nvfp4", 128, 5120, 17408, "add")["variant"] == 3
+
+
 def test_route_selector_k_split(lib, monkeypatch):
     """Workspace routes split the last partial wave along K; the plain routes never do."""
     monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
@@ -201,6 +232,11 @@ def test_route_selector_k_split(lib, monkeypatch):
                                ("fp8_rowscaled", 64, 6144, 17408, "linear"),
                                ("nvfp4", 128, 5120, 17408, "add"),
                                ("fp8_tensor", 128, 4096, 16384, "linear")]:
+        # NVFP4 narrow T splits inside clusters by default; pin the pair tile
+        if kind == "nvfp4":
+            monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
+        else:
+            monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
         plain = spg.select_route(kind, T, N, K, epi)
         assert plain["split_k"] == 1 and plain["workspace_bytes"] == 0
         r = spg.select_route(kind, T, N, K, epi, workspace=True)
@@ -220,6 +256,7 @@ def test_route_selector_k_split(lib, monkeypatch):
         nkb = (K // 2 if kind == "nvfp4" else K + 127) // 128
         kbps = -(-nkb // r["split_k"])
         assert kbps >= 4 and (r["split_k"] - 1) * kbps < nkb  # no empty piece
+    monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
     # NVFP4 at T = 256: the one-CTA 128 x 128 tile (measured faster there)
     assert spg.select_route("nvfp4", 256, 5120, 17408, "add", workspace=True)["block_m"] == 128
     # short K: the finish costs more than the split saves

@@ -111,6 +111,34 @@ def test_pair_kernel_timeout_is_reported_and_context_survives(variant, monkeypat
     assert_within_tol(to_f64(y), ref(), f"{variant} after time-out")
 
 
+def test_cluster_split_timeout_is_reported_and_context_survives(monkeypatch):
+    """The NVFP4 one-CTA tiles with the K split inside clusters: every CTA's
+    epilogue stalls, so none reaches the reduction; each still gives its
+    arrivals on its peers' barriers on the way out and waits (bounded) for
+    theirs, so no CTA leaves while a peer may still write into it."""
+    monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+    T, N, K = 64, 512, 6144
+    host, dev = _nvfp4_inputs(T, N, K)
+    r = spg.select_route("nvfp4", T, N, K)
+    assert r["variant"] == 7 and r["split_k"] == 3, r
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    spg.set_wait_timeout_ns(20_000_000)
+    spg.debug_inject_stall(True)
+    try:
+        spg.nvfp4_gemm(*dev)
+        code = spg.last_device_error_code()
+    finally:
+        spg.debug_inject_stall(False)
+        spg.set_wait_timeout_ns(2_000_000_000)
+    assert code == INJECTED, hex(code)
+    assert spg.last_device_error() == 0
+    y = spg.nvfp4_gemm(*dev)
+    torch.cuda.synchronize()
+    assert spg.last_device_error() == 0
+    assert_within_tol(to_f64(y), oracle.nvfp4_gemm(*host), "cluster split after time-out")
+
+
 def test_status_codes_are_distinct_for_host_errors():
     with pytest.raises(spg.SpgError) as e:
         spg.fp8_rowscaled_gemm(torch.zeros((4, 24), dtype=torch.uint8, device=DEV),

@@ -60,6 +60,15 @@ def test_route_invariants(kind, epi):
             if r["swap_ab"]:
                 assert kind in ("fp8_rowscaled", "fp8_tensor") and epi != "swiglu" and T <= 128, tag
                 assert r["block_n"] == (64 if T <= 64 else 128), tag
+            if r["variant"] == 7 and kind == "nvfp4":
+                # K split inside clusters: one piece per CTA, one wave, no workspace
+                s, n = r["split_k"], nkb(kind, K)
+                kbps = -(-n // s)
+                tiles = -(-T // 128) * -(-N // r["block_n"])
+                assert 2 <= s <= 4 and kbps >= 8 and (s - 1) * kbps < n, tag
+                assert r["block_m"] == 128 and r["grid"] == tiles * s <= 2 * PAIRS, tag
+                assert r["workspace_bytes"] == 0 and r["split_n"] == 1, tag
+                continue
             if not ws:
                 assert r["split_k"] == 1 and r["workspace_bytes"] == 0, tag
             if r["split_k"] > 1:
