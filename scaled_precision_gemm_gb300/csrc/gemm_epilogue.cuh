@@ -206,12 +206,13 @@ __device__ __forceinline__ uint32_t cluster_piece_finish(const GemmParams& p, ui
   const bool have_k = tc.kb_end > tc.kb_begin;
   // Receive area (cluster_recv_bytes): per owned chunk (li: its index among
   // the owner's chunks), 32-column sub-block sb, source piece src and lane
-  // quarter q one 4 KB block of 32 rows x 32 fp32, 16-byte groups
-  // XOR-swizzled by row so a quarter-warp's accesses fall in distinct banks.
-  // Byte offset of group g of this lane's row:
+  // quarter q one 4 KB block of 32 rows x 32 fp32, stored group-major: the
+  // 16-byte group g (columns 4g .. 4g+3) of the warp's 32 rows is one
+  // contiguous 512-byte run, so each warp-wide store to another CTA moves
+  // whole 128-byte lines and each local load is conflict-free.  Byte offset
+  // of group g of this lane's row:
   auto slot = [&](int li, int sb, int src, int g) {
-    return uint32_t((((li * kSub + sb) * S + src) * 4 + q) * 4096 + lane * 128 +
-                    ((g ^ (lane & 7)) * 16));
+    return uint32_t((((li * kSub + sb) * S + src) * 4 + q) * 4096 + g * 512 + lane * 16);
   };
   auto load_block = [&](int b, uint32_t (&r)[32]) {
     if (have_k) {

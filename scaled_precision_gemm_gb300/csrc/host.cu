@@ -438,9 +438,9 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     // (128 x 128 tiles) or 1sm256_cks (128 x 256).  The 128 x 128 form is
     // the default wherever every tile gets at least two pieces in one wave;
     // measured on GB300 (us, linear_add N = 5120, L2 flushed; against the
-    // best other tile route): K = 17408 T = 16-64 26.6 / 36.9-38.9, T = 128
-    // 26.7-28.7 / 43.0; K = 6144 T = 64-128 20.5 / 22.5.  The 128 x 256 form
-    // measured slower wherever both apply (34.8 / 26.6 at T = 64).
+    // best other tile route): K = 17408 T = 4-64 24.6-26.6 / 34.8-38.9,
+    // T = 128 26.6 / 43.0; K = 6144 T = 64-128 18.4 / 22.5.  The 128 x 256
+    // form measured slower wherever both apply (34.8 / 26.6 at T = 64).
     const bool cks128 = forced_name ? !std::strcmp(forced_name, "1sm_cks") : nb == 1;
     const bool cks256 = forced_name && !std::strcmp(forced_name, "1sm256_cks");
     if (cks128 || cks256) {
