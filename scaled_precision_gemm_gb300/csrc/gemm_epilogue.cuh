@@ -179,7 +179,33 @@ struct ClusterSplit {
   uint64_t* ready;
   uint8_t* ring;     // this CTA's operand ring (receive area)
   bool arrived;      // this warp has given its free and ready arrivals
+  // Cluster rank of the CTA holding piece s of this CTA's rows:
+  // s * rank_stride + rank_offset (one-CTA tiles 1, 0; CTA pairs 2 and the
+  // CTA's side of its pair).
+  uint32_t rank_stride, rank_offset;
+  __device__ __forceinline__ uint32_t peer(int s) const {
+    return uint32_t(s) * rank_stride + rank_offset;
+  }
 };
+
+// Exit path of an epilogue warp under a cluster K split: give the free and
+// ready arrivals if the reduction never ran (a time-out), then wait (drain
+// bound) until every warp of the cluster has finished writing into this CTA.
+__device__ __forceinline__ void cluster_split_exit(const GemmParams& p, ClusterSplit& cs) {
+  const int lane = threadIdx.x & 31;
+  if (!cs.arrived) {
+    __syncwarp();
+    if (lane == 0) {
+      for (int s = 0; s < p.split_k; ++s)
+        mbar_arrive_cluster(mapa_shared(smem_u32(cs.free_bar), cs.peer(s)));
+      for (int s = 0; s < p.split_k; ++s)
+        mbar_arrive_cluster(mapa_shared(smem_u32(cs.ready), cs.peer(s)));
+    }
+    cs.arrived = true;
+  }
+  if (lane == 0) mbar_wait_drain_cluster(cs.ready, 0, p.drain_ns, p.err);
+  __syncwarp();
+}
 
 // One epilogue warp's share of the cluster reduction of a K-split piece.
 // The warp owns TMEM lane quarter q (t_row: column 0 of the accumulator in
@@ -225,7 +251,7 @@ __device__ __forceinline__ uint32_t cluster_piece_finish(const GemmParams& p, ui
   const uint32_t ring_base = smem_u32(cs.ring);
   auto send_block = [&](int b, const uint32_t (&r)[32]) {
     const int i = b / kSub;
-    const uint32_t dst = mapa_shared(ring_base, uint32_t(i % S));
+    const uint32_t dst = mapa_shared(ring_base, cs.peer(i % S));
 #pragma unroll
     for (int g = 0; g < 8; ++g)
       st_cluster_v4(dst + slot(i / S, b % kSub, rank, g), r[4 * g], r[4 * g + 1], r[4 * g + 2],
@@ -233,7 +259,7 @@ __device__ __forceinline__ uint32_t cluster_piece_finish(const GemmParams& p, ui
   };
   __syncwarp();
   if (lane == 0)
-    for (int s = 0; s < S; ++s) mbar_arrive_cluster(mapa_shared(smem_u32(cs.free_bar), uint32_t(s)));
+    for (int s = 0; s < S; ++s) mbar_arrive_cluster(mapa_shared(smem_u32(cs.free_bar), cs.peer(s)));
   const bool can_send =
       __all_sync(0xffffffffu, mbar_wait_cluster(cs.free_bar, 0, ctl, kErrWaitFull));
   if (can_send) {
@@ -251,7 +277,7 @@ __device__ __forceinline__ uint32_t cluster_piece_finish(const GemmParams& p, ui
   fence_acq_rel_cluster();
   __syncwarp();
   if (lane == 0)
-    for (int s = 0; s < S; ++s) mbar_arrive_cluster(mapa_shared(smem_u32(cs.ready), uint32_t(s)));
+    for (int s = 0; s < S; ++s) mbar_arrive_cluster(mapa_shared(smem_u32(cs.ready), cs.peer(s)));
   cs.arrived = true;
   const bool ok = can_send &&
                   __all_sync(0xffffffffu, mbar_wait_cluster(cs.ready, 0, ctl, kErrWaitFull));
@@ -619,14 +645,16 @@ namespace spg {
 // is ready and completing on res_bars[warp].  p.M = weight rows (N of the
 // layer), p.N = tokens (T).  K-split pieces go through split_piece_finish
 // like the unswapped tile.
-template <int EPI, int BN, typename ItemFn, typename ArriveEmpty, int SCALE = kScaleRow>
+template <int EPI, int BN, typename ItemFn, typename ArriveEmpty, int SCALE = kScaleRow,
+          bool CLUSTER_SPLIT = false>
 __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CUtensorMap* tmY,
                                                    uint32_t tmem_base, uint64_t* acc_full,
                                                    ArriveEmpty arrive_empty, uint8_t* epi_smem,
                                                    int item_begin, int item_end, int item_step,
                                                    ItemFn item_fn, const WaitCtl& ctl,
                                                    int cta_rank, const CUtensorMap* tmR,
-                                                   uint64_t* res_bars, uint8_t* res_smem) {
+                                                   uint64_t* res_bars, uint8_t* res_smem,
+                                                   ClusterSplit* csplit = nullptr) {
   static_assert(EPI != SPG_EPI_SWIGLU, "the swapped tile has no SwiGLU epilogue");
   constexpr int kBufBytes = 32 * 64;
   constexpr int kChunks = BN / 32;
@@ -699,7 +727,12 @@ __device__ __forceinline__ void epilogue_loop_swap(const GemmParams& p, const CU
     if (!mbar_wait(&acc_full[buf], acc_ph, ctl, kErrWaitAccFull)) break;
     tc_fence_after();
     uint32_t own_mask = live ? 0xffffffffu : 0u;
-    if (tc.split >= 0) own_mask = split_piece_finish<BN, 32, 8>(p, t_row, tc, cta_rank, q, 0, BN, live);
+    if (tc.split >= 0) {
+      if constexpr (CLUSTER_SPLIT)
+        own_mask &= cluster_piece_finish<BN, 32>(p, t_row, tc, q, *csplit, ctl);
+      else
+        own_mask = split_piece_finish<BN, 32, 8>(p, t_row, tc, cta_rank, q, 0, BN, live);
+    }
     own_mask &= (1u << kChunks) - 1u;
     if constexpr (EPI == SPG_EPI_ADD) {
       // Every lane observes the completed copies itself.

@@ -12,6 +12,13 @@ spg_status dispatch(const spg_route& r, const GemmMaps& m, const GemmParams& p, 
     if (r.swap_ab) {
       // linear_add gives one ring stage to its residual blocks.
       constexpr bool kAdd = EPI == SPG_EPI_ADD;
+      if (r.variant == 8) {
+        if (r.block_n == 64)
+          return launch_gemm_2sm_variant<EPI, 64, kAdd ? 9 : 10, false, false, kScaleRow, true,
+                                         true>(m, p, r.grid, s);
+        return launch_gemm_2sm_variant<EPI, 128, kAdd ? 7 : 8, false, false, kScaleRow, true,
+                                       true>(m, p, r.grid, s);
+      }
       if (r.block_n == 64)
         return launch_gemm_2sm_variant<EPI, 64, kAdd ? 9 : 10, false, false, kScaleRow, true>(
             m, p, r.grid, s);
@@ -80,7 +87,10 @@ spg_status rowscaled_impl(const uint8_t* A, const float* sa, const uint8_t* W, c
     if (!p.err) return SPG_ERR_CUDA;
     if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
     const int pairs = num_sms() / 2;
-    plan_items(p, r, pairs, workspace);
+    if (r.variant == 8)
+      plan_pair_cluster_items(p, r, pairs);
+    else
+      plan_items(p, r, pairs, workspace);
     spg_route rr = r;
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
     p.row_scale = sw;

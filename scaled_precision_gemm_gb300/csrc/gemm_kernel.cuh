@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    ClusterSplit cs{cs_free, cs_ready, ring, false};
+    ClusterSplit cs{cs_free, cs_ready, ring, false, 1u, 0u};
     auto arrive_fn = [&](int b) { mbar_arrive(&acc_empty[b]); };
     auto item_fn = [&](int item) { return work_item(item, p, BN); };
     // Test hook: wait on a barrier nothing arrives on, so the bounded wait
@@ -303,22 +303,9 @@ __global__ void __launch_bounds__(192, 1)
           p, &tmY, tmem_base, acc_full, arrive_fn, epi, blockIdx.x, p.total_items, gridDim.x,
           item_fn, ctl, 0, nullptr, nullptr, nullptr, &cs);
     }
-    if constexpr (CSPLIT) {
-      // Leave only once every epilogue warp of the cluster has finished
-      // writing into this CTA (a warp that never reached the reduction gives
-      // its arrivals here).
-      if (!cs.arrived) {
-        __syncwarp();
-        if (lane == 0) {
-          for (int s = 0; s < p.split_k; ++s)
-            mbar_arrive_cluster(mapa_shared(smem_u32(cs_free), uint32_t(s)));
-          for (int s = 0; s < p.split_k; ++s)
-            mbar_arrive_cluster(mapa_shared(smem_u32(cs_ready), uint32_t(s)));
-        }
-      }
-      if (lane == 0) mbar_wait_drain_cluster(cs_ready, 0, p.drain_ns, p.err);
-      __syncwarp();
-    }
+    // Leave only once every epilogue warp of the cluster has finished
+    // writing into this CTA.
+    if constexpr (CSPLIT) cluster_split_exit(p, cs);
   }
 
   tc_fence_before();

@@ -20,6 +20,11 @@
 // wave of tiles is split along N into narrower items, whose MMAs carry the
 // narrower N in the instruction descriptor, or along K into pieces whose
 // partial sums meet in a workspace (work_item, split_piece_finish).
+// CSPLIT (swapped tile): every tile is split along K into split_k pieces run
+// by the split_k pairs of one cluster of 2 x split_k CTAs, one piece per
+// pair, and reduced through distributed shared memory (cluster_piece_finish):
+// a CTA pair is two CTAs whose cluster ranks differ in bit 0, the even one
+// leading it.
 #pragma once
 
 #include "gemm_epilogue.cuh"
@@ -32,7 +37,8 @@ namespace spg {
 // tokens, the MMA's N), and the epilogue writes the transposed accumulator
 // (epilogue_loop_swap).  The swapped tile never splits along N, so its
 // fourth tensor map (tmBnarrow) carries the residual of linear_add.
-template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false,
+          bool CSPLIT = false>
 struct Gemm2smCfg {
   static constexpr int kBM = 128;  // rows per CTA (the pair covers 256)
   static constexpr int kBKBytes = 128;
@@ -70,9 +76,10 @@ struct Gemm2smCfg {
   static_assert(!kResTma || kEpiWarps * (BN / 32) * 32 * 64 <= STAGES * kStageBytes,
                 "the last item's residual blocks must fit the operand ring");
   // barriers, tmem slot + abort flag, residual barriers (two per epilogue
-  // warp), stall barrier, PairExit
-  static_assert((2 * STAGES + 7 + 2 * kEpiWarps) * 8 + sizeof(PairExit) <= kBarBytes,
+  // warp), stall barrier, the cluster reduction's two barriers, PairExit
+  static_assert((2 * STAGES + 9 + 2 * kEpiWarps) * 8 + sizeof(PairExit) <= kBarBytes,
                 "barrier area too small");
+  static_assert(!CSPLIT || SWAP, "the cluster K split serves the swapped tile");
 
   // kind::f8f6f4, E4M3 x E4M3 -> f32, M = 256 (pair), N = BN.
   __host__ __device__ static constexpr uint32_t idesc() {
@@ -81,13 +88,14 @@ struct Gemm2smCfg {
   }
 };
 
-template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false,
+          bool CSPLIT = false>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmY,
                     const __grid_constant__ CUtensorMap tmBnarrow,
                     const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
-  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
+  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP, CSPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -106,11 +114,16 @@ __global__ void __launch_bounds__(192, 1)
   // (one per staging buffer)
   uint64_t* res_bars = drain + 2;
   uint64_t* stall = res_bars + 2 * Cfg::kEpiWarps;  // test hook: nothing arrives on it
-  PairExit* pexit = reinterpret_cast<PairExit*>(stall + 1);
+  uint64_t* cs_free = stall + 1;  // CSPLIT: cluster reduction barriers
+  uint64_t* cs_ready = stall + 2;
+  PairExit* pexit = reinterpret_cast<PairExit*>(stall + 3);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;      // this CTA's side of its pair
+  const uint32_t leader = crank & ~1u;   // cluster rank of the pair's leader
+  const uint16_t pair_mask = uint16_t(0x3u << leader);
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
 
@@ -127,6 +140,10 @@ __global__ void __launch_bounds__(192, 1)
     if constexpr (Cfg::kResBytes != 0 || Cfg::kResTma)
       for (int w = 0; w < 2 * Cfg::kEpiWarps; ++w) mbar_init(&res_bars[w], 1);
     mbar_init(stall, 1);
+    if constexpr (CSPLIT) {
+      mbar_init(cs_free, uint32_t(Cfg::kEpiWarps * p.split_k));
+      mbar_init(cs_ready, uint32_t(Cfg::kEpiWarps * p.split_k));
+    }
     mbar_init(&pexit->bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -174,7 +191,7 @@ __global__ void __launch_bounds__(192, 1)
           const bool narrow = tc.width < BN;
           const uint32_t b_bytes = narrow ? uint32_t(tc.width / 2) * Cfg::kBKBytes : Cfg::kBBytes;
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (Cfg::kABytes + b_bytes));
-          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), leader);
           const int kx = kb * Cfg::kBKBytes;
           if constexpr (A_MN)
             tma_load_3d_pair(sa, &tmA, bar, m0, kx, za);
@@ -198,7 +215,7 @@ __global__ void __launch_bounds__(192, 1)
       if (rank == 0)
         pair_exit_drain<STAGES>(pexit, full, issued, tx, p);
       else
-        pair_exit_publish<STAGES>(pexit, issued, tx);
+        pair_exit_publish<STAGES>(pexit, issued, tx, leader);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer (leader)
@@ -240,14 +257,14 @@ __global__ void __launch_bounds__(192, 1)
               bdesc = smem_desc(sb + j * 32, 16, 1024, kSwizzle128B);
             mma_f8f6f4_pair(d_tmem, adesc, bdesc, idesc, (kb != w.kb_begin) || j != 0);
           }
-          tc_commit_pair_multicast(&empty[s], 0x3);
+          tc_commit_pair_multicast(&empty[s], pair_mask);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair_multicast(&acc_full[buf], 0x3);
+        tc_commit_pair_multicast(&acc_full[buf], pair_mask);
       }
       tc_commit_pair(drain);
       mbar_wait_drain(drain, 0, p.drain_ns, p.err);
@@ -257,17 +274,23 @@ __global__ void __launch_bounds__(192, 1)
     // has aborted and its other roles drain and return.
   } else {
     // -------------------------------------------------------------- epilogue
-    auto arrive_fn = [&](int b) { mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0)); };
+    auto arrive_fn = [&](int b) {
+      mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), leader));
+    };
     auto item_fn = [&](int item) {
       WorkItem w = work_item(item, p, BN);
       w.mb = w.mb * 2 + int(rank);
       return w;
     };
-    if constexpr (SWAP)
-      epilogue_loop_swap<EPI, BN, decltype(item_fn), decltype(arrive_fn), SCALE>(
+    if constexpr (SWAP) {
+      ClusterSplit cs{cs_free, cs_ready, ring, false, 2u, rank};
+      epilogue_loop_swap<EPI, BN, decltype(item_fn), decltype(arrive_fn), SCALE, CSPLIT>(
           p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, p.total_items, num_pairs, item_fn,
-          ctl, int(rank), &tmBnarrow, res_bars, res_smem);
-    else
+          ctl, int(rank), &tmBnarrow, res_bars, res_smem, &cs);
+      // Leave only once every epilogue warp of the cluster has finished
+      // writing into this CTA.
+      if constexpr (CSPLIT) cluster_split_exit(p, cs);
+    } else
       epilogue_loop<EPI, SCALE, BN, decltype(item_fn), decltype(arrive_fn), Cfg::kResTma>(
           p, &tmY, tmem_base, acc_full, arrive_fn, epi, pair, p.total_items, num_pairs, item_fn,
           ctl, int(rank), &tmR, res_bars, ring);

@@ -247,12 +247,14 @@ struct PairExit {
   uint32_t bytes[kPairExitMaxStages];  // the peer's copy bytes per ring slot
 };
 
-// Peer CTA's producer: publish its issued count and per-slot bytes.
+// Peer CTA's producer: publish its issued count and per-slot bytes in the
+// leader's PairExit (leader: the leader's cluster rank).
 template <int STAGES>
 __device__ __forceinline__ void pair_exit_publish(PairExit* px, uint32_t issued,
-                                                  const uint32_t (&bytes)[STAGES]) {
+                                                  const uint32_t (&bytes)[STAGES],
+                                                  uint32_t leader = 0) {
   static_assert(STAGES <= kPairExitMaxStages, "PairExit holds at most 12 ring slots");
-  const uint32_t base = mapa_shared(smem_u32(px), 0);
+  const uint32_t base = mapa_shared(smem_u32(px), leader);
   st_cluster_u32(base + uint32_t(offsetof(PairExit, issued)), issued);
 #pragma unroll
   for (int s = 0; s < STAGES; ++s)

@@ -92,12 +92,30 @@ inline void plan_cluster_items(GemmParams& p, const spg_route& r, int ring_bytes
   p.total_items = p.total_tiles * k.split_k;
 }
 
-// Two-SM variant: clusters of 2 CTAs, grid = 2 x pairs.
-template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false>
+// K split of every tile of a swapped pair schedule inside clusters (route
+// variant 8): the selector's plan, one piece per pair.
+inline void plan_pair_cluster_items(GemmParams& p, const spg_route& r, int pairs) {
+  const KSplit k = ksplit_plan(p.total_tiles, pairs, p.num_k_blocks);
+  if (k.split_k != r.split_k || k.tail_tiles != p.total_tiles) return;  // the launcher refuses
+  p.split_k = k.split_k;
+  p.kb_per_split = k.kb_per_split;
+  p.split_full = 0;
+  p.total_items = p.total_tiles * k.split_k;
+}
+
+// Two-SM variant: clusters of 2 CTAs, grid = 2 x pairs.  CSPLIT (swapped
+// tile): clusters of 2 x p.split_k CTAs, one K piece per pair, every tile
+// split (grid = 2 x p.total_items).
+template <int EPI, int BN, int STAGES, bool A_MN, bool B_MN, int SCALE, bool SWAP = false,
+          bool CSPLIT = false>
 spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, int grid,
                                    cudaStream_t stream) {
-  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
-  auto kern = gemm_kernel_2sm<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP>;
+  using Cfg = Gemm2smCfg<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP, CSPLIT>;
+  auto kern = gemm_kernel_2sm<EPI, BN, STAGES, A_MN, B_MN, SCALE, SWAP, CSPLIT>;
+  if (CSPLIT && (p.split_k < 2 || 2 * p.split_k > 8 || p.split_full != 0 ||
+                 p.total_items != p.total_tiles * p.split_k || grid != 2 * p.total_items ||
+                 cluster_recv_bytes(BN, 32, p.split_k) > STAGES * Cfg::kStageBytes))
+    return SPG_ERR_INVALID_ARG;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPG_ERR_CUDA;
@@ -116,7 +134,7 @@ spg_status launch_gemm_2sm_variant(const GemmMaps& maps, const GemmParams& p, in
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CSPLIT ? static_cast<unsigned>(2 * p.split_k) : 2u;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;

@@ -77,11 +77,21 @@ spg_status tensor_impl(char layout_a, char layout_b, int64_t batch, const uint8_
     if (!p.err) return SPG_ERR_CUDA;
     if (const spg_status bs = set_bias(p, bias, bias_scale); bs != SPG_OK) return bs;
     const int pairs = num_sms() / 2;
-    plan_items(p, r, pairs, workspace);
+    if (r.variant == 8)
+      plan_pair_cluster_items(p, r, pairs);
+    else
+      plan_items(p, r, pairs, workspace);
     spg_route rr = r;
     rr.grid = 2 * (p.total_items < pairs ? p.total_items : pairs);
     p.scalar_a = sA;
     p.scalar_b = sB;
+    if (r.variant == 8) {
+      if (r.block_n == 64)
+        return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 64, 10, false, false, kScaleScalar, true,
+                                       true>(maps, p, rr.grid, stream);
+      return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 128, 8, false, false, kScaleScalar, true,
+                                     true>(maps, p, rr.grid, stream);
+    }
     if (r.block_n == 64)
       return launch_gemm_2sm_variant<SPG_EPI_LINEAR, 64, 10, false, false, kScaleScalar, true>(
           maps, p, rr.grid, stream);

@@ -352,13 +352,21 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
     r.split_n = 1;
     r.split_k = 1;
     int64_t items = r.tiles;
-    // The K split of the last partial wave, priced as for the unswapped
-    // pieces at full efficiency (the pieces stream weights).
-    KSplit k = tail_k_ok ? ksplit_plan(r.tiles, pairs, nkb) : KSplit();
+    // The K split, priced as for the unswapped pieces at full efficiency
+    // (the pieces stream weights).  With fewer weight tiles than pairs every
+    // tile is split and the pieces of a tile run as the pairs of one cluster,
+    // reduced through distributed shared memory (variant 8, no workspace);
+    // otherwise only the last partial wave splits, through a workspace.
+    const bool cluster = r.tiles < pairs;
+    const bool tail_k_cluster = !forced_tail || !std::strcmp(forced_tail, "k");
+    KSplit k = (cluster ? tail_k_cluster : tail_k_ok) ? ksplit_plan(r.tiles, pairs, nkb) : KSplit();
     if (k.split_k > 1 && tail_none_ok && ksplit_piece_time(k, r.block_n) >= kb) k = KSplit();
     if (k.split_k > 1) {
       r.split_k = k.split_k;
-      r.workspace_bytes = ksplit_workspace_bytes(k, r.block_n, epilogue);
+      if (cluster)
+        r.variant = 8;
+      else
+        r.workspace_bytes = ksplit_workspace_bytes(k, r.block_n, epilogue);
       items = r.tiles - k.tail_tiles + k.tail_tiles * k.split_k;
     }
     r.grid = static_cast<int>(2 * (items < pairs ? items : pairs));

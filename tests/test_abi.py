@@ -163,19 +163,33 @@ def test_act_workspace_sizes(lib, monkeypatch):
 
 def test_route_selector_swap(lib, monkeypatch):
     """The swapped narrow-T tile: FP8 row-scaled, one problem, linear or
-    linear_add, T <= 128; token tile 64 or 128 wide, weights in 256-row tiles."""
+    linear_add, T <= 128; token tile 64 or 128 wide, weights in 256-row tiles.
+    With fewer weight tiles than pairs every tile is split along K and its
+    pieces run as the pairs of one cluster (variant 8, no workspace, with or
+    without one); SPG_FORCE_TAIL=none keeps the whole tiles."""
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
     monkeypatch.setenv("SPG_FORCE_VARIANT", "swap")
     for T, bn in [(1, 64), (64, 64), (65, 128), (128, 128)]:
         for epi in ["linear", "add"]:
-            r = spg.select_route("fp8_rowscaled", T, 5120, 17408, epi, workspace=True)
-            assert r["swap_ab"] == 1 and r["block_m"] == 256 and r["block_n"] == bn, (T, r)
-            assert r["tiles"] == 20 and r["split_k"] == 3 and r["split_n"] == 1
-            assert r["workspace_bytes"] == 20 * (3 * 2 * 128 * bn * 4 + 2 * 4 * (bn // 32) * 8)
-            assert r["grid"] == 2 * min(60, 76)
-            assert r["smem_bytes"] <= 232448
-            plain = spg.select_route("fp8_rowscaled", T, 5120, 17408, epi)
-            assert plain["swap_ab"] == 1 and plain["split_k"] == 1 and plain["grid"] == 40
+            for ws in (False, True):
+                r = spg.select_route("fp8_rowscaled", T, 5120, 17408, epi, workspace=ws)
+                assert r["swap_ab"] == 1 and r["block_m"] == 256 and r["block_n"] == bn, (T, r)
+                assert r["variant"] == 8 and r["tiles"] == 20 and r["split_k"] == 3, r
+                assert r["split_n"] == 1 and r["workspace_bytes"] == 0, r
+                assert r["grid"] == 2 * 60
+                assert r["smem_bytes"] <= 232448
+            assert spg.gemm_workspace_bytes("fp8_rowscaled", T, 5120, 17408, epi) == 0
+    monkeypatch.setenv("SPG_FORCE_TAIL", "none")
+    plain = spg.select_route("fp8_rowscaled", 64, 5120, 17408, "add")
+    assert plain["swap_ab"] == 1 and plain["variant"] == 6 and plain["split_k"] == 1
+    assert plain["grid"] == 40
+    monkeypatch.delenv("SPG_FORCE_TAIL")
+    # more weight tiles than pairs (forced): the last partial wave splits
+    # through a workspace, without one the tiles stay whole
+    r = spg.select_route("fp8_rowscaled", 64, 40960, 17408, "add", workspace=True)
+    assert r["variant"] == 6 and r["tiles"] == 160 and r["split_k"] > 1 and r["workspace_bytes"] > 0
+    r = spg.select_route("fp8_rowscaled", 64, 40960, 17408, "add")
+    assert r["variant"] == 6 and r["split_k"] == 1 and r["workspace_bytes"] == 0
     # the default: swapped while the weight tiles leave half of the pairs
     # free (or T <= 16 and one wave of tiles)
     monkeypatch.delenv("SPG_FORCE_VARIANT")
@@ -232,11 +246,9 @@ def test_route_selector_k_split(lib, monkeypatch):
                                ("fp8_rowscaled", 64, 6144, 17408, "linear"),
                                ("nvfp4", 128, 5120, 17408, "add"),
                                ("fp8_tensor", 128, 4096, 16384, "linear")]:
-        # NVFP4 narrow T splits inside clusters by default; pin the pair tile
-        if kind == "nvfp4":
-            monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
-        else:
-            monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+        # narrow T splits inside clusters by default; pin the unswapped pair tile
+        pin = {"nvfp4": "2sm_st", "fp8_rowscaled": "2sm", "fp8_tensor": "2sm"}[kind]
+        monkeypatch.setenv("SPG_FORCE_VARIANT", pin)
         plain = spg.select_route(kind, T, N, K, epi)
         assert plain["split_k"] == 1 and plain["workspace_bytes"] == 0
         r = spg.select_route(kind, T, N, K, epi, workspace=True)

@@ -60,6 +60,15 @@ def test_route_invariants(kind, epi):
             if r["swap_ab"]:
                 assert kind in ("fp8_rowscaled", "fp8_tensor") and epi != "swiglu" and T <= 128, tag
                 assert r["block_n"] == (64 if T <= 64 else 128), tag
+            if r["variant"] == 8:
+                # swapped tile, every tile split inside clusters of 2 x split_k CTAs
+                s, n = r["split_k"], nkb(kind, K)
+                kbps = -(-n // s)
+                assert r["swap_ab"] == 1 and kind != "nvfp4", tag
+                assert 2 <= s <= 4 and kbps >= 4 and (s - 1) * kbps < n, tag
+                assert r["tiles"] * s <= PAIRS and r["grid"] == 2 * r["tiles"] * s, tag
+                assert r["workspace_bytes"] == 0 and r["split_n"] == 1, tag
+                continue
             if r["variant"] == 7 and kind == "nvfp4":
                 # K split inside clusters: one piece per CTA, one wave, no workspace
                 s, n = r["split_k"], nkb(kind, K)

@@ -97,7 +97,14 @@ def test_fp8_splitk_ragged(T, N, K, epi, variant):
     assert_within_tol(to_f64(y), ref, f"fp8 split-K {epi} {T}x{N}x{K} ({r['split_k']} pieces)")
 
 
-def test_fp8_splitk_taken_for_narrow_t():
+def test_fp8_splitk_taken_for_narrow_t(monkeypatch):
+    monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
+    monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
+    # the default narrow-T route: the swapped tile split inside clusters
+    r = spg.select_route("fp8_rowscaled", 64, 528, 16384, "linear", workspace=True)
+    assert r["variant"] == 8 and r["split_k"] > 1 and r["workspace_bytes"] == 0
+    # the unswapped pair tile splits through the workspace
+    monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm")
     r = spg.select_route("fp8_rowscaled", 64, 528, 16384, "linear", workspace=True)
     assert r["block_m"] == 256 and r["split_k"] > 1 and r["workspace_bytes"] > 0
 

@@ -6,7 +6,8 @@ N side (the accumulator is Y transposed; the epilogue writes it back as
 Y [T, N]).  The scales, bias and residual enter in the same order as in the
 unswapped epilogue, so the bar is the usual element-wise tolerance; with a
 K split the result still repeats bit for bit and the workspace counters are
-left at zero.
+left at zero.  With fewer weight tiles than CTA pairs (every shape here) the
+K split runs inside clusters of 2 x split_k CTAs and needs no workspace.
 """
 import numpy as np
 import pytest
@@ -51,7 +52,9 @@ def test_swap_ragged(T, N, K, epi, with_ws, swap):
         y = run(A, sa, W, sw, res, epi, ws if ws.numel() else None)
         check_workspace(buf, ws.numel(), r, epi)
     else:
-        assert r["split_k"] == 1
+        # no workspace: whole tiles, or (fewer tiles than pairs) the K split
+        # inside clusters, which needs none
+        assert r["workspace_bytes"] == 0 and (r["split_k"] == 1 or r["variant"] == 8), r
         y = run(A, sa, W, sw, res, epi)
     ref = oracle.fp8_rowscaled_gemm(A, sa, W, sw, res, epi)
     assert_within_tol(to_f64(y), ref, f"fp8 swap {epi} {T}x{N}x{K} ({r['split_k']} pieces)")
