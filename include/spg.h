@@ -86,7 +86,9 @@ typedef struct {
   int32_t smem_bytes;   /* dynamic shared memory per CTA                      */
   int32_t variant;      /* kernel variant index inside the library (FP8:      */
                         /* 0-3 pair tiles 256/192/160/128 wide, 4-5 one-CTA  */
-                        /* 256/128, 6 swapped pair tile; NVFP4: 0 pair tile  */
+                        /* 256/128, 6 swapped pair tile, 8 swapped pair tile */
+                        /* whose K pieces run as the pairs of one cluster    */
+                        /* (no workspace); NVFP4: 0 pair tile                */
                         /* with copied scales, 2 one-CTA, 3 pair tile with   */
                         /* warp-stored scales, 4 CUDA-core GEMV for T <= 4   */
                         /* (block_m 1, block_n 2 weight rows per warp), 5    */
@@ -353,10 +355,15 @@ SPG_API spg_status fp8_tensor_gemm_bias(char layout_a, char layout_b, int64_t ba
  * bit) and runs the fused epilogue on it.  The result is the same GEMM as
  * the plain entry points define, with fp32 sums taken in a different order.  The pages keep a separate
  * small-T route on sm_120 (ninfer PR #160, the paragraph on the quantizer's
- * plane layout); here the tcgen05 pair kernel covers narrow T by this split
- * and, for fp8_rowscaled_gemm(_ws) linear / linear_add at T <= 128, by a
- * swapped pair tile (the weights on the MMA's 256-row side, the tokens on
- * its N side; spg_route.swap_ab), which the plain entry points use too.
+ * plane layout); here the tcgen05 kernels cover narrow T by this split and,
+ * for fp8_rowscaled_gemm(_ws) linear / linear_add at T <= 128 (and the
+ * per-tensor NT GEMM at M <= 128), by a swapped pair tile (the weights on
+ * the MMA's 256-row side, the tokens on its N side; spg_route.swap_ab).
+ * With fewer tiles than the GPU has CTA pairs (swapped FP8 tile) or SMs
+ * (NVFP4 one-CTA tiles), every tile's K pieces run as the CTAs of one
+ * thread-block cluster and are summed in split order through distributed
+ * shared memory (route variants 8 and 7): no workspace, so the plain entry
+ * points take those splits too and spg_gemm_workspace_bytes is 0 for them.
  *
  * workspace: device memory, 16-byte aligned, at least
  *   spg_gemm_workspace_bytes(kind, T, N, K, epilogue, batch) bytes for the
@@ -434,7 +441,9 @@ SPG_API spg_status nvfp4_linear_bf16(const void* X, const uint8_t* W, const uint
 SPG_API spg_status spg_select_route(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
                             int64_t batch, spg_route* out);
 /* The route of the workspace entry points given a large enough workspace
- * (split_k > 1 and workspace_bytes > 0 when the K split is taken). */
+ * (split_k > 1 and workspace_bytes > 0 when the K split through the
+ * workspace is taken; variants 7 and 8 split inside clusters with
+ * workspace_bytes 0). */
 SPG_API spg_status spg_select_route_ws(int kind, int64_t T, int64_t N, int64_t K, int epilogue,
                                        int64_t batch, spg_route* out);
 
