@@ -251,8 +251,11 @@ SPG_API spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K, co
  * Tensors of at most 73,728 elements (decode widths) take a single kernel
  * (one CTA finds the maximum and encodes every block) instead of the four
  * launches of the two calls (GB300: 10.8 against 21.0 us at 1 x 17408, 14.9
- * against 16.9 at 4 x 17408; 18.9 against 14.9 at 7 x 17408).  Arguments, layouts and errors as for the two
- * calls (amax_scratch: one fp32 of caller-owned scratch). */
+ * against 16.9 at 4 x 17408); up to 524,288 elements one cluster of CTAs
+ * (16 where the device can hold such a cluster, else 8) shares its maxima
+ * through distributed shared memory and encodes in the same launch (10.8
+ * against 14.9 us at 16 x 17408).  Arguments, layouts and errors as for the
+ * two calls (amax_scratch: one fp32 of caller-owned scratch). */
 SPG_API spg_status spg_quantize_nvfp4_act(const void* x, int64_t rows, int64_t K, float* g,
                                           float* amax_scratch, uint8_t* codes, uint8_t* sf,
                                           spg_stream_t stream);

@@ -13,6 +13,7 @@
 // the HBM copy rate -- with an inexact plain multiply).
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.h"
@@ -269,6 +270,104 @@ __global__ void __launch_bounds__(kNvSmallThreads) quantize_nvfp4_small_kernel(
   }
 }
 
+// Global scale and block quantizer in one cluster of up to kNvClusterMax
+// CTAs, for tensors too large for one CTA but small enough that a few SMs
+// stream them faster than four launches take to start.  CTA r of the
+// cluster takes a contiguous run of 16-element blocks (a multiple of 32, so
+// a warp's lanes hold whole 64-element groups), reduces its maximum, and
+// stores it into slot r of every CTA's shared memory; after one cluster
+// barrier every CTA holds all the maxima, forms the same g and encodes its
+// blocks (its run is read a second time, from L2).  The scale tiles of the
+// last row block are zeroed before the barrier, which orders those stores
+// before the real rows' words written after it.
+constexpr int kNvClusterMax = 16;
+// Measured on GB300 (us, cluster / four launches): 87K elements 8.7 / 14.9,
+// 279K 10.8 / 14.9, 393K 10.7 / 12.8, 786K 12.8 / 12.8, 1.1M 14.9 / 12.8.
+constexpr int64_t kNvClusterMaxElems = 512 * 1024;
+
+__global__ void __launch_bounds__(kNvSmallThreads) quantize_nvfp4_cluster_kernel(
+    const uint4* __restrict__ x, uint32_t rows, uint32_t rows_pad, uint32_t upr,
+    float* __restrict__ g_out, uint2* __restrict__ codes, uint32_t* __restrict__ sf) {
+  __shared__ float red[kNvSmallThreads / 32];
+  __shared__ float part[kNvClusterMax];
+  const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
+  const uint32_t nblk = rows * upr * 4;
+  const uint32_t per = ((nblk + ncta - 1) / ncta + 31) / 32 * 32;
+  const uint32_t b0 = min(rank * per, nblk), b1 = min(b0 + per, nblk);
+  if (rows_pad != rows) {
+    uint4* t = reinterpret_cast<uint4*>(sf) + ((rows_pad >> 7) - 1) * upr * 32;
+    for (uint32_t i = rank * kNvSmallThreads + threadIdx.x; i < upr * 32;
+         i += ncta * kNvSmallThreads)
+      t[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  float a = 0.f;
+  for (uint32_t i = 2 * b0 + threadIdx.x; i < 2 * b1; i += kNvSmallThreads)
+    a = fmaxf(a, vec_amax(__ldg(x + i)));
+  a = block_max<kNvSmallThreads>(a, red);
+  if (threadIdx.x < ncta)
+    st_cluster_u32(mapa_shared(smem_u32(&part[rank]), threadIdx.x), __float_as_uint(a));
+  cluster_sync();
+  float m = 0.f;
+  for (uint32_t q = 0; q < ncta; ++q) m = fmaxf(m, part[q]);
+  const float g = nvfp4_global_from_amax(m);
+  if (rank == 0 && threadIdx.x == 0) *g_out = g;
+  const Nvfp4BlockEncoder enc(g);
+  const int lane = threadIdx.x & 31;
+  // every lane of a warp takes the same number of trips (the shuffles)
+  for (uint32_t base = b0 + threadIdx.x - lane; base < b1; base += kNvSmallThreads) {
+    const uint32_t blk = base + lane;
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    if (blk < b1) {
+      v0 = __ldg(x + 2 * blk);
+      v1 = __ldg(x + 2 * blk + 1);
+    }
+    uint2 c;
+    float dec;
+    const uint32_t sfc = enc.block(v0, v1, c.x, c.y, &dec);
+    uint32_t w = sfc << (8 * (lane & 3));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    if (blk < b1) {
+      codes[blk] = c;
+      if ((lane & 3) == 0) {
+        const uint32_t grp = blk >> 2;
+        const uint32_t r = grp / upr, cb = grp - r * upr;
+        sf[(r >> 7) * upr * 128 + cb * 128 + (r & 31) * 4 + ((r >> 5) & 3)] = w;
+      }
+    }
+  }
+}
+
+// Cluster size for quantize_nvfp4_cluster_kernel on the current device: 16
+// where such clusters can be resident (a non-portable size), else 8.
+int nvfp4_cluster_ctas() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  int c = cached[dev].load(std::memory_order_relaxed);
+  if (c != 0) return c;
+  c = 8;
+  auto kern = quantize_nvfp4_cluster_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kNvClusterMax, 1, 1);
+    cfg.blockDim = dim3(kNvSmallThreads, 1, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kNvClusterMax;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) c = kNvClusterMax;
+  }
+  cudaGetLastError();  // a refused query leaves no error behind
+  cached[dev].store(c, std::memory_order_relaxed);
+  return c;
+}
+
 // ----------------------------------------------------------------------
 // Allocation-free variant of the per-tensor quantizer.  Its amax scratch is
 // this file-scope device array instead of a caller-provided buffer: slots
@@ -462,12 +561,35 @@ extern "C" spg_status spg_quantize_nvfp4_act(const void* x, int64_t rows, int64_
   if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || !aligned16(g) ||
       !aligned16(amax_scratch))
     return SPG_ERR_MISALIGNED;
+  const int64_t rows_pad = (rows + 127) / 128 * 128;
   if (rows * K <= kNvSmallMaxElems) {
-    const int64_t rows_pad = (rows + 127) / 128 * 128;
     quantize_nvfp4_small_kernel<<<1, kNvSmallThreads, 0, stream>>>(
         static_cast<const uint4*>(x), static_cast<uint32_t>(rows),
         static_cast<uint32_t>(rows_pad), static_cast<uint32_t>(K / 64), g,
         reinterpret_cast<uint2*>(codes), reinterpret_cast<uint32_t*>(sf));
+    return launch_status();
+  }
+  if (rows * K <= kNvClusterMaxElems) {
+    const int ncta = nvfp4_cluster_ctas();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ncta), 1, 1);
+    cfg.blockDim = dim3(kNvSmallThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ncta);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cuda_status(cudaLaunchKernelEx(&cfg, quantize_nvfp4_cluster_kernel,
+                                       static_cast<const uint4*>(x), static_cast<uint32_t>(rows),
+                                       static_cast<uint32_t>(rows_pad),
+                                       static_cast<uint32_t>(K / 64), g,
+                                       reinterpret_cast<uint2*>(codes),
+                                       reinterpret_cast<uint32_t*>(sf)),
+                    "cudaLaunchKernelEx") != SPG_OK)
+      return SPG_ERR_CUDA;
     return launch_status();
   }
   const spg_status st = spg_nvfp4_global_scale(x, rows * K, g, amax_scratch, stream);

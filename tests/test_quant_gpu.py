@@ -183,12 +183,14 @@ def test_nvfp4_many_blocks_bit_exact():
     assert np.array_equal(sf_blocked_to_rowmajor(sf.cpu().numpy(), rows, K), osf)
 
 
-@pytest.mark.parametrize("rows,K", [(1, 64), (3, 1024), (4, 17408), (7, 5120), (64, 2048),
-                                    (129, 5120)])
+@pytest.mark.parametrize("rows,K", [(1, 64), (3, 1024), (4, 17408), (7, 5120), (5, 17408),
+                                    (64, 2048), (30, 17408), (85, 6144), (129, 5120),
+                                    (130, 6144), (128, 17408)])
 def test_nvfp4_act_quantizer(rows, K):
-    """Global scale + block quantizer in one call: one kernel up to 73,728
-    elements, the two-pass kernels beyond; bit-exact against the oracle and
-    identical to the two calls, padding scale rows zero."""
+    """Global scale + block quantizer in one call: one CTA up to 73,728
+    elements, one cluster up to 512 Ki elements, the two-pass kernels beyond;
+    bit-exact against the oracle and identical to the two calls, padding
+    scale rows zero."""
     x = normal_bf16((rows, K), seed=rows * 5 + K)
     xf = bf16_bits_to_f32(x).copy()
     xf[0, :16] = 0.0                           # an all-zero block
