@@ -558,6 +558,40 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def bind_host_near_gpu(torch, dev):
+    """Run this process on the CPUs the GPU's PCI device reports as local
+    (sysfs local_cpulist), so the pinned host buffers allocated next are
+    first touched, hence placed, in that NUMA node's memory.  Returns what
+    was done, for the JSON line; leaves the affinity alone when the device
+    or its CPU list cannot be read or shares no CPU with the allowed set."""
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except AttributeError:
+        return {"bound": False, "why": "no PCI id in the device properties"}
+    base = os.path.join("/sys/bus/pci/devices", bus)
+    try:
+        text = open(os.path.join(base, "local_cpulist")).read().strip()
+        node = open(os.path.join(base, "numa_node")).read().strip()
+    except OSError:
+        return {"bound": False, "pci": bus, "why": "no local_cpulist"}
+    local = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            local.update(range(int(a), int(b) + 1))
+        elif part:
+            local.add(int(part))
+    allowed = os.sched_getaffinity(0)
+    use = allowed & local
+    if not use:
+        return {"bound": False, "pci": bus, "numa_node": node, "why": "no allowed local CPU"}
+    if use != allowed:
+        os.sched_setaffinity(0, use)
+    return {"bound": True, "pci": bus, "numa_node": node, "cpus": len(use),
+            "changed": use != allowed}
+
+
 def run_e2e(args, spg, torch, dev, prepared, inputs, dist=None, world=1):
     """Same workload through the public API with HOST buffers: per case the
     bf16 activations (and residual) are copied from pinned host memory, the
@@ -566,14 +600,18 @@ def run_e2e(args, spg, torch, dev, prepared, inputs, dist=None, world=1):
     on two copy streams, ordered by events, so case i+1's inputs travel
     while case i computes and case i-1's output travels back."""
     h2d = d2h = 0
+    prev_affinity = os.sched_getaffinity(0)
+    host_affinity = bind_host_near_gpu(torch, dev)
     for k in prepared:
         k.x_host = k.x.cpu().pin_memory()
         k.res_host = None if k.res is None else k.res.cpu().pin_memory()
         k.out_host = torch.empty(k.out.shape, dtype=k.out.dtype).pin_memory()
+        k.out_host.zero_()  # first touch here, in the bound node's memory
         k.x_d = torch.empty_like(k.x)
         k.res_d = None if k.res is None else torch.empty_like(k.res)
         h2d += k.x_host.numel() * 2 + (0 if k.res_host is None else k.res_host.numel() * 2)
         d2h += k.out_host.numel() * 2
+    os.sched_setaffinity(0, prev_affinity)  # the pages stay where they were placed
     compute = torch.cuda.current_stream(dev)
     s_h2d = torch.cuda.Stream(dev)
     s_d2h = torch.cuda.Stream(dev)
@@ -635,7 +673,8 @@ def run_e2e(args, spg, torch, dev, prepared, inputs, dist=None, world=1):
     return {"value": round(value, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall_ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "copies": "two copy streams overlapping compute (pinned host buffers)"}
+            "copies": "two copy streams overlapping compute (pinned host buffers)",
+            "host_affinity": host_affinity}
 
 
 # ------------------------------------------------------------ CPU oracle
