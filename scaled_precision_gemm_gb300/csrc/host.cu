@@ -376,14 +376,16 @@ spg_route select_route_internal(int kind, int64_t T, int64_t N, int64_t K, int e
   }
   // NVFP4 at decode-sized T (1-4 tokens): the CUDA-core GEMV (variant 4;
   // two weight rows per warp, 4 warps per CTA; no workspace) where it
-  // measured faster than the tile routes on GB300 (us, GEMV / best tile):
-  // linear_add N = 5120, K = 17408: T = 1 / 2 24.6 / 36.9, 28.7 / 36.9, but
-  // T = 3 / 4 41.0 / 36.9, 47.2 / 34.8; K = 6144: T = 3 / 4 16.4 / 22.5,
-  // 18.5 / 22.5; the 34816-wide SwiGLU 39-59 against 37-39.  Hence: N up to
-  // 16384, and T <= 2 or K <= 8192.  SPG_FORCE_VARIANT=gemv pins it, any
-  // other forced variant disables it.  Its CTAs hold the decoded activations
-  // in shared memory (34 bytes per token and 32 K elements), so K is bounded.
-  const bool gemv_pays = N <= 16384 && (T <= 2 || K <= 8192);
+  // measured faster than the tile routes on GB300 (us, GEMV / best tile,
+  // the one-CTA cluster K split where it applies): linear_add N = 5120,
+  // K = 17408: T = 1 24.6 / 24.7, T = 2 28.7 / 26.6, T = 3 / 4 41.0 / 26.6;
+  // K = 6144: T = 1-2 14.3 / 18.4, T = 3 / 4 16.4 / 18.4, 18.4 / 18.4;
+  // N = 16384, K = 17408: T = 1 55.3 / 61.4, T = 2 67.6 / 61.4; the
+  // 34816-wide SwiGLU 39-59 against 37-39.  Hence: N up to 16384, and T = 1
+  // or K <= 8192.  SPG_FORCE_VARIANT=gemv pins it, any other forced variant
+  // disables it.  Its CTAs hold the decoded activations in shared memory (34
+  // bytes per token and 32 K elements), so K is bounded.
+  const bool gemv_pays = N <= 16384 && (T == 1 || K <= 8192);
   const int64_t gemv_tt = T;  // token slots of the instance (1 to 4)
   if (kind == SPG_KIND_NVFP4 && nb == 1 && T >= 1 && T <= 4 &&
       gemv_tt * (K / 32) * 34 <= 200 * 1024 &&

@@ -105,19 +105,20 @@ def test_route_selector_forced_variants(lib, monkeypatch):
 
 def test_route_selector_gemv(lib, monkeypatch):
     """NVFP4 at T <= 4 takes the CUDA-core GEMV (variant 4: two weight rows
-    per warp, four warps per CTA, no workspace) for N up to 16384 and T <= 2
+    per warp, four warps per CTA, no workspace) for N up to 16384 and T = 1
     or K <= 8192; a forced tile variant, wider N or T > 4 does not."""
     monkeypatch.delenv("SPG_FORCE_TAIL", raising=False)
     monkeypatch.delenv("SPG_FORCE_VARIANT", raising=False)
-    for T, K in [(1, 17408), (2, 17408), (3, 6144), (4, 6144)]:
+    for T, K in [(1, 17408), (1, 6144), (2, 6144), (3, 6144), (4, 6144)]:
         for epi in ("linear", "add", "swiglu"):
             r = spg.select_route("nvfp4", T, 5120, K, epi, workspace=True)
             assert r["variant"] == 4 and r["block_n"] == 2 and r["grid"] == 640
             assert r["split_k"] == 1 and r["workspace_bytes"] == 0
             assert r["smem_bytes"] == T * (K // 32) * 34  # decoded activations
     assert spg.gemm_workspace_bytes("nvfp4", 1, 5120, 17408, "add") == 0
-    for T in (3, 4):
-        assert spg.select_route("nvfp4", T, 5120, 17408, "add")["variant"] != 4
+    for T in (2, 3, 4):
+        assert spg.select_route("nvfp4", T, 5120, 17408, "add")["variant"] == 7
+    assert spg.select_route("nvfp4", 2, 16384, 17408, "add")["variant"] != 4
     assert spg.select_route("nvfp4", 1, 34816, 5120, "swiglu")["variant"] != 4
     assert spg.select_route("fp8_rowscaled", 1, 5120, 17408, "add")["variant"] != 4
     monkeypatch.setenv("SPG_FORCE_VARIANT", "2sm_st")
