@@ -587,7 +587,10 @@ def bind_host_near_gpu(torch, dev):
     if not use:
         return {"bound": False, "pci": bus, "numa_node": node, "why": "no allowed local CPU"}
     if use != allowed:
-        os.sched_setaffinity(0, use)
+        try:
+            os.sched_setaffinity(0, use)
+        except OSError as e:
+            return {"bound": False, "pci": bus, "numa_node": node, "why": f"sched_setaffinity: {e}"}
     return {"bound": True, "pci": bus, "numa_node": node, "cpus": len(use),
             "changed": use != allowed}
 
@@ -611,7 +614,10 @@ def run_e2e(args, spg, torch, dev, prepared, inputs, dist=None, world=1):
         k.res_d = None if k.res is None else torch.empty_like(k.res)
         h2d += k.x_host.numel() * 2 + (0 if k.res_host is None else k.res_host.numel() * 2)
         d2h += k.out_host.numel() * 2
-    os.sched_setaffinity(0, prev_affinity)  # the pages stay where they were placed
+    try:
+        os.sched_setaffinity(0, prev_affinity)  # the pages stay where they were placed
+    except OSError:
+        pass
     compute = torch.cuda.current_stream(dev)
     s_h2d = torch.cuda.Stream(dev)
     s_d2h = torch.cuda.Stream(dev)
