@@ -392,9 +392,9 @@ def run_gpu(args):
                 spg.nvfp4_gemm(A, sfA, gA, Wc, sfW, gW, residual=k.res_dev, epilogue=epi,
                                out=k.out, workspace=k.ws)
             # one quantizer kernel (one CTA, or one cluster) for activations of
-            # up to 512 Ki elements, else amax + finalize + quantize (plus one
-            # memset); then the GEMM
-            k.launches = 2 if T * K <= 512 * 1024 else 4
+            # up to 512 Ki elements, else amax + quantize (plus one memset);
+            # then the GEMM
+            k.launches = 2 if T * K <= 512 * 1024 else 3
         prepared.append(k)
 
     # Warm the library (first-call set-up: shared-memory limits, device error

@@ -254,8 +254,11 @@ SPG_API spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K, co
  * against 16.9 at 4 x 17408); up to 524,288 elements one cluster of CTAs
  * (16 where the device can hold such a cluster, else 8) shares its maxima
  * through distributed shared memory and encodes in the same launch (10.8
- * against 14.9 us at 16 x 17408).  Arguments, layouts and errors as for the
- * two calls (amax_scratch: one fp32 of caller-owned scratch). */
+ * against 14.9 us at 16 x 17408).  Larger tensors take the maximum over all
+ * SMs and then the block encoder, which forms g itself (three launches with
+ * the scratch's memset, one fewer than the two calls).  Arguments, layouts
+ * and errors as for the two calls (amax_scratch: one fp32 of caller-owned
+ * scratch). */
 SPG_API spg_status spg_quantize_nvfp4_act(const void* x, int64_t rows, int64_t K, float* g,
                                           float* amax_scratch, uint8_t* codes, uint8_t* sf,
                                           spg_stream_t stream);

@@ -168,16 +168,23 @@ __global__ void nvfp4_global_finalize_kernel(const float* __restrict__ amax, flo
 // (lanes 4j .. 4j+3) for its first lane to store as one word of the blocked
 // layout.  kNvSpans steps are loaded before any is encoded.  After the data
 // the grid zeroes the scale words of the padding rows.
+// FROM_AMAX: gptr holds the tensor's maximum instead of g; every CTA forms g
+// from it (the same value everywhere) and CTA 0 stores it to *g_out, which
+// saves the global scale's separate finalize launch.
 constexpr int kNvSpans = 4;
 
+template <bool FROM_AMAX>
 __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
     const uint4* __restrict__ x, uint32_t rows, uint32_t rows_pad, uint32_t upr,
-    const float* __restrict__ gptr, uint2* __restrict__ codes, uint32_t* __restrict__ sf) {
+    const float* __restrict__ gptr, uint2* __restrict__ codes, uint32_t* __restrict__ sf,
+    float* __restrict__ g_out) {
   const uint32_t nblk = rows * upr * 4;  // host guarantees rows_pad * upr * 4 < 2^31
   const int lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t base = warp * (32 * kNvSpans);
-  const Nvfp4BlockEncoder enc(*gptr);
+  const float g = FROM_AMAX ? nvfp4_global_from_amax(*gptr) : *gptr;
+  if (FROM_AMAX && blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  const Nvfp4BlockEncoder enc(g);
   uint4 v[kNvSpans][2];
 #pragma unroll
   for (int j = 0; j < kNvSpans; ++j) {
@@ -544,10 +551,10 @@ extern "C" spg_status spg_quantize_nvfp4(const void* x, int64_t rows, int64_t K,
   if (rows_pad * upr * 4 >= (int64_t(1) << 31)) return SPG_ERR_UNSUPPORTED_SHAPE;
   const int64_t per_cta = 8 * 32 * kNvSpans;  // blocks: 8 warps x 32 lanes x kNvSpans
   const int64_t grid = (rows * upr * 4 + per_cta - 1) / per_cta;
-  quantize_nvfp4_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+  quantize_nvfp4_kernel<false><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
       static_cast<const uint4*>(x), static_cast<uint32_t>(rows), static_cast<uint32_t>(rows_pad),
       static_cast<uint32_t>(upr), g, reinterpret_cast<uint2*>(codes),
-      reinterpret_cast<uint32_t*>(sf));
+      reinterpret_cast<uint32_t*>(sf), nullptr);
   return launch_status();
 }
 
@@ -592,9 +599,22 @@ extern "C" spg_status spg_quantize_nvfp4_act(const void* x, int64_t rows, int64_
       return SPG_ERR_CUDA;
     return launch_status();
   }
-  const spg_status st = spg_nvfp4_global_scale(x, rows * K, g, amax_scratch, stream);
-  if (st != SPG_OK) return st;
-  return spg_quantize_nvfp4(x, rows, K, g, codes, sf, stream);
+  // Large tensors: the maximum over all SMs, then the block encoder, which
+  // forms g from it (three launches with the scratch's memset).
+  if (rows_pad * (K / 64) * 4 >= (int64_t(1) << 31)) return SPG_ERR_UNSUPPORTED_SHAPE;
+  const int64_t nvec = rows * K / 8;
+  if (cudaMemsetAsync(amax_scratch, 0, sizeof(float), stream) != cudaSuccess) return SPG_ERR_CUDA;
+  amax_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(static_cast<const uint4*>(x), nvec,
+                                                        amax_scratch);
+  if (launch_status() != SPG_OK) return SPG_ERR_CUDA;
+  const int64_t upr = K / 64;
+  const int64_t per_cta = 8 * 32 * kNvSpans;
+  const int64_t grid = (rows * upr * 4 + per_cta - 1) / per_cta;
+  quantize_nvfp4_kernel<true><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), static_cast<uint32_t>(rows), static_cast<uint32_t>(rows_pad),
+      static_cast<uint32_t>(upr), amax_scratch, reinterpret_cast<uint2*>(codes),
+      reinterpret_cast<uint32_t*>(sf), g);
+  return launch_status();
 }
 
 extern "C" size_t spg_nvfp4_sf_bytes(int64_t rows, int64_t K) {
