@@ -91,3 +91,48 @@ def test_route_invariants(kind, epi):
                     assert need >= r["workspace_bytes"], tag
                 else:
                     assert need == r["workspace_bytes"], tag
+
+
+def recv_bytes(bn, cw, s):
+    """Partial sums one CTA of a cluster K split receives: per owned chunk,
+    32-column sub-block, source piece and TMEM lane quarter a 4 KB block."""
+    return -(-(bn // cw) // s) * (cw // 32) * s * 4 * 4096
+
+
+@pytest.mark.parametrize("pin", [None, "1sm_cks", "1sm256_cks", "swap"])
+@pytest.mark.parametrize("epi", ["linear", "add", "swiglu"])
+def test_cluster_split_plans(pin, epi, monkeypatch):
+    """Every K split inside clusters (variants 7 and 8, default or pinned):
+    one wave with one piece per CTA (pair), 2-4 pieces, none empty, clusters
+    of at most 8 CTAs, and the partial sums each CTA receives fit its
+    operand ring, which is where they land."""
+    if pin:
+        monkeypatch.setenv("SPG_FORCE_VARIANT", pin)
+    seen = 0
+    for T, N, K in SHAPES:
+        for kind in ("nvfp4", "fp8_rowscaled"):
+            if kind == "nvfp4" and K % 256:
+                continue
+            r = spg.select_route(kind, T, N, K, epi)
+            tag = (pin, kind, epi, T, N, K, r)
+            if r["variant"] == 7 and kind == "nvfp4":
+                s, n, bn = r["split_k"], nkb(kind, K), r["block_n"]
+                kbps = -(-n // s)
+                tiles = -(-T // 128) * -(-N // bn)
+                assert 2 <= s <= 4 and kbps >= 8 and (s - 1) * kbps < n, tag
+                assert r["grid"] == tiles * s <= 2 * PAIRS, tag
+                stage = 128 * 128 + bn * 128 + 2048 + (bn // 128) * 2048
+                assert r["stages"] * stage + 1024 + 4 * 2 * 2048 + 256 <= SMEM_MAX, tag
+                cw = 64 if epi == "swiglu" else 32
+                assert recv_bytes(bn, cw, s) <= r["stages"] * stage, tag
+                seen += 1
+            elif r["variant"] == 8:
+                s, n, bn = r["split_k"], nkb(kind, K), r["block_n"]
+                assert kind != "nvfp4" and epi != "swiglu" and r["swap_ab"] == 1, tag
+                assert 2 <= s <= 4 and 2 * s <= 8 and (s - 1) * (-(-n // s)) < n, tag
+                assert r["tiles"] * s <= PAIRS and r["grid"] == 2 * r["tiles"] * s, tag
+                stage = 128 * 128 + bn // 2 * 128
+                assert recv_bytes(bn, 32, s) <= r["stages"] * stage, tag
+                seen += 1
+    if pin != "swap" or epi != "swiglu":
+        assert seen > 0
